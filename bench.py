@@ -1,0 +1,515 @@
+#!/usr/bin/env python3
+"""Sparse decode-attention benchmark on GB300: tokens/s and effective KV GB/s.
+
+One step = one decode token for every request of the batch through the hot
+path: dsa_build_index (mask -> kept rows) + dsa_decode_sparse (gather the kept
+K/V rows, online softmax, split-KV merge).  Inputs are synthetic (seeded),
+shaped like the LlamaGen-XL-like workload by default (--config 2); other
+workloads: --config 3|4|5.  The dense causal decode of the same batch and the
+attention-mass pass are timed beside it.
+
+Timing: W eager warm-up steps, then K steps captured in one CUDA graph and
+replayed once between CUDA events (per-step = elapsed / K).  Consecutive steps
+rotate through R copies of the KV pool, R chosen so that the rows touched by R
+steps exceed 4x the L2, so every step streams its rows from HBM.  nvidia-smi
+samples clocks over a busy window that encloses the timed replay.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config C]
+    python bench.py --impl reference ...   # the fp64 CPU oracle, timed
+Multi-GPU (torchrun): every rank runs its own batch (weak scaling, replicas
+only: the path has no exchange step); the timed region is bracketed by
+barriers and the max over ranks is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import io
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from kv_cache_serving_gb300 import dsa  # noqa: E402
+from kv_cache_serving_gb300 import workloads as wl  # noqa: E402
+from kv_cache_serving_gb300.session import DecodeBatch  # noqa: E402
+
+METRIC = "sparse decode-attn tokens/s and effective KV GB/s (% of GB300 HBM peak)"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--config", type=int, default=2, choices=[2, 3, 4, 5])
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--cpu-seconds", type=float, default=12.0,
+                   help="CPU time budget of the oracle baseline sample")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--busy-seconds", type=float, default=1.5,
+                   help="GPU busy time around the timed region for clock sampling")
+    return p.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# environment
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    return rank, world, local
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+            return v, "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.seek(0)
+        rows = [r for r in csv.reader(io.StringIO(self.file.read())) if len(r) >= 9]
+        self.file.close()
+        os.unlink(self.file.name)
+        if not rows:
+            return None
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4)
+                          if r[5 + k].strip().lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes
+# ---------------------------------------------------------------------------
+
+def step_bytes(w, kept_idx, kept_cnt):
+    """Bytes a sparse step must move at minimum, and the dense decode's."""
+    B, Hq, Hkv, D = w["batch"], w["hq"], w["hkv"], w["head_dim"]
+    elt = 2 if w["dtype"] == "bf16" else 4
+    q_elt = 2 if w["dtype"] == "bf16" else 4
+    L = w["seq_len"].astype(np.int64)
+    rows = int(kept_cnt.sum())
+    pages = 0
+    for b in range(B):
+        touched = set()
+        for hk in range(Hkv):
+            touched.update((kept_idx[b, hk, :kept_cnt[b, hk]] >> 4).tolist())
+        pages += len(touched)
+    q_b = B * Hq * D * q_elt
+    out_b = B * Hq * D * 4 + B * Hq * 4
+    sparse_decode = rows * 2 * D * elt + q_b + out_b + 4 * rows + 4 * pages + 4 * B * Hkv
+    index = (B * Hkv * w["mask_words"] * 4 + 3 * 4 * B) + 4 * rows + 4 * B * Hkv
+    dense_rows = int(L.sum()) * Hkv
+    dense = dense_rows * 2 * D * elt + q_b + out_b + 4 * int(((L + 15) // 16).sum())
+    return dict(kv=rows * 2 * D * elt, sparse_decode=sparse_decode, index=index,
+                step=sparse_decode + index, dense=dense, rows=rows, dense_rows=dense_rows)
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+
+def graph_of(fn, steps, stream):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for k in range(steps):
+            fn(k)
+    return g
+
+
+def time_graph(g, stream):
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    g.replay()
+    e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1) / 1e3  # seconds
+
+
+def busy(g, seconds, per_replay):
+    n = max(1, int(seconds / max(per_replay, 1e-6)))
+    for _ in range(n):
+        g.replay()
+    torch.cuda.synchronize()
+
+
+def cpu_oracle_sample(w_cpu, seconds, sparse=True):
+    """Time the fp64 oracle on a bounded random sample of (request, head) pairs;
+    returns (tokens/s equivalent for the full step, pairs, seconds, threads)."""
+    import oracle
+    B, Hq = w_cpu["batch"], w_cpu["hq"]
+    rng = np.random.default_rng(0)
+    allp = [(b, h) for b in range(B) for h in range(Hq)]
+    order = rng.permutation(len(allp))
+    threads = oracle.default_threads()
+    n0 = min(len(allp), max(threads, 16))
+    t = time.perf_counter()
+    oracle.decode(w_cpu, sparse=sparse, bh=[allp[i] for i in order[:n0]], nthreads=threads)
+    t0 = time.perf_counter() - t
+    n = int(min(len(allp), max(n0, n0 * seconds / max(t0, 1e-6))))
+    t = time.perf_counter()
+    oracle.decode(w_cpu, sparse=sparse, bh=[allp[i] for i in order[:n]], nthreads=threads)
+    dt = time.perf_counter() - t
+    step_s = dt * len(allp) / n
+    return B / step_s, n, dt, threads
+
+
+def to_cpu_workload(w, bt):
+    c = dict(w)
+    c["q"] = bt.q.cpu()
+    c["k_pages"] = bt.k_pages.cpu()
+    c["v_pages"] = bt.v_pages.cpu()
+    c["keep_mask"] = bt.keep_mask.cpu().numpy().view(np.uint32)
+    return c
+
+
+def run_ours(args):
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=device)
+    cfg = wl.CONFIGS[args.config]
+    w = wl.generate(cfg, seed=cfg.seed + 1000 * rank, device=str(device))
+    bt = DecodeBatch.from_workload(w, device=device)
+    torch.cuda.synchronize()
+    # one non-default stream for everything (graph capture needs one)
+    stream = torch.cuda.Stream(device)
+    torch.cuda.set_stream(stream)
+
+    mass_ms = None
+    if cfg.mask == "top_mass":
+        # per-head masks from this batch's measured attention mass (our kernel)
+        mass, om = bt.attention_mass(r_local=2, r_diag=2)
+        mask = wl.top_mass_keep_mask(om.cpu().numpy(), w["window"], w["hkv"], w["mask_words"],
+                                     band=cfg.band, frac=cfg.top_mass_frac)
+        bt.set_keep_mask(mask)
+        w["keep_mask"] = mask
+    bt.build_index()
+    torch.cuda.synchronize()
+    bt.check("build_index")
+    kept_idx = bt.kept_idx.cpu().numpy()
+    kept_cnt = bt.kept_cnt.cpu().numpy()
+    by = step_bytes(w, kept_idx, kept_cnt)
+
+    # KV replicas so that consecutive steps never find their rows in L2
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    pool = bt.k_pages.numel() * bt.k_pages.element_size() * 2
+    free, _ = torch.cuda.mem_get_info(device)
+    R = max(1, math.ceil(4 * l2 / max(by["kv"], 1)))
+    R = int(max(1, min(R, 64, (0.5 * free) // pool)))
+    pools = [(bt.k_pages, bt.v_pages)] + [(bt.k_pages.clone(), bt.v_pages.clone())
+                                          for _ in range(R - 1)]
+    d = bt.dims
+    K, W = args.steps, args.warmup
+
+    def sparse_step(k):
+        kp, vp = pools[k % R]
+        dsa.dsa_build_index(d, bt.seq_len, bt.prompt_len, bt.window, bt.keep_mask, bt.kept_idx,
+                            bt.kept_cnt, bt.ws, stream)
+        dsa.dsa_decode_sparse(d, bt.q, kp, vp, bt.page_table, bt.seq_len, bt.kept_idx,
+                              bt.kept_cnt, bt.scale, bt.out, bt.lse, bt.ws, stream)
+
+    def decode_only(k):
+        kp, vp = pools[k % R]
+        dsa.dsa_decode_sparse(d, bt.q, kp, vp, bt.page_table, bt.seq_len, bt.kept_idx,
+                              bt.kept_cnt, bt.scale, bt.out, bt.lse, bt.ws, stream)
+
+    out_dense = torch.empty_like(bt.out)
+    lse_dense = torch.empty_like(bt.lse)
+
+    def dense_step(k):
+        kp, vp = pools[k % R]
+        dsa.dsa_decode_dense(d, bt.q, kp, vp, bt.page_table, bt.seq_len, bt.scale, out_dense,
+                             lse_dense, bt.ws, stream)
+
+    # warm-up: W eager steps of each kind
+    for k in range(W):
+        sparse_step(k)
+        dense_step(k)
+    torch.cuda.synchronize()
+    bt.check("warm-up")
+
+    g_sparse = graph_of(sparse_step, K, stream)
+    g_dec = graph_of(decode_only, K, stream)
+    g_dense = graph_of(dense_step, K, stream)
+    for g in (g_sparse, g_dec, g_dense):
+        g.replay()  # graph upload + one more untimed pass
+    torch.cuda.synchronize()
+
+    probe = time_graph(g_sparse, stream)
+    sampler = ClockSampler(local)
+    sampler.start()
+    busy(g_sparse, args.busy_seconds, probe)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_sparse = time_graph(g_sparse, stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    busy(g_sparse, args.busy_seconds / 3, probe)
+    clocks = sampler.stop()
+
+    t_dec = time_graph(g_dec, stream)
+    t_dense = time_graph(g_dense, stream)
+    torch.cuda.synchronize()
+    bt.check("timed region")
+
+    if world > 1:
+        t = torch.tensor([t_sparse, t_dec, t_dense], device=device, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        t_sparse, t_dec, t_dense = t.tolist()
+
+    # end-to-end through the API with host buffers: inputs H2D, result D2H, every step
+    pin = lambda t: t.cpu().pin_memory()  # noqa: E731
+    host_in = [(pin(bt.q), bt.q), (pin(bt.seq_len), bt.seq_len),
+               (pin(bt.prompt_len), bt.prompt_len), (pin(bt.window), bt.window),
+               (pin(bt.keep_mask), bt.keep_mask), (pin(bt.page_table), bt.page_table)]
+    host_out = [(bt.out, torch.empty(bt.out.shape, dtype=bt.out.dtype).pin_memory()),
+                (bt.lse, torch.empty(bt.lse.shape, dtype=bt.lse.dtype).pin_memory())]
+    h2d = sum(h.numel() * h.element_size() for h, _ in host_in)
+    d2h = sum(h.numel() * h.element_size() for _, h in host_out)
+
+    def e2e_step(k):
+        for h, dv in host_in:
+            dv.copy_(h, non_blocking=True)
+        sparse_step(k)
+        for dv, h in host_out:
+            h.copy_(dv, non_blocking=True)
+
+    for k in range(min(W, 3)):
+        e2e_step(k)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for k in range(K):
+        e2e_step(k)
+    e1.record(stream)
+    e1.synchronize()
+    t_e2e = e0.elapsed_time(e1) / 1e3
+    if world > 1:
+        t = torch.tensor([t_e2e], device=device, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        t_e2e = t.item()
+
+    # attention-mass pass (the characterisation kernel), timed alone
+    if K > 0:
+        m_out = torch.empty((w["batch"], w["hq"], 4), dtype=torch.float32, device=device)
+        om_out = torch.empty((w["batch"], w["hq"], w["max_window"] + 1), dtype=torch.float32,
+                             device=device)
+
+        def mass_step(k):
+            kp, _ = pools[k % R]
+            dsa.dsa_attention_mass(d, bt.q, kp, bt.page_table, bt.seq_len, bt.prompt_len,
+                                   bt.window, bt.grid_w, 2, 2, bt.scale, m_out, om_out, bt.ws,
+                                   stream)
+        for k in range(3):
+            mass_step(k)
+        g_mass = graph_of(mass_step, min(K, 50), stream)
+        g_mass.replay()
+        mass_ms = 1e3 * time_graph(g_mass, stream) / min(K, 50)
+
+    B = w["batch"]
+    ms_step = 1e3 * t_sparse / K
+    tokens = world * B / (t_sparse / K)
+    peak, peak_src = hbm_peak()
+    dec_s = t_dec / K
+    achieved = by["sparse_decode"] / dec_s / 1e9
+    _, _, launches_dec = dsa.dsa_decode_plan(d, True)
+    _, _, launches_dense = dsa.dsa_decode_plan(d, False)
+    chunk, nch, _ = dsa.dsa_decode_plan(d, True)
+
+    result = {
+        "metric": METRIC,
+        "value": tokens,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "storage_dtype": w["dtype"],
+        "data": "synthetic",
+        "config": {
+            "workload": cfg.name, "batch": B, "hq": w["hq"], "hkv": w["hkv"],
+            "head_dim": w["head_dim"], "page_size": 16, "mask": cfg.mask,
+            "seq_len_mean": float(np.mean(w["seq_len"])),
+            "kept_rows_per_head_mean": by["rows"] / (B * w["hkv"]),
+            "l2": f"inputs larger than L2: {R} rotating KV pool copies, "
+                  f"{R * by['kv'] / 1e6:.0f} MB of kept rows per rotation (L2 {l2 / 1e6:.0f} MB)",
+            "parallelism": f"replicas x{world}",
+            "decode_chunk_rows": chunk, "decode_chunks_max": nch,
+        },
+        "effective_kv_gbs": by["step"] / (t_sparse / K) / 1e9,
+        "pct_of_hbm_peak": 100.0 * by["step"] / (t_sparse / K) / 1e9 / peak,
+        "step_bytes": by["step"],
+        "roofline": {
+            "kernel": "dsa_decode_sparse (decode + LSE merge kernels)",
+            "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak, "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
+            if peak_src == "measured" else "fallback 6.8 TB/s",
+            "traffic": None,
+            "bytes_per_launch": by["sparse_decode"], "launch_us": 1e6 * dec_s,
+        },
+        "sparse_vs_dense": {
+            "dense_ms_per_step": 1e3 * t_dense / K,
+            "dense_tokens_per_s": world * B / (t_dense / K),
+            "speedup": t_dense / t_sparse,
+            "kept_fraction": by["rows"] / by["dense_rows"],
+            "dense_bytes": by["dense"],
+            "dense_gbs": by["dense"] / (t_dense / K) / 1e9,
+        },
+        "attention_mass_ms": mass_ms,
+        "e2e": {"value": world * B / (t_e2e / K), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": 1e3 * t_e2e / K},
+        "gpu_launches": K * (1 + launches_dec),
+        "clocks": clocks,
+    }
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        w_cpu = to_cpu_workload(w, bt)
+        tps, n, dt, threads = cpu_oracle_sample(w_cpu, args.cpu_seconds)
+        result["cpu_baseline"] = {
+            "value": tps, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"fp64 C oracle, sparse decode of {n} of {B * w['hq']} (request, head) "
+                      f"pairs in {dt:.1f} s, scaled to the full step"}
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# the reference arm: the fp64 CPU oracle, timed as it stands
+# ---------------------------------------------------------------------------
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    cfg = wl.CONFIGS[args.config]
+    w = wl.generate(cfg)
+    if cfg.mask == "top_mass":
+        # the same selection rule as the GPU arm, applied to the oracle's mass
+        _, om = oracle.mass(w)
+        om = om.reshape(w["batch"], w["hq"], -1)
+        w["keep_mask"] = wl.top_mass_keep_mask(om, w["window"], w["hkv"], w["mask_words"],
+                                               band=cfg.band, frac=cfg.top_mass_frac)
+    B, Hq = w["batch"], w["hq"]
+    allp = [(b, h) for b in range(B) for h in range(Hq)]
+    rng = np.random.default_rng(0)
+    threads = oracle.default_threads()
+    budget = max(0.05, 90.0 / (args.steps + args.warmup))
+    n = min(len(allp), max(threads, 16))
+    t = time.perf_counter()
+    oracle.decode(w, sparse=True, bh=[allp[i] for i in rng.permutation(len(allp))[:n]])
+    per_pair = (time.perf_counter() - t) / n
+    n = int(min(len(allp), max(1, budget / per_pair)))
+    for k in range(args.warmup):
+        sel = [allp[i] for i in rng.permutation(len(allp))[:n]]
+        oracle.decode(w, sparse=True, bh=sel, nthreads=threads)
+    total = 0.0
+    for k in range(args.steps):
+        sel = [allp[i] for i in rng.permutation(len(allp))[:n]]
+        t = time.perf_counter()
+        oracle.decode(w, sparse=True, bh=sel, nthreads=threads)
+        total += time.perf_counter() - t
+    step_s = total / args.steps * len(allp) / n
+    tps = B / step_s
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": tps, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * step_s, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": cfg.name, "batch": B, "hq": Hq, "hkv": w["hkv"],
+                   "head_dim": w["head_dim"]},
+        "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": f"each step: fp64 C oracle sparse decode of {n} of {len(allp)} "
+                                   f"(request, head) pairs, scaled to the full step"},
+        "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

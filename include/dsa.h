@@ -1,0 +1,212 @@
+/*
+ * dsa.h -- C ABI of libdsa: diagonal-aware sparse decode attention over a paged
+ * KV cache, for NVIDIA GB300 (sm_103a).
+ *
+ * The operation is the decode step of the method on the page "Understanding and
+ * Exploiting Diagonal Attention Sparsity in Autoregressive Image Generation":
+ * for each request, one query token attends only to the prompt-prefix rows of
+ * the KV cache and to the rows of a recent window W whose offset is kept by a
+ * per-head keep mask (arXiv abstract: "selectively skips KV entries along the
+ * diagonal attention direction within a recent window"; paper-daily summary,
+ * section 核心公式 / core formula: Attention = softmax(QK^T/sqrt(d) (.) M) V,
+ * with the band mask M_ij = 1 iff |i-j| <= B and j >= i-W as one instance).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * Shapes (row-major, element counts):
+ *   q            [batch][hq][head_dim]                 dtype dims->q_dtype
+ *   k_pages      [num_pages][16][hkv][head_dim]        dtype dims->kv_dtype
+ *   v_pages      [num_pages][16][hkv][head_dim]        dtype dims->kv_dtype
+ *   page_table   [batch][max_pages_per_req] int32: row j of request b lives in
+ *                page page_table[b][j / 16], slot j % 16.  Entries past
+ *                ceil(seq_len[b] / 16) are never read.
+ *   seq_len      [batch] int32, L_b >= 1 rows already in the cache; the query
+ *                is token i = L_b - 1, whose own K/V row is row i.
+ *   prompt_len   [batch] int32, P_b >= 0 prompt rows (always kept).
+ *   window       [batch] int32, 0 <= W_b <= max_window.
+ *   keep_mask    [batch][hkv][mask_words] uint32: bit (o-1) of the little-endian
+ *                bit string keeps window offset o = i - j, 1 <= o <= W_b.
+ * Query head h reads KV head h / (hq / hkv) (grouped-query attention).
+ * The kept set of (b, kv head hk) is
+ *   K(b,hk) = { j < min(P_b, L_b) } U { i } U { i-o : 1 <= o <= W_b, bit o-1 set, i-o >= P_b }
+ * in ascending j.  Masked rows are not read and do not enter the softmax.
+ *
+ * Memory: every pointer is a DEVICE pointer owned by the caller; the library
+ * allocates nothing and keeps no pointer after a call returns.  `ws` is a
+ * caller-owned device workspace of dsa_workspace_size(dims) bytes, aligned to
+ * 256 bytes, zero-filled once before its first use (cudaMemsetAsync), and not
+ * shared by calls that may run concurrently.
+ *
+ * Ordering: every call is asynchronous on `stream` (a cudaStream_t; NULL is the
+ * legacy default stream) and returns once its kernels are enqueued.
+ *
+ * Errors: calls return a dsa_status and never throw or abort.  Shapes, dtypes,
+ * sizes and null pointers are checked on the host before anything is launched
+ * (DSA_ERR_INVALID_ARG / DSA_ERR_UNSUPPORTED; nothing is written).  Launch
+ * failures give DSA_ERR_CUDA.  Per-request values live on the device, so the
+ * kernels check them there: an invalid seq_len / prompt_len / window / kept
+ * count, a kept index outside 0..i, or a page id outside 0..num_pages-1 sets
+ * the workspace's error word (first error wins), no memory outside the
+ * caller's buffers is touched, and the outputs of the affected request are
+ * unspecified (NaN where the request itself is invalid).
+ * dsa_get_device_error() reads the word.
+ */
+#ifndef DSA_H_
+#define DSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DSA_OK = 0,
+  DSA_ERR_INVALID_ARG = 1, /* null pointer, bad size or inconsistent dims      */
+  DSA_ERR_UNSUPPORTED = 2, /* dtype, head_dim, page size or group not built    */
+  DSA_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed             */
+  DSA_ERR_DEVICE = 4,      /* the kernels flagged invalid per-request data     */
+  DSA_ERR_TIMEOUT = 5      /* a bounded on-device wait gave up                 */
+} dsa_status;
+
+typedef enum { DSA_F32 = 0, DSA_BF16 = 1 } dsa_dtype;
+
+/* Device error codes stored in the workspace error word. */
+enum {
+  DSA_DEV_OK = 0,
+  DSA_DEV_BAD_SEQ_LEN = 1,  /* seq_len < 1 or > max_pages_per_req * 16     */
+  DSA_DEV_BAD_PROMPT = 2,   /* prompt_len < 0                              */
+  DSA_DEV_BAD_WINDOW = 3,   /* window < 0 or > max_window                  */
+  DSA_DEV_BAD_PAGE = 4,     /* page id outside 0..num_pages-1              */
+  DSA_DEV_BAD_INDEX = 5,    /* kept index outside 0..seq_len-1             */
+  DSA_DEV_BAD_COUNT = 6,    /* kept count < 1 or > max_kept                */
+  DSA_DEV_TIMEOUT = 7,      /* a bounded wait for an async copy gave up    */
+  DSA_DEV_BAD_GRID_W = 8    /* grid width < 1 (attention mass)             */
+};
+
+/* Problem sizes, shared by all calls on one KV cache. */
+typedef struct {
+  int32_t batch;             /* requests B >= 0                               */
+  int32_t hq;                /* query heads                                   */
+  int32_t hkv;               /* KV heads; hq % hkv == 0, hq/hkv in {1,2,4,8}   */
+  int32_t head_dim;          /* d in {64, 128}                                */
+  int32_t page_size;         /* rows per page; must be 16                     */
+  int32_t num_pages;         /* pages in k_pages / v_pages                    */
+  int32_t max_pages_per_req; /* columns of page_table                         */
+  int32_t max_window;        /* largest W_b allowed                           */
+  int32_t mask_words;        /* uint32 words per keep mask, >= ceil(max_window/32) */
+  int32_t max_kept;          /* capacity of each kept_idx list, >= 1          */
+  int32_t q_dtype;           /* dsa_dtype of q                                */
+  int32_t kv_dtype;          /* dsa_dtype of k_pages and v_pages              */
+} dsa_dims;
+
+/* Library version, (major << 16) | minor. */
+int32_t dsa_version(void);
+
+/* Human-readable name of a status; never NULL. */
+const char* dsa_status_string(dsa_status status);
+
+/* Bytes of device workspace every call on `dims` needs (0 if dims is invalid).
+ * Depends on dims only. */
+size_t dsa_workspace_size(const dsa_dims* dims);
+
+/*
+ * dsa_build_index -- mask -> kept-row list (index compaction).
+ * Writes, for every (b, hk), kept_cnt[b][hk] = |K(b,hk)| and the ascending
+ * logical rows of K(b,hk) into kept_idx[b][hk][0 .. cnt-1]; entries past cnt are
+ * unspecified.  Follows the band/window formula of the paper-daily summary
+ * (section 核心公式) with its worked example (section 具体技术细节示例: for
+ * N=8, W=4, B=2, query 6 the kept keys are 4..7, or 4..6 once decode is causal),
+ * plus the prompt prefix the abstract reports attention concentrates on.
+ *   seq_len, prompt_len, window  [batch] int32 (device)
+ *   keep_mask                    [batch][hkv][mask_words] uint32 (device)
+ *   kept_idx  (out)              [batch][hkv][max_kept] int32 (device)
+ *   kept_cnt  (out)              [batch][hkv] int32 (device)
+ * A count above max_kept sets DSA_DEV_BAD_COUNT and stores count 0.
+ */
+dsa_status dsa_build_index(const dsa_dims* dims, const int32_t* seq_len,
+                           const int32_t* prompt_len, const int32_t* window,
+                           const uint32_t* keep_mask, int32_t* kept_idx, int32_t* kept_cnt,
+                           void* ws, void* stream);
+
+/*
+ * dsa_decode_sparse -- decode attention over the kept rows only.
+ * out[b][h][:] = sum_{j in K(b,hk)} a_j v_j with a = softmax_j(scale * q_bh . k_j),
+ * lse[b][h]    = ln sum_{j in K(b,hk)} exp(scale * q_bh . k_j)      (natural log),
+ * for hk = h / (hq/hkv) -- the masked softmax of the summary's core formula,
+ * masked entries removed.  Only the kept K/V rows are read.  fp32 accumulation.
+ *   q                 [batch][hq][head_dim] (q_dtype)
+ *   k_pages, v_pages  [num_pages][16][hkv][head_dim] (kv_dtype)
+ *   page_table        [batch][max_pages_per_req] int32
+ *   seq_len           [batch] int32
+ *   kept_idx, kept_cnt  as written by dsa_build_index
+ *   scale             softmax scale, normally 1/sqrt(head_dim)
+ *   out   (out)       [batch][hq][head_dim] float32
+ *   lse   (out)       [batch][hq] float32, or NULL
+ */
+dsa_status dsa_decode_sparse(const dsa_dims* dims, const void* q, const void* k_pages,
+                             const void* v_pages, const int32_t* page_table,
+                             const int32_t* seq_len, const int32_t* kept_idx,
+                             const int32_t* kept_cnt, float scale, float* out, float* lse,
+                             void* ws, void* stream);
+
+/*
+ * dsa_decode_dense -- the dense causal baseline: the same as dsa_decode_sparse
+ * with K(b,hk) = {0 .. L_b - 1} (the T_dense of the summary's speedup
+ * T_dense / T_sparse, section 核心公式).  Arguments as above.
+ */
+dsa_status dsa_decode_dense(const dsa_dims* dims, const void* q, const void* k_pages,
+                            const void* v_pages, const int32_t* page_table,
+                            const int32_t* seq_len, float scale, float* out, float* lse,
+                            void* ws, void* stream);
+
+/*
+ * dsa_attention_mass -- where the dense decode softmax puts its mass, per
+ * (request, query head): the characterisation behind the method (abstract:
+ * attention concentrates on prompt and local tokens, with a diagonal pattern
+ * from the spatial locality of visual tokens; summary, section 技术方法详解:
+ * raster order makes spatial neighbours sit at offsets k*w +- r).
+ * With a_j the dense causal softmax weights of query i = L_b - 1 and o = i - j:
+ *   mass[b][h][0]  prompt    sum of a_j over j < P_b
+ *   mass[b][h][1]  local     j >= P_b and o <= r_local
+ *   mass[b][h][2]  diagonal  j >= P_b, r_local < o <= W_b, |o - k*w_b| <= r_diag for a k >= 1
+ *   mass[b][h][3]  other     every remaining row
+ *   offset_mass[b][h][o] = a_{i-o} for 0 <= o <= min(W_b, i), else 0;
+ *                          [batch][hq][max_window+1] float32, or NULL.
+ *   grid_w   [batch] int32, image grid width w_b >= 1 (row stride in tokens).
+ *   prompt_len, window as above; r_local, r_diag >= 0.
+ * Only K rows are read (one pass).
+ */
+dsa_status dsa_attention_mass(const dsa_dims* dims, const void* q, const void* k_pages,
+                              const int32_t* page_table, const int32_t* seq_len,
+                              const int32_t* prompt_len, const int32_t* window,
+                              const int32_t* grid_w, int32_t r_local, int32_t r_diag,
+                              float scale, float* mass, float* offset_mass, void* ws,
+                              void* stream);
+
+/*
+ * dsa_decode_plan -- how dsa_decode_sparse (sparse != 0) or dsa_decode_dense
+ * (sparse == 0) will split its work on the CURRENT device: rows per CTA
+ * (*chunk), CTAs per (request, kv head) at most (*num_chunks), and kernel
+ * launches per call (*launches).  Host-only; any output pointer may be NULL.
+ */
+dsa_status dsa_decode_plan(const dsa_dims* dims, int32_t sparse, int32_t* chunk,
+                           int32_t* num_chunks, int32_t* launches);
+
+/*
+ * Waits for `stream`, then reads the workspace error word into *code_out (one of
+ * DSA_DEV_*).  Returns DSA_OK when the word is 0, DSA_ERR_TIMEOUT when it is
+ * DSA_DEV_TIMEOUT, DSA_ERR_DEVICE for any other code, DSA_ERR_CUDA if the copy
+ * fails.  Synchronising.
+ */
+dsa_status dsa_get_device_error(const void* ws, void* stream, int32_t* code_out);
+
+/* Clears the workspace error word (asynchronous on `stream`). */
+dsa_status dsa_clear_device_error(void* ws, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_H_ */

@@ -1,0 +1,207 @@
+// common.cuh -- device helpers shared by the libdsa kernels (sm_103a).
+//
+// Row gathers use the Blackwell bulk-copy engine: one lane issues a
+// cp.async.bulk of a whole K or V row (head_dim elements, 128-512 bytes,
+// 16-byte aligned) from global memory into shared memory, completing on an
+// mbarrier that carries the expected byte count.  Waits on mbarriers are
+// bounded: after kWaitLimitNs a kernel records DSA_DEV_TIMEOUT and stops.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "dsa.h"
+
+namespace dsa {
+
+constexpr int kPage = 16;
+constexpr uint64_t kWaitLimitNs = 500ull * 1000 * 1000;  // give up on a copy after 0.5 s
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Workspace: [0, 256) header (error word at offset 0), then per-call partials.
+constexpr size_t kWsHeader = 256;
+
+__device__ __forceinline__ void set_error(int32_t* err, int32_t code) {
+  atomicCAS(err, 0, code);
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+
+// Makes mbarrier initialisation visible to the async (bulk-copy) proxy.
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait for phase `parity` of `bar` to complete: false after kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (;;) {
+#pragma unroll 1
+    for (int it = 0; it < 64; ++it)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// Orders this thread's generic-proxy shared-memory accesses before later
+// async-proxy (bulk copy) writes to the same shared memory.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// One bulk copy global -> shared; `bytes` and both addresses are multiples of 16.
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes,
+                                              uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// element loads: N consecutive elements -> fp32 registers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
+
+struct bf16_t {
+  uint16_t bits;
+};
+
+template <typename T, int N>
+struct Vec;
+
+template <>
+struct Vec<float, 2> {
+  __device__ __forceinline__ static void load(const float* p, float* o) {
+    float2 v = *reinterpret_cast<const float2*>(p);
+    o[0] = v.x;
+    o[1] = v.y;
+  }
+};
+template <>
+struct Vec<float, 4> {
+  __device__ __forceinline__ static void load(const float* p, float* o) {
+    float4 v = *reinterpret_cast<const float4*>(p);
+    o[0] = v.x;
+    o[1] = v.y;
+    o[2] = v.z;
+    o[3] = v.w;
+  }
+};
+template <>
+struct Vec<bf16_t, 2> {
+  __device__ __forceinline__ static void load(const bf16_t* p, float* o) {
+    uint32_t v = *reinterpret_cast<const uint32_t*>(p);
+    o[0] = bf16_lo(v);
+    o[1] = bf16_hi(v);
+  }
+};
+template <>
+struct Vec<bf16_t, 4> {
+  __device__ __forceinline__ static void load(const bf16_t* p, float* o) {
+    uint2 v = *reinterpret_cast<const uint2*>(p);
+    o[0] = bf16_lo(v.x);
+    o[1] = bf16_hi(v.x);
+    o[2] = bf16_lo(v.y);
+    o[3] = bf16_hi(v.y);
+  }
+};
+
+// q[DPL] of one head from global memory, either dtype, scaled.
+template <int DPL>
+__device__ __forceinline__ void load_q(const void* q, bool q_bf16, size_t elem, float mul,
+                                       float* o) {
+  if (q_bf16)
+    Vec<bf16_t, DPL>::load(reinterpret_cast<const bf16_t*>(q) + elem, o);
+  else
+    Vec<float, DPL>::load(reinterpret_cast<const float*>(q) + elem, o);
+#pragma unroll
+  for (int e = 0; e < DPL; ++e) o[e] *= mul;
+}
+
+// ---------------------------------------------------------------------------
+// warp reductions
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, off));
+  return x;
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+  return x;
+}
+
+// Reduce-scatter of T per-lane partial sums across the 32 lanes of a warp:
+// on return, lane l holds the full warp sum of v[row] for row = l >> (5 - log2 T)
+// (each row's sum is replicated on 32/T lanes).  Each halving step sends half
+// of the remaining values to the partner lane and keeps the other half.
+template <int T>
+__device__ __forceinline__ float reduce_scatter(float (&v)[T], int lane) {
+  static_assert(T == 8 || T == 16 || T == 32, "tile rows");
+#pragma unroll
+  for (int n = T, off = 16; n > 1; n >>= 1, off >>= 1) {
+    const bool hi = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) {
+      const float lo_v = v[i], hi_v = v[i + n / 2];
+      const float send = hi ? lo_v : hi_v;
+      const float keep = hi ? hi_v : lo_v;
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+    }
+  }
+  float s = v[0];
+#pragma unroll
+  for (int off = 32 / T / 2; off >= 1; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+  return s;
+}
+
+template <int T>
+struct RowMap {
+  static constexpr int kShift = (T == 32) ? 0 : (T == 16 ? 1 : 2);
+  __device__ __forceinline__ static int row(int lane) { return lane >> kShift; }
+  __device__ __forceinline__ static bool owner(int lane) {
+    return (lane & ((1 << kShift) - 1)) == 0;
+  }
+};
+
+}  // namespace dsa

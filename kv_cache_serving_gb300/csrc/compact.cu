@@ -1,0 +1,75 @@
+// compact.cu -- keep mask -> ascending kept-row list (index compaction).
+//
+// The kept set of the decode query i = L-1 of request b, kv head hk is every
+// prompt row j < P, the query row i, and every window row i-o (1 <= o <= W)
+// whose mask bit o-1 is set: the band/window mask of "Understanding and
+// Exploiting Diagonal Attention Sparsity in Autoregressive Image Generation"
+// (paper-daily summary, section 核心公式, and its worked example, section
+// 具体技术细节示例), read causally, plus the prompt prefix the arXiv abstract
+// reports attention concentrates on.
+//
+// One warp per (b, hk).  Prompt rows are written as a plain range; window rows
+// are scanned 32 at a time in ascending j, kept lanes found with a ballot and
+// placed with a popcount prefix, so the list comes out sorted with no sort.
+#include "common.cuh"
+#include "internal.h"
+
+namespace dsa {
+
+__global__ void __launch_bounds__(256) compact_kernel(const CompactLaunch a) {
+  const int lane = threadIdx.x & 31;
+  const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (gw >= a.batch * a.hkv) return;
+  const int b = gw / a.hkv;
+  const int L = a.seq_len[b], P = a.prompt_len[b], W = a.window[b];
+  int code = 0;
+  if (L < 1 || L > a.max_pages * kPage) code = DSA_DEV_BAD_SEQ_LEN;
+  else if (P < 0) code = DSA_DEV_BAD_PROMPT;
+  else if (W < 0 || W > a.max_window) code = DSA_DEV_BAD_WINDOW;
+  if (code != 0) {
+    if (lane == 0) {
+      set_error(a.err, code);
+      a.kept_cnt[gw] = 0;
+    }
+    return;
+  }
+  const int i = L - 1;
+  const int np = min(P, L);
+  int32_t* out = a.kept_idx + static_cast<size_t>(gw) * a.max_kept;
+  const uint32_t* mask = a.keep_mask + static_cast<size_t>(gw) * a.mask_words;
+  const int cap = a.max_kept;
+
+  for (int j = lane; j < np && j < cap; j += 32) out[j] = j;
+  int n = np;
+  if (i >= np) {
+    const int lo = max(np, i - W);
+    for (int base = lo; base <= i; base += 32) {
+      const int j = base + lane;
+      bool keep = false;
+      if (j <= i) {
+        const int o = i - j;
+        keep = (o == 0) || ((__ldg(mask + ((o - 1) >> 5)) >> ((o - 1) & 31)) & 1u);
+      }
+      const unsigned ballot = __ballot_sync(0xffffffffu, keep);
+      const int pos = n + __popc(ballot & ((1u << lane) - 1u));
+      if (keep && pos < cap) out[pos] = j;
+      n += __popc(ballot);
+    }
+  }
+  if (lane == 0) {
+    if (n > cap) {
+      set_error(a.err, DSA_DEV_BAD_COUNT);
+      n = 0;
+    }
+    a.kept_cnt[gw] = n;
+  }
+}
+
+cudaError_t launch_compact(const CompactLaunch& a, cudaStream_t s) {
+  const int warps = a.batch * a.hkv;
+  if (warps == 0) return cudaSuccess;
+  compact_kernel<<<(warps + 7) / 8, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace dsa

@@ -1,0 +1,377 @@
+// decode.cuh -- split-KV flash-decode over a paged KV cache (sparse kept list or
+// dense causal range), and the log-sum-exp merge of its per-chunk partials.
+//
+// Method: softmax(q K^T * scale) V of one decode query per (request, head) over
+// the rows of the kept set -- the masked attention of "Understanding and
+// Exploiting Diagonal Attention Sparsity in Autoregressive Image Generation",
+// paper-daily summary, section 核心公式 (core formula), with masked entries
+// skipped rather than zeroed (arXiv abstract: KV entries are skipped).
+//
+// Work decomposition: grid (chunk, kv head, request).  A CTA owns `chunk`
+// consecutive entries of the row list of one (request, kv head) and all G query
+// heads of that kv head (grouped-query attention shares the rows).  Its NW
+// warps take tiles of T rows round-robin.  Each warp runs its own S-stage
+// shared-memory ring: lanes issue one bulk async copy per K row and per V row
+// (the row's page comes from the page table), completing on the stage's
+// mbarrier; compute never waits for anything but its own copies.
+//
+// Per tile, a warp computes the T x G scores with each lane holding D/32
+// dimensions, reduce-scatters them so that lane l owns row l >> shift, runs
+// the online-softmax update in the log2 domain (q is pre-scaled by
+// scale*log2(e)), and accumulates p_j v_j into per-lane fp32 accumulators.
+// The CTA merges its warps' (m, l, acc) in shared memory and either writes the
+// final output (one chunk) or a partial that merge_kernel combines.
+#pragma once
+
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace dsa {
+
+template <int D, typename KV, int G>
+struct DecodeTiling {
+  static constexpr int kRowBytes = D * static_cast<int>(sizeof(KV));
+  static constexpr int kTByBytes = 8192 / (2 * kRowBytes);  // K+V of one stage = 8 KB
+  static constexpr int kTByRegs = 64 / G;                   // G*T score partials per lane
+  static constexpr int kT0 = kTByBytes < kTByRegs ? kTByBytes : kTByRegs;
+  static constexpr int T = kT0 > 32 ? 32 : (kT0 < 8 ? 8 : kT0);
+  static constexpr int S = 3;   // stages per warp
+  static constexpr int NW = 4;  // warps per CTA
+  static constexpr int kDPL = D / 32;
+  static constexpr int kStageBytes = 2 * T * kRowBytes;
+  static constexpr int kWarpBytes = S * kStageBytes;
+  static constexpr int kBarOff = NW * kWarpBytes;
+  static constexpr int kPOff = kBarOff + NW * S * 8;
+  static constexpr int kMOff = kPOff + NW * G * T * 4;
+  static constexpr int kSmem = kMOff + NW * G * (D + 2) * 4;
+  static_assert(kStageBytes % 128 == 0, "stage alignment");
+  static_assert(kPOff % 16 == 0, "p buffer alignment");
+};
+
+// Rows of the work list of (b, hk), or a negative device error code.  Shared
+// by the decode and merge kernels so that both take the same decision.
+template <bool SPARSE>
+__device__ __forceinline__ int request_rows(const DecodeLaunch& a, int b, int hk, int L) {
+  if (L < 1 || L > a.max_pages * kPage) return -DSA_DEV_BAD_SEQ_LEN;
+  if (!SPARSE) return L;
+  const int n = a.kept_cnt[static_cast<size_t>(b) * a.hkv + hk];
+  if (n < 1 || n > a.max_kept || n > L) return -DSA_DEV_BAD_COUNT;
+  return n;
+}
+
+template <int D, typename KV, int G, bool SPARSE>
+__global__ void __launch_bounds__(DecodeTiling<D, KV, G>::NW * 32)
+    decode_kernel(const DecodeLaunch a) {
+  using Tl = DecodeTiling<D, KV, G>;
+  constexpr int T = Tl::T, S = Tl::S, NW = Tl::NW, DPL = Tl::kDPL;
+  constexpr int kRowBytes = Tl::kRowBytes;
+  extern __shared__ __align__(128) unsigned char smem[];
+
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int c = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
+  const int L = a.seq_len[b];
+  const int n = request_rows<SPARSE>(a, b, hk, L);
+  if (n < 0) {
+    if (c == 0) {
+      if (threadIdx.x == 0) set_error(a.err, -n);
+      for (int x = threadIdx.x; x < G * D; x += NW * 32) {
+        const size_t qh = static_cast<size_t>(b) * a.hq + hk * G + x / D;
+        a.out[qh * D + x % D] = __int_as_float(0x7fc00000);
+        if (a.lse != nullptr && x % D == 0) a.lse[qh] = __int_as_float(0x7fc00000);
+      }
+    }
+    return;
+  }
+  const int row0 = c * a.chunk;
+  if (row0 >= n) return;
+  const int row1 = min(n, row0 + a.chunk);
+  const int nchunks = (n + a.chunk - 1) / a.chunk;
+  const int ntiles = (row1 - row0 + T - 1) / T;
+
+  KV* kst = reinterpret_cast<KV*>(smem + warp * Tl::kWarpBytes);  // [S][T][D]
+  KV* vst = kst + S * T * D;                                      // [S][T][D]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Tl::kBarOff) + warp * S;
+  float* pbuf = reinterpret_cast<float*>(smem + Tl::kPOff) + warp * G * T;  // [G][T]
+  float* mbuf = reinterpret_cast<float*>(smem + Tl::kMOff);                 // [NW][G][D+2]
+
+  if (lane == 0) {
+#pragma unroll
+    for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+
+  const KV* kg = reinterpret_cast<const KV*>(a.k);
+  const KV* vg = reinterpret_cast<const KV*>(a.v);
+  const int32_t* idx = SPARSE ? a.kept_idx + (static_cast<size_t>(b) * a.hkv + hk) * a.max_kept
+                              : nullptr;
+  const int32_t* pt = a.page_table + static_cast<size_t>(b) * a.max_pages;
+
+  // Enqueue the bulk copies of local tile t (rows of global tile warp + t*NW).
+  auto issue = [&](int t, int stage) {
+    const int tr0 = row0 + (warp + t * NW) * T;
+    const int nrows = min(T, row1 - tr0);
+    if (lane == 0) mbar_arrive_expect_tx(&bars[stage], static_cast<uint32_t>(nrows * 2 * kRowBytes));
+    __syncwarp();
+#pragma unroll
+    for (int u = 0; u < (2 * T + 31) / 32; ++u) {
+      const int x = lane + 32 * u;
+      const int r = x & (T - 1);
+      if (x < 2 * T && r < nrows) {
+        int j = SPARSE ? idx[tr0 + r] : tr0 + r;
+        if (static_cast<unsigned>(j) >= static_cast<unsigned>(L)) {
+          set_error(a.err, DSA_DEV_BAD_INDEX);
+          j = 0;
+        }
+        int pg = pt[j >> 4];
+        if (static_cast<unsigned>(pg) >= static_cast<unsigned>(a.num_pages)) {
+          set_error(a.err, DSA_DEV_BAD_PAGE);
+          pg = 0;
+        }
+        const size_t off =
+            ((static_cast<size_t>(pg) * kPage + (j & (kPage - 1))) * a.hkv + hk) * D;
+        const bool is_v = x >= T;
+        KV* dst = (is_v ? vst : kst) + (static_cast<size_t>(stage) * T + r) * D;
+        bulk_copy_g2s(dst, (is_v ? vg : kg) + off, kRowBytes, &bars[stage]);
+      }
+    }
+  };
+
+  float qv[G][DPL];
+#pragma unroll
+  for (int h = 0; h < G; ++h)
+    load_q<DPL>(a.q, a.q_bf16 != 0, (static_cast<size_t>(b) * a.hq + hk * G + h) * D + lane * DPL,
+                a.scale_log2, qv[h]);
+
+  float m_run[G], l_run[G], acc[G][DPL];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    m_run[h] = -INFINITY;
+    l_run[h] = 0.f;
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) acc[h][e] = 0.f;
+  }
+
+  const int my_tiles = warp < ntiles ? (ntiles - warp + NW - 1) / NW : 0;
+  for (int t = 0; t < S && t < my_tiles; ++t) issue(t, t);
+
+  const int myrow = RowMap<T>::row(lane);
+  const bool own = RowMap<T>::owner(lane);
+  int failed_at = -1;
+  for (int t = 0; t < my_tiles; ++t) {
+    const int stage = t % S;
+    if (!mbar_wait(&bars[stage], static_cast<uint32_t>(t / S) & 1u)) {
+      failed_at = t;
+      break;
+    }
+    const int nrows = min(T, row1 - (row0 + (warp + t * NW) * T));
+    const KV* kt = kst + static_cast<size_t>(stage) * T * D + lane * DPL;
+    const KV* vt = vst + static_cast<size_t>(stage) * T * D + lane * DPL;
+
+    // scores: partial dot products over this lane's dimensions
+    float part[G][T];
+#pragma unroll
+    for (int r = 0; r < T; ++r) {
+      float kf[DPL];
+      Vec<KV, DPL>::load(kt + r * D, kf);
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        float s = 0.f;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) s = fmaf(qv[h][e], kf[e], s);
+        part[h][r] = s;
+      }
+    }
+    // online softmax (log2 domain); rows past nrows hold stale data and are masked
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      float s = reduce_scatter<T>(part[h], lane);
+      s = (myrow < nrows) ? s : -INFINITY;
+      const float mnew = fmaxf(m_run[h], warp_max(s));
+      const float alpha = exp2f(m_run[h] - mnew);
+      const float p = exp2f(s - mnew);
+      l_run[h] = l_run[h] * alpha + (own ? p : 0.f);
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) acc[h][e] *= alpha;
+      m_run[h] = mnew;
+      if (own) pbuf[h * T + myrow] = p;
+    }
+    __syncwarp();
+    // acc += p_j v_j
+    auto pv_row = [&](int r) {
+      float vf[DPL];
+      Vec<KV, DPL>::load(vt + r * D, vf);
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float p = pbuf[h * T + r];
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) acc[h][e] = fmaf(p, vf[e], acc[h][e]);
+      }
+    };
+    if (nrows == T) {
+#pragma unroll
+      for (int r = 0; r < T; ++r) pv_row(r);
+    } else {
+      for (int r = 0; r < nrows; ++r) pv_row(r);
+    }
+    __syncwarp();
+    fence_proxy_async_smem();
+    if (t + S < my_tiles) issue(t + S, stage);
+  }
+  if (failed_at >= 0) {
+    // Give the copies still in flight a bounded chance to land before exiting.
+    if (lane == 0) set_error(a.err, DSA_DEV_TIMEOUT);
+    for (int t = failed_at; t < my_tiles && t < failed_at + S; ++t)
+      mbar_wait(&bars[t % S], static_cast<uint32_t>(t / S) & 1u);
+  }
+
+  // merge the warps of this CTA
+  float* mw = mbuf + static_cast<size_t>(warp) * G * (D + 2);
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) mw[h * (D + 2) + lane * DPL + e] = acc[h][e];
+    const float l = warp_sum(l_run[h]);
+    if (lane == 0) {
+      mw[h * (D + 2) + D] = m_run[h];
+      mw[h * (D + 2) + D + 1] = l;
+    }
+  }
+  __syncthreads();
+  for (int x = threadIdx.x; x < G * D; x += NW * 32) {
+    const int h = x / D, d = x % D;
+    float mstar = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) mstar = fmaxf(mstar, mbuf[(w * G + h) * (D + 2) + D]);
+    float o = 0.f, ls = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      const float* src = mbuf + (w * G + h) * (D + 2);
+      const float sc = src[D] == -INFINITY ? 0.f : exp2f(src[D] - mstar);
+      o = fmaf(sc, src[d], o);
+      ls = fmaf(sc, src[D + 1], ls);
+    }
+    const size_t qh = static_cast<size_t>(b) * a.hq + hk * G + h;
+    if (nchunks == 1) {
+      a.out[qh * D + d] = o / ls;
+      if (a.lse != nullptr && d == 0) a.lse[qh] = (mstar + log2f(ls)) * kLn2;
+    } else {
+      float* pp = a.part + (qh * a.num_chunks + c) * (D + 2);
+      pp[d] = o;
+      if (d == 0) {
+        pp[D] = mstar;
+        pp[D + 1] = ls;
+      }
+    }
+  }
+}
+
+// One warp per (request, query head): combine the chunk partials by
+// log-sum-exp.  Heads whose rows fit one chunk were finished by decode_kernel.
+template <int D, bool SPARSE>
+__global__ void __launch_bounds__(128) merge_kernel(const DecodeLaunch a) {
+  constexpr int DPL = D / 32;
+  const int lane = threadIdx.x & 31;
+  const int gw = blockIdx.x * 4 + (threadIdx.x >> 5);
+  if (gw >= a.batch * a.hq) return;
+  const int b = gw / a.hq, qh = gw % a.hq;
+  const int hk = qh / (a.hq / a.hkv);
+  const int n = request_rows<SPARSE>(a, b, hk, a.seq_len[b]);
+  if (n < 0) return;  // decode_kernel wrote NaN and the error code
+  const int nch = (n + a.chunk - 1) / a.chunk;
+  if (nch <= 1) return;
+  const float* pp = a.part + static_cast<size_t>(gw) * a.num_chunks * (D + 2);
+  float mstar = -INFINITY;
+  for (int c = lane; c < nch; c += 32) mstar = fmaxf(mstar, pp[c * (D + 2) + D]);
+  mstar = warp_max(mstar);
+  float o[DPL], ls = 0.f;
+#pragma unroll
+  for (int e = 0; e < DPL; ++e) o[e] = 0.f;
+  for (int c = 0; c < nch; ++c) {
+    const float* src = pp + c * (D + 2);
+    const float sc = exp2f(src[D] - mstar);
+    ls = fmaf(sc, src[D + 1], ls);
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) o[e] = fmaf(sc, src[lane * DPL + e], o[e]);
+  }
+  float* out = a.out + static_cast<size_t>(gw) * D + lane * DPL;
+#pragma unroll
+  for (int e = 0; e < DPL; ++e) out[e] = o[e] / ls;
+  if (a.lse != nullptr && lane == 0) a.lse[gw] = (mstar + log2f(ls)) * kLn2;
+}
+
+template <int D, typename KV, int G, bool SPARSE>
+cudaError_t launch_decode_one(const DecodeLaunch& a, cudaStream_t s) {
+  using Tl = DecodeTiling<D, KV, G>;
+  auto kern = decode_kernel<D, KV, G, SPARSE>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Tl::kSmem);
+  if (e != cudaSuccess) return e;
+  const dim3 grid(a.num_chunks, a.hkv, a.batch);
+  kern<<<grid, Tl::NW * 32, Tl::kSmem, s>>>(a);
+  return cudaGetLastError();
+}
+
+template <typename KV, bool SPARSE>
+cudaError_t launch_decode_dispatch(const DecodeLaunch& a, cudaStream_t s) {
+  const int g = a.hq / a.hkv;
+#define DSA_CASE(DD, GG) \
+  if (a.head_dim == DD && g == GG) return launch_decode_one<DD, KV, GG, SPARSE>(a, s);
+  DSA_CASE(64, 1)
+  DSA_CASE(64, 2)
+  DSA_CASE(64, 4)
+  DSA_CASE(64, 8)
+  DSA_CASE(128, 1)
+  DSA_CASE(128, 2)
+  DSA_CASE(128, 4)
+  DSA_CASE(128, 8)
+#undef DSA_CASE
+  return cudaErrorInvalidValue;
+}
+
+template <typename KV>
+int decode_rows_per_pass_t(int head_dim, int group) {
+#define DSA_CASE(DD, GG) \
+  if (head_dim == DD && group == GG) return DecodeTiling<DD, KV, GG>::NW * DecodeTiling<DD, KV, GG>::T;
+  DSA_CASE(64, 1)
+  DSA_CASE(64, 2)
+  DSA_CASE(64, 4)
+  DSA_CASE(64, 8)
+  DSA_CASE(128, 1)
+  DSA_CASE(128, 2)
+  DSA_CASE(128, 4)
+  DSA_CASE(128, 8)
+#undef DSA_CASE
+  return 0;
+}
+
+template <typename KV>
+int decode_ctas_per_sm_t(int head_dim, int group, bool sparse) {
+  int n = 0;
+#define DSA_CASE(DD, GG)                                                                   \
+  if (head_dim == DD && group == GG) {                                                     \
+    using Tl = DecodeTiling<DD, KV, GG>;                                                   \
+    auto kern = sparse ? decode_kernel<DD, KV, GG, true> : decode_kernel<DD, KV, GG, false>; \
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,            \
+                             Tl::kSmem) != cudaSuccess)                                    \
+      return 1;                                                                            \
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, Tl::NW * 32, Tl::kSmem) != \
+        cudaSuccess)                                                                       \
+      return 1;                                                                            \
+    return n < 1 ? 1 : n;                                                                  \
+  }
+  DSA_CASE(64, 1)
+  DSA_CASE(64, 2)
+  DSA_CASE(64, 4)
+  DSA_CASE(64, 8)
+  DSA_CASE(128, 1)
+  DSA_CASE(128, 2)
+  DSA_CASE(128, 4)
+  DSA_CASE(128, 8)
+#undef DSA_CASE
+  return 1;
+}
+
+}  // namespace dsa

@@ -1,0 +1,306 @@
+// dsa_api.cu -- the extern "C" entry points of libdsa (declared in dsa.h):
+// host-side validation, work-chunk sizing, and kernel dispatch.  Nothing here
+// computes attention; every step of the path runs in the kernels.
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "dsa.h"
+#include "internal.h"
+
+namespace dsa {
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+bool dims_valid(const dsa_dims* d) {
+  if (d == nullptr) return false;
+  if (d->batch < 0 || d->hq < 1 || d->hkv < 1 || d->head_dim < 1) return false;
+  if (d->hq % d->hkv != 0) return false;
+  if (d->num_pages < 1 || d->max_pages_per_req < 1 || d->max_window < 0) return false;
+  if (d->mask_words < 1 || static_cast<int64_t>(d->mask_words) * 32 < d->max_window) return false;
+  if (d->max_kept < 1) return false;
+  if (d->q_dtype != DSA_F32 && d->q_dtype != DSA_BF16) return false;
+  if (d->kv_dtype != DSA_F32 && d->kv_dtype != DSA_BF16) return false;
+  // page_table entries index rows as page * 16 * hkv * head_dim elements in 64-bit math;
+  // logical positions are int32.
+  if (static_cast<int64_t>(d->max_pages_per_req) * kPage > INT32_MAX / 2) return false;
+  return true;
+}
+
+bool dims_supported(const dsa_dims* d) {
+  const int g = d->hq / d->hkv;
+  return d->page_size == kPage && (d->head_dim == 64 || d->head_dim == 128) &&
+         (g == 1 || g == 2 || g == 4 || g == 8);
+}
+
+dsa_status check_dims(const dsa_dims* d) {
+  if (!dims_valid(d)) return DSA_ERR_INVALID_ARG;
+  if (!dims_supported(d)) return DSA_ERR_UNSUPPORTED;
+  return DSA_OK;
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Upper bound of chunks per (request, kv head) for a row count n_max.
+int chunk_bound(int64_t n_max) {
+  const int64_t c = ceil_div(n_max, kChunkQuantum);
+  return static_cast<int>(c < kMaxChunks ? (c < 1 ? 1 : c) : kMaxChunks);
+}
+
+int64_t dense_rows(const dsa_dims* d) { return static_cast<int64_t>(d->max_pages_per_req) * kPage; }
+
+size_t partial_bytes(const dsa_dims* d, int per_head_floats) {
+  const int64_t n_max = dense_rows(d) > d->max_kept ? dense_rows(d) : d->max_kept;
+  return static_cast<size_t>(d->batch) * d->hq * chunk_bound(n_max) * per_head_floats *
+         sizeof(float);
+}
+
+int sm_count() {
+  static int cache[kMaxDevices] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (dev >= 0 && dev < kMaxDevices && cache[dev] > 0) return cache[dev];
+  int n = 1;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+    n = 1;
+  if (dev >= 0 && dev < kMaxDevices) cache[dev] = n;
+  return n;
+}
+
+// Rows per CTA: enough CTAs for ~8 waves of resident CTAs, at most kMaxChunks
+// chunks per (request, kv head), a multiple of the CTA's rows per pass.
+void choose_chunks(int64_t n_max, int64_t units, int resident, int quantum, int* chunk,
+                   int* num_chunks) {
+  if (quantum < kChunkQuantum) quantum = kChunkQuantum;
+  const int64_t target = 8LL * resident;
+  int64_t c = ceil_div(n_max * units, target > 0 ? target : 1);
+  const int64_t lo = ceil_div(n_max, kMaxChunks);
+  if (c < lo) c = lo;
+  c = ceil_div(c, quantum) * quantum;
+  const int64_t hi = ceil_div(n_max, quantum) * quantum;
+  if (c > hi) c = hi;
+  if (c < quantum) c = quantum;
+  // chunk_bound() sizes the workspace with chunks of kChunkQuantum rows, so any
+  // chunk >= max(quantum, n_max / kMaxChunks) fits.
+  *chunk = static_cast<int>(c);
+  *num_chunks = static_cast<int>(ceil_div(n_max, c));
+}
+
+dsa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA; }
+
+int32_t* err_word(void* ws) { return reinterpret_cast<int32_t*>(ws); }
+
+float* partials(void* ws) {
+  return reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(ws) + kWsHeader);
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+struct Plan {
+  int chunk, num_chunks, quantum, per_sm;
+};
+
+Plan decode_plan(const dsa_dims* d, bool sparse) {
+  const bool kv_bf16 = d->kv_dtype == DSA_BF16;
+  const int g = d->hq / d->hkv;
+  const int64_t n_max = sparse ? d->max_kept : dense_rows(d);
+  Plan p{};
+  p.quantum = kv_bf16 ? decode_rows_per_pass_bf16(d->head_dim, g)
+                      : decode_rows_per_pass_f32(d->head_dim, g);
+  p.per_sm = kv_bf16 ? decode_ctas_per_sm_bf16(d->head_dim, g, sparse)
+                     : decode_ctas_per_sm_f32(d->head_dim, g, sparse);
+  choose_chunks(n_max, static_cast<int64_t>(d->batch) * d->hkv, sm_count() * p.per_sm, p.quantum,
+                &p.chunk, &p.num_chunks);
+  return p;
+}
+
+dsa_status decode_common(const dsa_dims* d, bool sparse, const void* q, const void* k,
+                         const void* v, const int32_t* page_table, const int32_t* seq_len,
+                         const int32_t* kept_idx, const int32_t* kept_cnt, float scale,
+                         float* out, float* lse, void* ws, void* stream) {
+  const dsa_status st = check_dims(d);
+  if (st != DSA_OK) return st;
+  if (!q || !k || !v || !page_table || !seq_len || !out || !ws) return DSA_ERR_INVALID_ARG;
+  if (sparse && (!kept_idx || !kept_cnt)) return DSA_ERR_INVALID_ARG;
+  if (!(scale == scale) || !aligned(ws, 256) || !aligned(k, 16) || !aligned(v, 16) ||
+      !aligned(q, 16))
+    return DSA_ERR_INVALID_ARG;
+  if (d->batch == 0) return DSA_OK;
+  const bool kv_bf16 = d->kv_dtype == DSA_BF16;
+  const Plan plan = decode_plan(d, sparse);
+  DecodeLaunch a{};
+  a.q = q;
+  a.q_bf16 = d->q_dtype == DSA_BF16;
+  a.k = k;
+  a.v = v;
+  a.page_table = page_table;
+  a.seq_len = seq_len;
+  a.kept_idx = kept_idx;
+  a.kept_cnt = kept_cnt;
+  a.batch = d->batch;
+  a.hq = d->hq;
+  a.hkv = d->hkv;
+  a.head_dim = d->head_dim;
+  a.max_pages = d->max_pages_per_req;
+  a.num_pages = d->num_pages;
+  a.max_kept = d->max_kept;
+  a.chunk = plan.chunk;
+  a.num_chunks = plan.num_chunks;
+  a.scale_log2 = scale * kLog2e;
+  a.out = out;
+  a.lse = lse;
+  a.part = partials(ws);
+  a.err = err_word(ws);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = kv_bf16 ? launch_decode_bf16(a, sparse, s) : launch_decode_f32(a, sparse, s);
+  if (e != cudaSuccess) return DSA_ERR_CUDA;
+  return from_cuda(launch_merge(a, sparse, s));
+}
+
+}  // namespace
+}  // namespace dsa
+
+using namespace dsa;
+
+extern "C" {
+
+int32_t dsa_version(void) { return (0 << 16) | 1; }
+
+const char* dsa_status_string(dsa_status status) {
+  switch (status) {
+    case DSA_OK: return "DSA_OK";
+    case DSA_ERR_INVALID_ARG: return "DSA_ERR_INVALID_ARG";
+    case DSA_ERR_UNSUPPORTED: return "DSA_ERR_UNSUPPORTED";
+    case DSA_ERR_CUDA: return "DSA_ERR_CUDA";
+    case DSA_ERR_DEVICE: return "DSA_ERR_DEVICE";
+    case DSA_ERR_TIMEOUT: return "DSA_ERR_TIMEOUT";
+  }
+  return "DSA_ERR_UNKNOWN";
+}
+
+size_t dsa_workspace_size(const dsa_dims* dims) {
+  if (check_dims(dims) != DSA_OK) return 0;
+  const size_t dec = partial_bytes(dims, dims->head_dim + 2);
+  const size_t mass = partial_bytes(dims, 6);
+  return kWsHeader + (dec > mass ? dec : mass);
+}
+
+dsa_status dsa_build_index(const dsa_dims* dims, const int32_t* seq_len,
+                           const int32_t* prompt_len, const int32_t* window,
+                           const uint32_t* keep_mask, int32_t* kept_idx, int32_t* kept_cnt,
+                           void* ws, void* stream) {
+  const dsa_status st = check_dims(dims);
+  if (st != DSA_OK) return st;
+  if (!seq_len || !prompt_len || !window || !keep_mask || !kept_idx || !kept_cnt || !ws)
+    return DSA_ERR_INVALID_ARG;
+  if (!aligned(ws, 256)) return DSA_ERR_INVALID_ARG;
+  CompactLaunch a{};
+  a.seq_len = seq_len;
+  a.prompt_len = prompt_len;
+  a.window = window;
+  a.keep_mask = keep_mask;
+  a.kept_idx = kept_idx;
+  a.kept_cnt = kept_cnt;
+  a.batch = dims->batch;
+  a.hkv = dims->hkv;
+  a.max_pages = dims->max_pages_per_req;
+  a.max_window = dims->max_window;
+  a.mask_words = dims->mask_words;
+  a.max_kept = dims->max_kept;
+  a.err = err_word(ws);
+  return from_cuda(launch_compact(a, static_cast<cudaStream_t>(stream)));
+}
+
+dsa_status dsa_decode_sparse(const dsa_dims* dims, const void* q, const void* k_pages,
+                             const void* v_pages, const int32_t* page_table,
+                             const int32_t* seq_len, const int32_t* kept_idx,
+                             const int32_t* kept_cnt, float scale, float* out, float* lse,
+                             void* ws, void* stream) {
+  return decode_common(dims, true, q, k_pages, v_pages, page_table, seq_len, kept_idx, kept_cnt,
+                       scale, out, lse, ws, stream);
+}
+
+dsa_status dsa_decode_dense(const dsa_dims* dims, const void* q, const void* k_pages,
+                            const void* v_pages, const int32_t* page_table,
+                            const int32_t* seq_len, float scale, float* out, float* lse,
+                            void* ws, void* stream) {
+  return decode_common(dims, false, q, k_pages, v_pages, page_table, seq_len, nullptr, nullptr,
+                       scale, out, lse, ws, stream);
+}
+
+dsa_status dsa_attention_mass(const dsa_dims* dims, const void* q, const void* k_pages,
+                              const int32_t* page_table, const int32_t* seq_len,
+                              const int32_t* prompt_len, const int32_t* window,
+                              const int32_t* grid_w, int32_t r_local, int32_t r_diag,
+                              float scale, float* mass, float* offset_mass, void* ws,
+                              void* stream) {
+  const dsa_status st = check_dims(dims);
+  if (st != DSA_OK) return st;
+  if (!q || !k_pages || !page_table || !seq_len || !prompt_len || !window || !grid_w || !mass ||
+      !ws)
+    return DSA_ERR_INVALID_ARG;
+  if (r_local < 0 || r_diag < 0 || !(scale == scale) || !aligned(ws, 256) ||
+      !aligned(k_pages, 16) || !aligned(q, 16))
+    return DSA_ERR_INVALID_ARG;
+  if (dims->batch == 0) return DSA_OK;
+  const int64_t n_max = dense_rows(dims);
+  MassLaunch a{};
+  a.q = q;
+  a.q_bf16 = dims->q_dtype == DSA_BF16;
+  a.k = k_pages;
+  a.page_table = page_table;
+  a.seq_len = seq_len;
+  a.prompt_len = prompt_len;
+  a.window = window;
+  a.grid_w = grid_w;
+  a.batch = dims->batch;
+  a.hq = dims->hq;
+  a.hkv = dims->hkv;
+  a.head_dim = dims->head_dim;
+  a.max_pages = dims->max_pages_per_req;
+  a.num_pages = dims->num_pages;
+  a.max_window = dims->max_window;
+  a.r_local = r_local;
+  a.r_diag = r_diag;
+  choose_chunks(n_max, static_cast<int64_t>(dims->batch) * dims->hkv, sm_count() * 2,
+                kChunkQuantum, &a.chunk, &a.num_chunks);
+  a.scale_log2 = scale * kLog2e;
+  a.mass = mass;
+  a.offset_mass = offset_mass;
+  a.part = partials(ws);
+  a.err = err_word(ws);
+  return from_cuda(launch_mass(a, dims->kv_dtype == DSA_BF16, static_cast<cudaStream_t>(stream)));
+}
+
+dsa_status dsa_decode_plan(const dsa_dims* dims, int32_t sparse, int32_t* chunk,
+                           int32_t* num_chunks, int32_t* launches) {
+  const dsa_status st = check_dims(dims);
+  if (st != DSA_OK) return st;
+  const Plan p = decode_plan(dims, sparse != 0);
+  if (chunk) *chunk = p.chunk;
+  if (num_chunks) *num_chunks = p.num_chunks;
+  if (launches) *launches = dims->batch == 0 ? 0 : (p.num_chunks > 1 ? 2 : 1);
+  return DSA_OK;
+}
+
+dsa_status dsa_get_device_error(const void* ws, void* stream, int32_t* code_out) {
+  if (!ws || !code_out) return DSA_ERR_INVALID_ARG;
+  int32_t code = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&code, ws, sizeof(code), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return DSA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return DSA_ERR_CUDA;
+  *code_out = code;
+  if (code == DSA_DEV_OK) return DSA_OK;
+  return code == DSA_DEV_TIMEOUT ? DSA_ERR_TIMEOUT : DSA_ERR_DEVICE;
+}
+
+dsa_status dsa_clear_device_error(void* ws, void* stream) {
+  if (!ws) return DSA_ERR_INVALID_ARG;
+  return from_cuda(cudaMemsetAsync(ws, 0, sizeof(int32_t), static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,80 @@
+// internal.h -- host-side launch interface between the C ABI and the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace dsa {
+
+// Rows of one decode / mass work unit are split into chunks of `chunk` rows;
+// each chunk is one CTA.  At most kMaxChunks chunks per (request, kv head).
+constexpr int kMaxChunks = 32;
+constexpr int kChunkQuantum = 64;  // chunk sizes are multiples of this
+
+struct DecodeLaunch {
+  const void* q;
+  int q_bf16;
+  const void* k;
+  const void* v;
+  const int32_t* page_table;
+  const int32_t* seq_len;
+  const int32_t* kept_idx;  // sparse only
+  const int32_t* kept_cnt;  // sparse only
+  int32_t batch, hq, hkv, head_dim, max_pages, num_pages, max_kept;
+  int32_t chunk, num_chunks;
+  float scale_log2;  // softmax scale * log2(e)
+  float* out;
+  float* lse;
+  float* part;  // [batch][hq][num_chunks][head_dim + 2]
+  int32_t* err;
+};
+
+struct MassLaunch {
+  const void* q;
+  int q_bf16;
+  const void* k;
+  const int32_t* page_table;
+  const int32_t* seq_len;
+  const int32_t* prompt_len;
+  const int32_t* window;
+  const int32_t* grid_w;
+  int32_t batch, hq, hkv, head_dim, max_pages, num_pages, max_window;
+  int32_t r_local, r_diag;
+  int32_t chunk, num_chunks;
+  float scale_log2;
+  float* mass;         // [batch][hq][4]
+  float* offset_mass;  // [batch][hq][max_window+1] or null
+  float* part;         // [batch][hq][num_chunks][6]
+  int32_t* err;
+};
+
+struct CompactLaunch {
+  const int32_t* seq_len;
+  const int32_t* prompt_len;
+  const int32_t* window;
+  const uint32_t* keep_mask;
+  int32_t* kept_idx;
+  int32_t* kept_cnt;
+  int32_t batch, hkv, max_pages, max_window, mask_words, max_kept;
+  int32_t* err;
+};
+
+// Each returns cudaSuccess or the launch error.  `sparse` selects the kept
+// list (true) or the dense range 0..L-1 (false).
+cudaError_t launch_decode_bf16(const DecodeLaunch& a, bool sparse, cudaStream_t s);
+cudaError_t launch_decode_f32(const DecodeLaunch& a, bool sparse, cudaStream_t s);
+cudaError_t launch_merge(const DecodeLaunch& a, bool sparse, cudaStream_t s);
+cudaError_t launch_mass(const MassLaunch& a, bool kv_bf16, cudaStream_t s);
+cudaError_t launch_compact(const CompactLaunch& a, cudaStream_t s);
+
+// Rows one pass of all warps of a decode CTA covers (warps x tile rows), for
+// the host's chunk choice.
+int decode_rows_per_pass_bf16(int head_dim, int group);
+int decode_rows_per_pass_f32(int head_dim, int group);
+// Resident CTAs per SM of the decode kernel for this instantiation (>= 1).
+int decode_ctas_per_sm_bf16(int head_dim, int group, bool sparse);
+int decode_ctas_per_sm_f32(int head_dim, int group, bool sparse);
+
+}  // namespace dsa

@@ -1,0 +1,213 @@
+"""Thin ctypes binding of libdsa (include/dsa.h): argument marshalling only.
+
+Every function has the name of its C entry point, takes torch CUDA tensors
+(or None where the C argument may be NULL), passes their device pointers and
+the current CUDA stream, and raises DSAError on a non-OK status.  All compute
+runs in the library's CUDA kernels; there is no fallback of any kind: if the
+library cannot be built or loaded, the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+DSA_OK, DSA_ERR_INVALID_ARG, DSA_ERR_UNSUPPORTED, DSA_ERR_CUDA, DSA_ERR_DEVICE, \
+    DSA_ERR_TIMEOUT = range(6)
+DSA_F32, DSA_BF16 = 0, 1
+DEV_ERRORS = {0: "OK", 1: "BAD_SEQ_LEN", 2: "BAD_PROMPT", 3: "BAD_WINDOW", 4: "BAD_PAGE",
+              5: "BAD_INDEX", 6: "BAD_COUNT", 7: "TIMEOUT", 8: "BAD_GRID_W"}
+PAGE = 16
+
+
+class DSAError(RuntimeError):
+    def __init__(self, status: int, what: str, dev_code: int | None = None):
+        self.status = status
+        self.dev_code = dev_code
+        msg = f"{what}: {status_name(status)}"
+        if dev_code is not None:
+            msg += f" (device code {dev_code} {DEV_ERRORS.get(dev_code, '?')})"
+        super().__init__(msg)
+
+
+class dsa_dims(ctypes.Structure):
+    _fields_ = [(name, ctypes.c_int32) for name in (
+        "batch", "hq", "hkv", "head_dim", "page_size", "num_pages", "max_pages_per_req",
+        "max_window", "mask_words", "max_kept", "q_dtype", "kv_dtype")]
+
+
+_lib = None
+_lib_path = None
+
+
+def library_path() -> str:
+    """Path of the loaded libdsa.so (building it first if needed)."""
+    _load()
+    return _lib_path
+
+
+def _load():
+    global _lib, _lib_path
+    if _lib is not None:
+        return _lib
+    path = os.environ.get("DSA_LIBRARY")
+    if not path:
+        from . import build as _build
+        path = _build.build()
+    lib = ctypes.CDLL(path)
+    P, I32, F32, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
+    D = ctypes.POINTER(dsa_dims)
+    sig = {
+        "dsa_version": ([], I32),
+        "dsa_status_string": ([I32], ctypes.c_char_p),
+        "dsa_workspace_size": ([D], SZ),
+        "dsa_build_index": ([D, P, P, P, P, P, P, P, P], I32),
+        "dsa_decode_sparse": ([D, P, P, P, P, P, P, P, F32, P, P, P, P], I32),
+        "dsa_decode_dense": ([D, P, P, P, P, P, F32, P, P, P, P], I32),
+        "dsa_attention_mass": ([D, P, P, P, P, P, P, P, I32, I32, F32, P, P, P, P], I32),
+        "dsa_decode_plan": ([D, I32, ctypes.POINTER(I32), ctypes.POINTER(I32),
+                             ctypes.POINTER(I32)], I32),
+        "dsa_get_device_error": ([P, P, ctypes.POINTER(I32)], I32),
+        "dsa_clear_device_error": ([P, P], I32),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib, _lib_path = lib, path
+    return lib
+
+
+def status_name(status: int) -> str:
+    try:
+        return _load().dsa_status_string(int(status)).decode()
+    except OSError:
+        return f"status {status}"
+
+
+def dsa_version() -> int:
+    return _load().dsa_version()
+
+
+def dsa_status_string(status: int) -> str:
+    return _load().dsa_status_string(int(status)).decode()
+
+
+def make_dims(batch, hq, hkv, head_dim, num_pages, max_pages_per_req, max_window, mask_words,
+              max_kept, q_dtype, kv_dtype, page_size=PAGE) -> dsa_dims:
+    def code(dt):
+        if isinstance(dt, int):
+            return dt
+        return {torch.float32: DSA_F32, torch.bfloat16: DSA_BF16, "f32": DSA_F32,
+                "bf16": DSA_BF16}[dt]
+    return dsa_dims(batch, hq, hkv, head_dim, page_size, num_pages, max_pages_per_req,
+                    max_window, mask_words, max_kept, code(q_dtype), code(kv_dtype))
+
+
+def _ptr(t, dtype=None, what="tensor"):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{what} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{what} must be contiguous")
+    if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise TypeError(f"{what} has dtype {t.dtype}, expected {dtype}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(status, what):
+    if status != DSA_OK:
+        raise DSAError(status, what)
+
+
+def dsa_workspace_size(dims: dsa_dims) -> int:
+    return int(_load().dsa_workspace_size(ctypes.byref(dims)))
+
+
+def alloc_workspace(dims: dsa_dims, device=None) -> torch.Tensor:
+    """A zero-filled workspace of dsa_workspace_size(dims) bytes (torch owns it)."""
+    n = dsa_workspace_size(dims)
+    if n == 0:
+        raise DSAError(DSA_ERR_INVALID_ARG, "dsa_workspace_size")
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
+_I32 = torch.int32
+_MASK = (torch.int32, getattr(torch, "uint32", torch.int32))
+_QKV = (torch.float32, torch.bfloat16)
+
+
+def dsa_build_index(dims, seq_len, prompt_len, window, keep_mask, kept_idx, kept_cnt, ws,
+                    stream=None):
+    _check(_load().dsa_build_index(
+        ctypes.byref(dims), _ptr(seq_len, _I32, "seq_len"), _ptr(prompt_len, _I32, "prompt_len"),
+        _ptr(window, _I32, "window"), _ptr(keep_mask, _MASK, "keep_mask"),
+        _ptr(kept_idx, _I32, "kept_idx"), _ptr(kept_cnt, _I32, "kept_cnt"), _ptr(ws), _stream(stream)),
+        "dsa_build_index")
+
+
+def dsa_decode_sparse(dims, q, k_pages, v_pages, page_table, seq_len, kept_idx, kept_cnt, scale,
+                      out, lse, ws, stream=None):
+    _check(_load().dsa_decode_sparse(
+        ctypes.byref(dims), _ptr(q, _QKV, "q"), _ptr(k_pages, _QKV, "k_pages"),
+        _ptr(v_pages, _QKV, "v_pages"), _ptr(page_table, _I32, "page_table"),
+        _ptr(seq_len, _I32, "seq_len"), _ptr(kept_idx, _I32, "kept_idx"),
+        _ptr(kept_cnt, _I32, "kept_cnt"), float(scale), _ptr(out, torch.float32, "out"),
+        _ptr(lse, torch.float32, "lse"), _ptr(ws), _stream(stream)), "dsa_decode_sparse")
+
+
+def dsa_decode_dense(dims, q, k_pages, v_pages, page_table, seq_len, scale, out, lse, ws,
+                     stream=None):
+    _check(_load().dsa_decode_dense(
+        ctypes.byref(dims), _ptr(q, _QKV, "q"), _ptr(k_pages, _QKV, "k_pages"),
+        _ptr(v_pages, _QKV, "v_pages"), _ptr(page_table, _I32, "page_table"),
+        _ptr(seq_len, _I32, "seq_len"), float(scale), _ptr(out, torch.float32, "out"),
+        _ptr(lse, torch.float32, "lse"), _ptr(ws), _stream(stream)), "dsa_decode_dense")
+
+
+def dsa_attention_mass(dims, q, k_pages, page_table, seq_len, prompt_len, window, grid_w,
+                       r_local, r_diag, scale, mass, offset_mass, ws, stream=None):
+    _check(_load().dsa_attention_mass(
+        ctypes.byref(dims), _ptr(q, _QKV, "q"), _ptr(k_pages, _QKV, "k_pages"),
+        _ptr(page_table, _I32, "page_table"), _ptr(seq_len, _I32, "seq_len"),
+        _ptr(prompt_len, _I32, "prompt_len"), _ptr(window, _I32, "window"),
+        _ptr(grid_w, _I32, "grid_w"), int(r_local), int(r_diag), float(scale),
+        _ptr(mass, torch.float32, "mass"), _ptr(offset_mass, torch.float32, "offset_mass"),
+        _ptr(ws), _stream(stream)), "dsa_attention_mass")
+
+
+def dsa_decode_plan(dims, sparse: bool):
+    """(rows per CTA, max CTAs per (request, kv head), kernel launches per call)
+    on the current device."""
+    c, n, l = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    _check(_load().dsa_decode_plan(ctypes.byref(dims), int(sparse), ctypes.byref(c),
+                                   ctypes.byref(n), ctypes.byref(l)), "dsa_decode_plan")
+    return c.value, n.value, l.value
+
+
+def dsa_get_device_error(ws, stream=None) -> int:
+    """Synchronising read of the workspace error word; returns the DSA_DEV_* code."""
+    code = ctypes.c_int32(0)
+    st = _load().dsa_get_device_error(_ptr(ws), _stream(stream), ctypes.byref(code))
+    if st == DSA_ERR_CUDA:
+        raise DSAError(st, "dsa_get_device_error")
+    return int(code.value)
+
+
+def dsa_clear_device_error(ws, stream=None):
+    _check(_load().dsa_clear_device_error(_ptr(ws), _stream(stream)), "dsa_clear_device_error")
+
+
+def check_device_error(ws, what="libdsa", stream=None):
+    """Raise DSAError if the kernels flagged invalid data since the last clear."""
+    code = dsa_get_device_error(ws, stream)
+    if code != 0:
+        raise DSAError(DSA_ERR_TIMEOUT if code == 7 else DSA_ERR_DEVICE, what, code)

@@ -1,0 +1,97 @@
+"""Device-resident batch for the libdsa calls: tensors, dims and workspace.
+
+``DecodeBatch.from_workload`` copies a batch drawn by ``workloads.generate`` to
+the GPU once; its methods are one-line calls of the C ABI through the ctypes
+binding.  PyTorch provides the device memory and the stream, nothing else.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+from . import dsa
+
+
+def _i32(x, device):
+    return torch.as_tensor(np.ascontiguousarray(x, dtype=np.int32)).to(device)
+
+
+class DecodeBatch:
+    def __init__(self, *, q, k_pages, v_pages, page_table, seq_len, prompt_len, window,
+                 grid_w, keep_mask, max_window, mask_words, max_kept, device="cuda"):
+        self.device = torch.device(device)
+        self.q = q.to(self.device).contiguous()
+        self.k_pages = k_pages.to(self.device).contiguous()
+        self.v_pages = v_pages.to(self.device).contiguous()
+        self.page_table = _i32(page_table, self.device)
+        self.seq_len = _i32(seq_len, self.device)
+        self.prompt_len = _i32(prompt_len, self.device)
+        self.window = _i32(window, self.device)
+        self.grid_w = _i32(grid_w, self.device)
+        B, Hq, D = self.q.shape
+        num_pages, page, Hkv, _ = self.k_pages.shape
+        self.batch, self.hq, self.hkv, self.head_dim = B, Hq, Hkv, D
+        if keep_mask is None:
+            keep_mask = np.zeros((B, Hkv, mask_words), dtype=np.uint32)
+        self.keep_mask = torch.as_tensor(
+            np.ascontiguousarray(keep_mask, dtype=np.uint32).view(np.int32)).to(self.device)
+        self.dims = dsa.make_dims(B, Hq, Hkv, D, num_pages, self.page_table.shape[1], max_window,
+                                  mask_words, max_kept, self.q.dtype, self.k_pages.dtype)
+        self.scale = 1.0 / math.sqrt(D)
+        self.ws = dsa.alloc_workspace(self.dims, self.device)
+        self.kept_idx = torch.zeros((B, Hkv, max_kept), dtype=torch.int32, device=self.device)
+        self.kept_cnt = torch.zeros((B, Hkv), dtype=torch.int32, device=self.device)
+        self.out = torch.empty((B, Hq, D), dtype=torch.float32, device=self.device)
+        self.lse = torch.empty((B, Hq), dtype=torch.float32, device=self.device)
+
+    @classmethod
+    def from_workload(cls, w: dict, device="cuda", keep_mask=None):
+        return cls(q=w["q"], k_pages=w["k_pages"], v_pages=w["v_pages"],
+                   page_table=w["page_table"], seq_len=w["seq_len"], prompt_len=w["prompt_len"],
+                   window=w["window"], grid_w=w["grid_w"],
+                   keep_mask=w["keep_mask"] if keep_mask is None else keep_mask,
+                   max_window=w["max_window"], mask_words=w["mask_words"],
+                   max_kept=w["max_kept"], device=device)
+
+    def set_keep_mask(self, keep_mask):
+        self.keep_mask.copy_(torch.as_tensor(
+            np.ascontiguousarray(keep_mask, dtype=np.uint32).view(np.int32)))
+
+    # -- the C ABI calls --------------------------------------------------
+    def build_index(self, stream=None):
+        dsa.dsa_build_index(self.dims, self.seq_len, self.prompt_len, self.window, self.keep_mask,
+                            self.kept_idx, self.kept_cnt, self.ws, stream)
+
+    def decode_sparse(self, out=None, lse=None, stream=None):
+        out = self.out if out is None else out
+        lse = self.lse if lse is None else lse
+        dsa.dsa_decode_sparse(self.dims, self.q, self.k_pages, self.v_pages, self.page_table,
+                              self.seq_len, self.kept_idx, self.kept_cnt, self.scale, out, lse,
+                              self.ws, stream)
+        return out, lse
+
+    def decode_dense(self, out=None, lse=None, stream=None):
+        out = self.out if out is None else out
+        lse = self.lse if lse is None else lse
+        dsa.dsa_decode_dense(self.dims, self.q, self.k_pages, self.v_pages, self.page_table,
+                             self.seq_len, self.scale, out, lse, self.ws, stream)
+        return out, lse
+
+    def attention_mass(self, r_local=2, r_diag=2, with_offsets=True, stream=None):
+        mass = torch.empty((self.batch, self.hq, 4), dtype=torch.float32, device=self.device)
+        om = None
+        if with_offsets:
+            om = torch.empty((self.batch, self.hq, self.dims.max_window + 1), dtype=torch.float32,
+                             device=self.device)
+        dsa.dsa_attention_mass(self.dims, self.q, self.k_pages, self.page_table, self.seq_len,
+                               self.prompt_len, self.window, self.grid_w, r_local, r_diag,
+                               self.scale, mass, om, self.ws, stream)
+        return mass, om
+
+    def device_error(self) -> int:
+        return dsa.dsa_get_device_error(self.ws)
+
+    def check(self, what="libdsa"):
+        dsa.check_device_error(self.ws, what)

@@ -1,0 +1,88 @@
+"""The C-ABI library builds, loads, and exports every symbol include/dsa.h
+declares; host-side validation rejects bad arguments before touching a GPU.
+No compute call is made here (no GPU needed)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from kv_cache_serving_gb300 import build, dsa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dsa.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dsa_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_path():
+    names = declared_functions()
+    for want in ("dsa_build_index", "dsa_decode_sparse", "dsa_decode_dense",
+                 "dsa_attention_mass", "dsa_workspace_size", "dsa_status_string",
+                 "dsa_get_device_error"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = build.build()
+    out = subprocess.run(["nm", "-D", "--defined-only", lib], capture_output=True, text=True,
+                         check=True).stdout
+    exported = set(re.findall(r"\s[TW]\s+(dsa_\w+)", out))
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, missing
+    # C linkage: no mangled dsa entry points leak out as the only definition
+    assert all(not n.startswith("_Z") for n in exported)
+
+
+def test_host_only_calls():
+    assert dsa.dsa_version() >= 1
+    assert dsa.dsa_status_string(0) == "DSA_OK"
+    assert dsa.dsa_status_string(4) == "DSA_ERR_DEVICE"
+    assert dsa.dsa_status_string(99) == "DSA_ERR_UNKNOWN"
+    d = dsa.make_dims(4, 8, 2, 128, 100, 20, 96, 3, 400, "bf16", "bf16")
+    n = dsa.dsa_workspace_size(d)
+    assert n >= 256 + 4 * 8 * (128 + 2) * 4
+    assert n % 4 == 0
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("head_dim", 96, dsa.DSA_ERR_UNSUPPORTED),
+    ("page_size", 32, dsa.DSA_ERR_UNSUPPORTED),
+    ("hq", 6, dsa.DSA_ERR_INVALID_ARG),        # not a multiple of hkv=4
+    ("hq", 48, dsa.DSA_ERR_UNSUPPORTED),       # group 12 not built
+    ("mask_words", 2, dsa.DSA_ERR_INVALID_ARG),  # 64 bits < max_window 96
+    ("max_kept", 0, dsa.DSA_ERR_INVALID_ARG),
+    ("kv_dtype", 7, dsa.DSA_ERR_INVALID_ARG),
+])
+def test_dims_validation(field, value, status):
+    d = dsa.make_dims(2, 8, 4, 128, 10, 4, 96, 3, 50, "bf16", "bf16")
+    setattr(d, field, value)
+    lib = dsa._load()
+    assert lib.dsa_workspace_size(ctypes.byref(d)) == 0
+    fake = ctypes.c_void_p(1 << 20)   # never dereferenced: validation fails first
+    st = lib.dsa_decode_dense(ctypes.byref(d), fake, fake, fake, fake, fake, 0.1, fake, None,
+                              fake, None)
+    assert st == status
+
+
+def test_null_pointers_rejected_before_launch():
+    lib = dsa._load()
+    d = dsa.make_dims(2, 8, 4, 128, 10, 4, 96, 3, 50, "bf16", "bf16")
+    fake = ctypes.c_void_p(1 << 20)
+    D = ctypes.byref(d)
+    assert lib.dsa_decode_sparse(D, fake, fake, fake, fake, fake, None, fake, 0.1, fake, None,
+                                 fake, None) == dsa.DSA_ERR_INVALID_ARG
+    assert lib.dsa_build_index(D, fake, fake, None, fake, fake, fake, fake, None) == \
+        dsa.DSA_ERR_INVALID_ARG
+    assert lib.dsa_attention_mass(D, fake, fake, fake, fake, fake, fake, fake, -1, 2, 0.1, fake,
+                                  None, fake, None) == dsa.DSA_ERR_INVALID_ARG
+    # misaligned workspace
+    assert lib.dsa_decode_dense(D, fake, fake, fake, fake, fake, 0.1, fake, None,
+                                ctypes.c_void_p((1 << 20) + 8), None) == dsa.DSA_ERR_INVALID_ARG
+    code = ctypes.c_int32(0)
+    assert lib.dsa_get_device_error(None, None, ctypes.byref(code)) == dsa.DSA_ERR_INVALID_ARG

@@ -1,0 +1,312 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 CPU oracle.
+
+Bars (written here, derived in the design notes):
+  kept-index lists and counts: bit-exact;
+  fp32 inputs: max |gpu - oracle| <= 1e-5 on outputs;
+  bf16 q/KV (fp32 accumulation): max <= 2e-2 and mean <= 2e-3 on outputs;
+  lse: max <= 1e-4; attention-mass bins and per-offset weights: max <= 1e-5.
+Every oracle input comes from the seeded generators; config-5 masks come from
+the oracle's own attention mass.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from kv_cache_serving_gb300 import workloads as wl
+from kv_cache_serving_gb300.session import DecodeBatch
+
+pytestmark = pytest.mark.gpu
+
+F32_MAX = 1e-5
+BF16_MAX, BF16_MEAN = 2e-2, 2e-3
+LSE_MAX = 1e-4
+MASS_MAX = 1e-5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    assert torch.cuda.is_available(), "GPU tests need CUDA"
+    torch.cuda.init()
+
+
+def assert_outputs(gpu, ref, fp32):
+    gpu = np.asarray(gpu, dtype=np.float64).reshape(ref.shape)
+    assert np.isfinite(gpu).all()
+    err = np.abs(gpu - ref)
+    if fp32:
+        assert err.max() <= F32_MAX, err.max()
+    else:
+        assert err.max() <= BF16_MAX, err.max()
+        assert err.mean() <= BF16_MEAN, err.mean()
+
+
+def oracle_kept(w, mask=None):
+    mask = w["keep_mask"] if mask is None else mask
+    res = {}
+    for b in range(w["batch"]):
+        for hk in range(w["hkv"]):
+            res[b, hk] = oracle.kept_set(int(w["seq_len"][b]), int(w["prompt_len"][b]),
+                                         int(w["window"][b]), mask[b, hk])
+    return res
+
+
+def check_index(bt, w, mask=None):
+    bt.build_index()
+    torch.cuda.synchronize()
+    assert bt.device_error() == 0
+    cnt = bt.kept_cnt.cpu().numpy()
+    idx = bt.kept_idx.cpu().numpy()
+    for (b, hk), want in oracle_kept(w, mask).items():
+        assert cnt[b, hk] == len(want), (b, hk)
+        assert np.array_equal(idx[b, hk, :cnt[b, hk]], want), (b, hk)
+
+
+def oracle_inputs(w, mask=None):
+    d = dict(w)
+    if mask is not None:
+        d["keep_mask"] = mask
+    return d
+
+
+def run_both(w, mask=None, bh=None):
+    """GPU sparse + dense vs oracle on all (or the listed) (b, h) pairs."""
+    bt = DecodeBatch.from_workload(w, keep_mask=mask)
+    check_index(bt, w, mask)
+    fp32 = w["dtype"] == "f32"
+    inp = oracle_inputs(w, mask)
+    for sparse in (True, False):
+        out, lse = bt.decode_sparse() if sparse else bt.decode_dense()
+        torch.cuda.synchronize()
+        assert bt.device_error() == 0
+        o = out.cpu().numpy().reshape(-1, w["head_dim"])
+        l = lse.cpu().numpy().reshape(-1)
+        ref_o, ref_l = oracle.decode(inp, sparse=sparse, bh=bh)
+        if bh is not None:
+            sel = [b * w["hq"] + h for b, h in bh]
+            o, l = o[sel], l[sel]
+        assert_outputs(o, ref_o, fp32)
+        assert np.abs(l - ref_l).max() <= LSE_MAX
+    return bt
+
+
+def small_cfg(D, G, dtype, batch=5, hkv=2, Lmax=700, Pmax=100, W=64, seed=0, mask="random"):
+    return wl.Config(f"t-{D}-{G}-{dtype}", batch, hkv * G, hkv, D, dtype, (0, Pmax), (8,), None,
+                     W, ("abs", 1, Lmax), mask, band=2, seed=seed)
+
+
+# ---------------------------------------------------------------------------
+# small problems: every built (head_dim, group, dtype), several tiles, ragged
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+@pytest.mark.parametrize("D", [64, 128])
+def test_small_parity(D, G, dtype):
+    w = wl.generate(small_cfg(D, G, dtype, seed=D + G), spare_pages=3)
+    run_both(w)
+
+
+@pytest.mark.parametrize("D,G", [(64, 1), (128, 4)])
+def test_mixed_q_dtype(D, G):
+    w = wl.generate(small_cfg(D, G, "bf16", seed=7))
+    w["q"] = torch.randn(w["q"].shape, generator=torch.Generator().manual_seed(70))
+    run_both(w)   # q fp32, KV bf16
+
+
+def test_many_units_single_chunk_path():
+    # many short requests: each (request, kv head) fits one chunk, so the decode
+    # kernel writes the final output itself.
+    w = wl.generate(small_cfg(128, 1, "bf16", batch=96, hkv=8, Lmax=60, Pmax=20, W=32, seed=3))
+    run_both(w)
+
+
+# ---------------------------------------------------------------------------
+# the workloads
+# ---------------------------------------------------------------------------
+
+def test_tiny_fp32_every_decode_step():
+    cfg = wl.scaled(wl.CONFIGS[1], seq=("abs", 80, 80))
+    w = wl.generate(cfg)
+    golden = {}
+    with open(os.path.join(os.path.dirname(__file__), "golden", "tiny_fp32_kept_sets.txt")) as f:
+        for ln in f:
+            ln = ln.split("#")[0].strip()
+            if ln:
+                L, rows = ln.split(":")
+                golden[int(L)] = rows.split()
+    for L in range(17, 81):
+        w["seq_len"] = np.array([L], np.int32)
+        bt = run_both(w)
+        if L in golden:
+            from test_oracle_pins import expand_ranges
+            n = int(bt.kept_cnt[0, 0])
+            assert bt.kept_idx[0, 0, :n].cpu().tolist() == expand_ranges(golden[L])
+
+
+@pytest.mark.parametrize("cid", [2, 3, 4])
+def test_workload_reduced_batch(cid):
+    cfg = wl.CONFIGS[cid]
+    w = wl.generate(wl.scaled(cfg, batch=3 if cid == 4 else 6))
+    run_both(w)
+
+
+def top_mass_masks_from_oracle(w):
+    _, om = oracle.mass(w, r_local=2, r_diag=2)
+    om = om.reshape(w["batch"], w["hq"], -1)
+    return wl.top_mass_keep_mask(om, w["window"], w["hkv"], w["mask_words"],
+                                 band=w["config"].band, frac=w["config"].top_mass_frac)
+
+
+def test_mixed_serving_reduced_batch():
+    w = wl.generate(wl.scaled(wl.CONFIGS[5], batch=6))
+    run_both(w, mask=top_mass_masks_from_oracle(w))
+
+
+@pytest.mark.parametrize("cid", [2, 3, 4, 5])
+def test_workload_full_size_sampled(cid):
+    """Full-size batches in the launch configuration the benchmark uses; kept lists compared in full, outputs on 48 sampled (b, h) pairs."""
+    w = wl.generate(wl.CONFIGS[cid])
+    rng = np.random.default_rng(100 + cid)
+    bh = [(int(rng.integers(w["batch"])), int(rng.integers(w["hq"]))) for _ in range(48)]
+    mask = None
+    if cid == 5:
+        _, om = oracle.mass(w, bh=None, with_offsets=True)
+        om = om.reshape(w["batch"], w["hq"], -1)
+        mask = wl.top_mass_keep_mask(om, w["window"], w["hkv"], w["mask_words"])
+    run_both(w, mask=mask, bh=bh)
+
+
+# ---------------------------------------------------------------------------
+# invariants and edge cases
+# ---------------------------------------------------------------------------
+
+def test_skipped_rows_are_never_read():
+    w = wl.generate(wl.scaled(wl.CONFIGS[3], batch=4), spare_pages=5)
+    kept = oracle_kept(w)
+    bt = DecodeBatch.from_workload(w)
+    bt.build_index()
+    base = bt.decode_sparse()[0].clone()
+    for value in (float("nan"), float("inf"), 1e30):
+        p = wl.poison_unread(w, lambda b, hk: kept[b, hk], value)
+        bp = DecodeBatch.from_workload(p)
+        bp.build_index()
+        out = bp.decode_sparse()[0]
+        torch.cuda.synchronize()
+        assert torch.equal(out, base)
+
+
+def test_batch_zero_is_a_no_op():
+    w = wl.generate(small_cfg(64, 1, "bf16", batch=1))
+    bt = DecodeBatch.from_workload(w)
+    bt.dims.batch = 0
+    bt.build_index()
+    bt.decode_sparse()
+    bt.decode_dense()
+    torch.cuda.synchronize()
+    assert bt.device_error() == 0
+
+
+def test_first_token_and_prompt_only():
+    w = wl.generate(small_cfg(128, 2, "f32", batch=4, seed=9))
+    w["seq_len"] = np.array([1, 1, 5, 30], np.int32)
+    w["prompt_len"] = np.array([0, 3, 10, 30], np.int32)   # L <= P for the last two
+    run_both(w)
+
+
+def test_window_zero_and_empty_or_full_masks():
+    w = wl.generate(small_cfg(64, 4, "bf16", batch=4, seed=11, W=40))
+    w["window"] = np.array([0, 40, 40, 40], np.int32)
+    m = w["keep_mask"].copy()
+    m[1] = 0
+    m[2] = 0xFFFFFFFF
+    run_both(w, mask=m)
+
+
+def test_all_ones_mask_covering_sequence_equals_dense():
+    w = wl.generate(small_cfg(128, 1, "bf16", batch=3, Lmax=200, W=256, seed=12))
+    w["window"] = np.full(3, 256, np.int32)
+    m = np.full_like(w["keep_mask"], 0xFFFFFFFF)
+    bt = run_both(w, mask=m)
+    dense_ref, _ = oracle.decode(w, sparse=False)
+    out, _ = bt.decode_sparse()
+    assert_outputs(out.cpu().numpy().reshape(dense_ref.shape), dense_ref, fp32=False)
+
+
+def test_large_window_many_mask_words():
+    w = wl.generate(small_cfg(128, 8, "bf16", batch=3, Lmax=3000, Pmax=50, W=1000, seed=13))
+    run_both(w)
+
+
+# ---------------------------------------------------------------------------
+# attention mass
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("cid,batch,r_local,r_diag", [(2, 4, 2, 2), (4, 2, 1, 2), (5, 5, 2, 1),
+                                                      (1, 1, 2, 1)])
+def test_attention_mass_parity(cid, batch, r_local, r_diag):
+    w = wl.generate(wl.scaled(wl.CONFIGS[cid], batch=batch))
+    bt = DecodeBatch.from_workload(w)
+    mass, om = bt.attention_mass(r_local=r_local, r_diag=r_diag)
+    torch.cuda.synchronize()
+    assert bt.device_error() == 0
+    ref_m, ref_om = oracle.mass(w, r_local=r_local, r_diag=r_diag)
+    m = mass.cpu().numpy().reshape(-1, 4)
+    assert np.abs(m - ref_m).max() <= MASS_MAX
+    assert np.abs(m.sum(axis=1) - 1).max() <= 1e-5
+    assert np.abs(om.cpu().numpy().reshape(ref_om.shape) - ref_om).max() <= MASS_MAX
+
+
+# ---------------------------------------------------------------------------
+# invalid per-request data: flagged on the device, no fault
+# ---------------------------------------------------------------------------
+
+def test_device_errors_are_flagged():
+    w = wl.generate(small_cfg(64, 2, "bf16", batch=4, seed=21, Lmax=300))
+    bt = DecodeBatch.from_workload(w)
+
+    # seq_len 0 for request 1: dense output of that request is NaN, others fine
+    bt.seq_len[1] = 0
+    bt.decode_dense()
+    torch.cuda.synchronize()
+    assert bt.device_error() == 1
+    assert torch.isnan(bt.out[1]).all()
+    ref, _ = oracle.decode(w, sparse=False, bh=[(0, h) for h in range(w["hq"])])
+    assert_outputs(bt.out[0].cpu().numpy(), ref, fp32=False)
+    bt.seq_len[1] = int(w["seq_len"][1])
+    bt.ws.zero_()
+
+    # a page id outside the pool
+    bt.page_table[2, 0] = w["num_pages"] + 7
+    bt.decode_dense()
+    torch.cuda.synchronize()
+    assert bt.device_error() == 4
+    bt.page_table[2, 0] = int(w["page_table"][2, 0])
+    bt.ws.zero_()
+
+    # a window above max_window: build_index flags it and stores count 0,
+    # then decode_sparse flags the count
+    bt.window[3] = w["max_window"] + 1
+    bt.build_index()
+    torch.cuda.synchronize()
+    assert bt.device_error() == 3
+    assert int(bt.kept_cnt[3].max()) == 0
+    bt.ws.zero_()
+    bt.decode_sparse()
+    torch.cuda.synchronize()
+    assert bt.device_error() == 6
+    bt.window[3] = int(w["window"][3])
+    bt.ws.zero_()
+
+    # a kept index past the end of the sequence
+    bt.build_index()
+    bt.kept_idx[0, 1, 0] = int(w["seq_len"][0]) + 3
+    bt.decode_sparse()
+    torch.cuda.synchronize()
+    assert bt.device_error() == 5
+    bt.ws.zero_()
+
+    # everything valid again: clean run
+    run_both(w)
