@@ -162,9 +162,13 @@ class _Bound:
         P = _np(inp["prompt_len"], np.int32)
         W = _np(inp["window"], np.int32)
         gw = _np(inp.get("grid_w", np.ones(B)), np.int32)
-        mask = _np(inp["keep_mask"], np.uint32)
-        self.keep += [pt, L, P, W, gw, mask]
         self.max_window = int(inp["max_window"])
+        if inp.get("keep_mask") is None:      # attention mass reads no mask
+            words = int(inp.get("mask_words", max(1, (self.max_window + 31) // 32)))
+            mask = np.zeros((B, Hkv, words), dtype=np.uint32)
+        else:
+            mask = _np(inp["keep_mask"], np.uint32)
+        self.keep += [pt, L, P, W, gw, mask]
         self.pr = Problem(
             batch=B, hq=Hq, hkv=Hkv, head_dim=D, num_pages=num_pages,
             max_pages=pt.shape[1], max_window=self.max_window, mask_words=mask.shape[-1],
