@@ -67,7 +67,9 @@ typedef enum {
   DSA_ERR_UNSUPPORTED = 2, /* dtype, head_dim, page size or group not built    */
   DSA_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed             */
   DSA_ERR_DEVICE = 4,      /* the kernels flagged invalid per-request data     */
-  DSA_ERR_TIMEOUT = 5      /* a bounded on-device wait gave up                 */
+  DSA_ERR_TIMEOUT = 5,     /* a bounded on-device wait gave up                 */
+  DSA_ERR_SCRATCH_LIMIT = 6 /* the problem needs more than the fixed scratch of
+                               dsa_decode_sparse_noalloc                        */
 } dsa_status;
 
 typedef enum { DSA_F32 = 0, DSA_BF16 = 1 } dsa_dtype;
@@ -193,6 +195,46 @@ dsa_status dsa_attention_mass(const dsa_dims* dims, const void* q, const void* k
  */
 dsa_status dsa_decode_plan(const dsa_dims* dims, int32_t sparse, int32_t* chunk,
                            int32_t* num_chunks, int32_t* launches);
+
+/*
+ * dsa_decode_sparse_noalloc -- dsa_decode_sparse for callers that cannot
+ * allocate device memory.  The paper has no counterpart: this is a packaging
+ * variant of the same computation, for hosts that only lend us pointers.
+ *
+ * Who needs it: code that runs where device allocation is unavailable or
+ * forbidden -- a plugin inside an inference server whose memory pool owns all
+ * of the device memory and hands out nothing but tensors, a real-time decode
+ * loop where a cudaMalloc/cudaFree would synchronise the device and miss its
+ * deadline, or a host application that receives input and output buffers from
+ * another runtime and has no way to ask it for a scratch buffer of our size.
+ *
+ * Instead of a caller workspace, the call uses one scratch array that the
+ * library itself places in device memory at load time
+ * (DSA_NOALLOC_SCRATCH_BYTES on every GPU that loads the library, held until
+ * the process exits).  Arguments, layouts and results are those of
+ * dsa_decode_sparse, without `ws`; the caller still owns q, the KV pages, the
+ * page table, the kept lists and out / lse.
+ *   dev_error  device pointer to one int32, or NULL: receives this call's
+ *              device error code (DSA_DEV_*, 0 when clean), asynchronously on
+ *              `stream`.
+ * Returns DSA_ERR_SCRATCH_LIMIT, before touching the GPU, when the batch needs
+ * more scratch than DSA_NOALLOC_SCRATCH_BYTES (256 bytes plus
+ * batch * hq * chunks * (head_dim + 2) * 4, chunks as in dsa_decode_plan);
+ * use dsa_decode_sparse with a workspace then.
+ * Set-up: the first call on each device looks up the scratch array's device
+ * address (with that device current); make that first call before any stream
+ * capture on the device.
+ * Every call shares the one scratch array and clears the part that must start
+ * at zero; calls whose work overlaps on the GPU (other streams, other host
+ * threads) race on it and must be serialised by the caller.
+ * Allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
+ */
+#define DSA_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+dsa_status dsa_decode_sparse_noalloc(const dsa_dims* dims, const void* q, const void* k_pages,
+                                     const void* v_pages, const int32_t* page_table,
+                                     const int32_t* seq_len, const int32_t* kept_idx,
+                                     const int32_t* kept_cnt, float scale, float* out,
+                                     float* lse, int32_t* dev_error, void* stream);
 
 /*
  * Waits for `stream`, then reads the workspace error word into *code_out (one of

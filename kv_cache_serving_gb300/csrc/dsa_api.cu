@@ -3,6 +3,7 @@
 // computes attention; every step of the path runs in the kernels.
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
 
 #include <cuda_runtime.h>
 
@@ -177,6 +178,7 @@ const char* dsa_status_string(dsa_status status) {
     case DSA_ERR_CUDA: return "DSA_ERR_CUDA";
     case DSA_ERR_DEVICE: return "DSA_ERR_DEVICE";
     case DSA_ERR_TIMEOUT: return "DSA_ERR_TIMEOUT";
+    case DSA_ERR_SCRATCH_LIMIT: return "DSA_ERR_SCRATCH_LIMIT";
   }
   return "DSA_ERR_UNKNOWN";
 }
@@ -304,3 +306,69 @@ dsa_status dsa_clear_device_error(void* ws, void* stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// dsa_decode_sparse_noalloc: the sparse decode with its scratch (error word and
+// split-KV partials) in a fixed array the library owns, for callers that cannot
+// allocate device memory.
+// ---------------------------------------------------------------------------
+namespace dsa {
+namespace {
+
+// Every GPU that loads the library holds this array until the process exits.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[DSA_NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {nullptr};
+
+// Device address of g_noalloc_scratch on the current device (looked up once per
+// device: the host-side name is only a stand-in, never a device address).
+dsa_status noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DSA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+      return DSA_ERR_CUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return DSA_OK;
+}
+
+}  // namespace
+}  // namespace dsa
+
+extern "C" dsa_status dsa_decode_sparse_noalloc(const dsa_dims* dims, const void* q,
+                                                const void* k_pages, const void* v_pages,
+                                                const int32_t* page_table, const int32_t* seq_len,
+                                                const int32_t* kept_idx, const int32_t* kept_cnt,
+                                                float scale, float* out, float* lse,
+                                                int32_t* dev_error, void* stream) {
+  const dsa_status st = check_dims(dims);
+  if (st != DSA_OK) return st;
+  if (!q || !k_pages || !v_pages || !page_table || !seq_len || !kept_idx || !kept_cnt || !out)
+    return DSA_ERR_INVALID_ARG;
+  // Scratch this call needs: the header plus one partial per (request, query
+  // head, chunk), counted even when a single chunk leaves it unused.
+  const Plan plan = decode_plan(dims, true);
+  const size_t need = kWsHeader + static_cast<size_t>(dims->batch) * dims->hq *
+                                      static_cast<size_t>(plan.num_chunks > 0 ? plan.num_chunks
+                                                                              : 1) *
+                                      (dims->head_dim + 2) * sizeof(float);
+  if (need > DSA_NOALLOC_SCRATCH_BYTES) return DSA_ERR_SCRATCH_LIMIT;
+  void* ws = nullptr;
+  const dsa_status su = noalloc_scratch(&ws);
+  if (su != DSA_OK) return su;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the error word (and the rest of the header) must start at zero
+  if (cudaMemsetAsync(ws, 0, kWsHeader, s) != cudaSuccess) return DSA_ERR_CUDA;
+  const dsa_status rc = decode_common(dims, true, q, k_pages, v_pages, page_table, seq_len,
+                                      kept_idx, kept_cnt, scale, out, lse, ws, stream);
+  if (rc != DSA_OK) return rc;
+  if (dev_error != nullptr &&
+      cudaMemcpyAsync(dev_error, ws, sizeof(int32_t), cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+    return DSA_ERR_CUDA;
+  return DSA_OK;
+}

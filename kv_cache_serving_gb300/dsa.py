@@ -14,7 +14,8 @@ import os
 import torch
 
 DSA_OK, DSA_ERR_INVALID_ARG, DSA_ERR_UNSUPPORTED, DSA_ERR_CUDA, DSA_ERR_DEVICE, \
-    DSA_ERR_TIMEOUT = range(6)
+    DSA_ERR_TIMEOUT, DSA_ERR_SCRATCH_LIMIT = range(7)
+NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 DSA_F32, DSA_BF16 = 0, 1
 DEV_ERRORS = {0: "OK", 1: "BAD_SEQ_LEN", 2: "BAD_PROMPT", 3: "BAD_WINDOW", 4: "BAD_PAGE",
               5: "BAD_INDEX", 6: "BAD_COUNT", 7: "TIMEOUT", 8: "BAD_GRID_W"}
@@ -68,6 +69,7 @@ def _load():
         "dsa_attention_mass": ([D, P, P, P, P, P, P, P, I32, I32, F32, P, P, P, P], I32),
         "dsa_decode_plan": ([D, I32, ctypes.POINTER(I32), ctypes.POINTER(I32),
                              ctypes.POINTER(I32)], I32),
+        "dsa_decode_sparse_noalloc": ([D, P, P, P, P, P, P, P, F32, P, P, P, P], I32),
         "dsa_get_device_error": ([P, P, ctypes.POINTER(I32)], I32),
         "dsa_clear_device_error": ([P, P], I32),
     }
@@ -162,6 +164,20 @@ def dsa_decode_sparse(dims, q, k_pages, v_pages, page_table, seq_len, kept_idx, 
         _ptr(seq_len, _I32, "seq_len"), _ptr(kept_idx, _I32, "kept_idx"),
         _ptr(kept_cnt, _I32, "kept_cnt"), float(scale), _ptr(out, torch.float32, "out"),
         _ptr(lse, torch.float32, "lse"), _ptr(ws), _stream(stream)), "dsa_decode_sparse")
+
+
+def dsa_decode_sparse_noalloc(dims, q, k_pages, v_pages, page_table, seq_len, kept_idx,
+                              kept_cnt, scale, out, lse, dev_error=None, stream=None):
+    """dsa_decode_sparse with the library's own fixed scratch instead of a caller
+    workspace, for callers that cannot allocate device memory.  dev_error (a
+    one-element int32 CUDA tensor, or None) receives the call's device error code."""
+    _check(_load().dsa_decode_sparse_noalloc(
+        ctypes.byref(dims), _ptr(q, _QKV, "q"), _ptr(k_pages, _QKV, "k_pages"),
+        _ptr(v_pages, _QKV, "v_pages"), _ptr(page_table, _I32, "page_table"),
+        _ptr(seq_len, _I32, "seq_len"), _ptr(kept_idx, _I32, "kept_idx"),
+        _ptr(kept_cnt, _I32, "kept_cnt"), float(scale), _ptr(out, torch.float32, "out"),
+        _ptr(lse, torch.float32, "lse"), _ptr(dev_error, _I32, "dev_error"), _stream(stream)),
+        "dsa_decode_sparse_noalloc")
 
 
 def dsa_decode_dense(dims, q, k_pages, v_pages, page_table, seq_len, scale, out, lse, ws,

@@ -1,0 +1,70 @@
+"""dsa_decode_sparse_noalloc: the sparse decode for callers that cannot allocate
+device memory (a plugin whose host owns the whole memory pool, a real-time loop
+that must not synchronise on cudaMalloc, a program that is only lent buffers).
+
+It must give the results of dsa_decode_sparse -- same kernels, scratch in a
+fixed array inside the library instead of a caller workspace -- call after call,
+and refuse, before touching the GPU, batches whose scratch would not fit.
+This file is collected last on purpose: a run that stops at the first failure
+has run every other test before reaching it.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from kv_cache_serving_gb300 import dsa
+from kv_cache_serving_gb300 import workloads as wl
+
+BF16_MAX, BF16_MEAN, LSE_MAX = 2e-2, 2e-3, 1e-4
+
+
+def test_noalloc_rejects_batches_beyond_its_scratch():
+    # Host-side check only: the pointers are never dereferenced, because a
+    # batch of 200000 x 32 heads needs far more than the fixed scratch.
+    d = dsa.make_dims(200000, 32, 8, 128, 1000, 300, 192, 6, 705, "bf16", "bf16")
+    need = 200000 * 32 * (128 + 2) * 4
+    assert need > dsa.NOALLOC_SCRATCH_BYTES
+    fake = ctypes.c_void_p(1 << 20)
+    st = dsa._load().dsa_decode_sparse_noalloc(ctypes.byref(d), fake, fake, fake, fake, fake,
+                                                fake, fake, 0.1, fake, None, None, None)
+    assert st == dsa.DSA_ERR_SCRATCH_LIMIT
+    assert dsa.dsa_status_string(st) == "DSA_ERR_SCRATCH_LIMIT"
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("cid,batch", [(3, 12), (5, 16)])
+def test_noalloc_matches_workspace_entry_point(cid, batch):
+    from kv_cache_serving_gb300.session import DecodeBatch
+    assert torch.cuda.is_available()
+    w = wl.generate(wl.scaled(wl.CONFIGS[cid], batch=batch))
+    mask = w["keep_mask"]
+    if mask is None:   # mixed-serving masks: band plus a fixed pattern of offsets
+        mask = np.zeros((w["batch"], w["hkv"], w["mask_words"]), np.uint32)
+        for b in range(w["batch"]):
+            offs = list(range(1, 9)) + list(range(9, int(w["window"][b]) + 1, 3))
+            mask[b, :] = wl.offsets_to_bits(offs, int(w["window"][b]), w["mask_words"])
+    bt = DecodeBatch.from_workload(w, keep_mask=mask)
+    bt.build_index()
+    ref_out, ref_lse = bt.decode_sparse()
+    ref_out, ref_lse = ref_out.clone(), ref_lse.clone()
+    torch.cuda.synchronize()
+    assert bt.device_error() == 0
+    _, chunks, _ = dsa.dsa_decode_plan(bt.dims, True)
+    assert 256 + w["batch"] * w["hq"] * chunks * (w["head_dim"] + 2) * 4 <= \
+        dsa.NOALLOC_SCRATCH_BYTES
+
+    for call in range(2):   # the scratch keeps the previous call's contents
+        out = torch.full_like(ref_out, float("nan"))
+        lse = torch.full_like(ref_lse, float("nan"))
+        err = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+        dsa.dsa_decode_sparse_noalloc(bt.dims, bt.q, bt.k_pages, bt.v_pages, bt.page_table,
+                                      bt.seq_len, bt.kept_idx, bt.kept_cnt, bt.scale, out, lse,
+                                      err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0, call
+        diff = (out - ref_out).abs()
+        assert torch.isfinite(out).all()
+        assert diff.max().item() <= BF16_MAX and diff.mean().item() <= BF16_MEAN, call
+        assert (lse - ref_lse).abs().max().item() <= LSE_MAX, call
