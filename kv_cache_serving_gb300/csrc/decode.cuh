@@ -109,33 +109,43 @@ __global__ void __launch_bounds__(DecodeTiling<D, KV, G>::NW * 32)
                               : nullptr;
   const int32_t* pt = a.page_table + static_cast<size_t>(b) * a.max_pages;
 
+  const int my_tiles = warp < ntiles ? (ntiles - warp + NW - 1) / NW : 0;
+
+  // Row addresses are produced by a software pipeline so that no copy waits on
+  // the dependent loads kept index -> page id: the kept index of a tile is
+  // loaded two tiles before its copy is issued, its page id one tile before.
+  // Lane l serves row l % T of a tile: lanes [0,T) copy K rows, [T,2T) V rows
+  // (with T = 32 every lane copies both).
+  const int my_r = lane & (T - 1);
+  auto tile_r0 = [&](int t) { return row0 + (warp + t * NW) * T; };
+  auto tile_rows = [&](int t) { return min(T, row1 - tile_r0(t)); };
+  auto load_j = [&](int t) -> int {
+    if (t >= my_tiles || my_r >= tile_rows(t)) return 0;
+    const int r = tile_r0(t) + my_r;
+    return SPARSE ? __ldg(idx + r) : r;
+  };
+  auto load_pg = [&](int t, int& j) -> int {
+    if (t >= my_tiles || my_r >= tile_rows(t)) return 0;
+    if (static_cast<unsigned>(j) >= static_cast<unsigned>(L)) {
+      set_error(a.err, DSA_DEV_BAD_INDEX);
+      j = 0;
+    }
+    return __ldg(pt + (j >> 4));
+  };
   // Enqueue the bulk copies of local tile t (rows of global tile warp + t*NW).
-  auto issue = [&](int t, int stage) {
-    const int tr0 = row0 + (warp + t * NW) * T;
-    const int nrows = min(T, row1 - tr0);
+  auto issue = [&](int t, int stage, int j, int pg) {
+    const int nrows = tile_rows(t);
     if (lane == 0) mbar_arrive_expect_tx(&bars[stage], static_cast<uint32_t>(nrows * 2 * kRowBytes));
     __syncwarp();
-#pragma unroll
-    for (int u = 0; u < (2 * T + 31) / 32; ++u) {
-      const int x = lane + 32 * u;
-      const int r = x & (T - 1);
-      if (x < 2 * T && r < nrows) {
-        int j = SPARSE ? idx[tr0 + r] : tr0 + r;
-        if (static_cast<unsigned>(j) >= static_cast<unsigned>(L)) {
-          set_error(a.err, DSA_DEV_BAD_INDEX);
-          j = 0;
-        }
-        int pg = pt[j >> 4];
-        if (static_cast<unsigned>(pg) >= static_cast<unsigned>(a.num_pages)) {
-          set_error(a.err, DSA_DEV_BAD_PAGE);
-          pg = 0;
-        }
-        const size_t off =
-            ((static_cast<size_t>(pg) * kPage + (j & (kPage - 1))) * a.hkv + hk) * D;
-        const bool is_v = x >= T;
-        KV* dst = (is_v ? vst : kst) + (static_cast<size_t>(stage) * T + r) * D;
-        bulk_copy_g2s(dst, (is_v ? vg : kg) + off, kRowBytes, &bars[stage]);
+    if (my_r < nrows && (T == 32 || lane < 2 * T)) {
+      if (static_cast<unsigned>(pg) >= static_cast<unsigned>(a.num_pages)) {
+        set_error(a.err, DSA_DEV_BAD_PAGE);
+        pg = 0;
       }
+      const size_t off = ((static_cast<size_t>(pg) * kPage + (j & (kPage - 1))) * a.hkv + hk) * D;
+      const size_t dst = (static_cast<size_t>(stage) * T + my_r) * D;
+      if (T == 32 || lane < T) bulk_copy_g2s(kst + dst, kg + off, kRowBytes, &bars[stage]);
+      if (T == 32 || lane >= T) bulk_copy_g2s(vst + dst, vg + off, kRowBytes, &bars[stage]);
     }
   };
 
@@ -154,8 +164,17 @@ __global__ void __launch_bounds__(DecodeTiling<D, KV, G>::NW * 32)
     for (int e = 0; e < DPL; ++e) acc[h][e] = 0.f;
   }
 
-  const int my_tiles = warp < ntiles ? (ntiles - warp + NW - 1) / NW : 0;
-  for (int t = 0; t < S && t < my_tiles; ++t) issue(t, t);
+  // prologue: kept indices of tiles 0..S+1, page ids of tiles 0..S, copies of
+  // tiles 0..S-1 (two dependent round trips in all)
+  int jr[S + 2], pr[S + 1];
+#pragma unroll
+  for (int t = 0; t < S + 2; ++t) jr[t] = load_j(t);
+#pragma unroll
+  for (int t = 0; t < S + 1; ++t) pr[t] = load_pg(t, jr[t]);
+#pragma unroll
+  for (int t = 0; t < S; ++t)
+    if (t < my_tiles) issue(t, t, jr[t], pr[t]);
+  int j0 = jr[S], pg0 = pr[S], j1 = jr[S + 1];  // next tile to issue: S
 
   const int myrow = RowMap<T>::row(lane);
   const bool own = RowMap<T>::owner(lane);
@@ -218,7 +237,11 @@ __global__ void __launch_bounds__(DecodeTiling<D, KV, G>::NW * 32)
     }
     __syncwarp();
     fence_proxy_async_smem();
-    if (t + S < my_tiles) issue(t + S, stage);
+    if (t + S < my_tiles) issue(t + S, stage, j0, pg0);
+    // advance the address pipeline: page id of tile t+S+1, kept index of t+S+2
+    j0 = j1;
+    pg0 = load_pg(t + S + 1, j0);
+    j1 = load_j(t + S + 2);
   }
   if (failed_at >= 0) {
     // Give the copies still in flight a bounded chance to land before exiting.
