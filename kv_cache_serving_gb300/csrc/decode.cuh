@@ -15,12 +15,17 @@
 // (the row's page comes from the page table), completing on the stage's
 // mbarrier; compute never waits for anything but its own copies.
 //
-// Per tile, a warp computes the T x G scores with each lane holding D/32
-// dimensions, reduce-scatters them so that lane l owns row l >> shift, runs
-// the online-softmax update in the log2 domain (q is pre-scaled by
-// scale*log2(e)), and accumulates p_j v_j into per-lane fp32 accumulators.
-// The CTA merges its warps' (m, l, acc) in shared memory and either writes the
-// final output (one chunk) or a partial that merge_kernel combines.
+// Per tile a warp works on 4 rows at a time: lane (g = lane/8, j = lane%8)
+// handles rows g, g+4, ... of the tile and 16-byte vectors j, j+8, ... of each
+// row (byte offsets 16 j + 128 u: conflict-free shared loads).  A row's G dot
+// products are summed over its 8 lanes by a 3-step butterfly, so every lane
+// holds the scores of its own rows; with bf16 q and K the products use the
+// mixed-precision fma.rn.f32.bf16 (bf16 x bf16 exact, fp32 accumulation).  The
+// online softmax runs in the log2 domain (scores times scale*log2 e); p_j v_j
+// accumulates into per-lane fp32 partial sums over the lane's rows, and the 4
+// row groups are summed once, at the end.  The CTA merges its warps' (m, l,
+// acc) in shared memory and either writes the final output (one chunk) or a
+// partial that merge_kernel combines.
 #pragma once
 
 #include <math.h>
@@ -30,25 +35,73 @@
 
 namespace dsa {
 
+// Build-time tuning knobs: stages per warp and warps per CTA.
+#ifndef DSA_DECODE_STAGES
+#define DSA_DECODE_STAGES 3
+#endif
+#ifndef DSA_DECODE_WARPS
+#define DSA_DECODE_WARPS 4
+#endif
+
 template <int D, typename KV, int G>
 struct DecodeTiling {
-  static constexpr int kRowBytes = D * static_cast<int>(sizeof(KV));
-  static constexpr int kTByBytes = 8192 / (2 * kRowBytes);  // K+V of one stage = 8 KB
-  static constexpr int kTByRegs = 64 / G;                   // G*T score partials per lane
-  static constexpr int kT0 = kTByBytes < kTByRegs ? kTByBytes : kTByRegs;
+  static constexpr int kElt = static_cast<int>(sizeof(KV));
+  static constexpr int kRowBytes = D * kElt;
+  static constexpr int kT0 = 8192 / (2 * kRowBytes);  // K+V of one stage = 8 KB
   static constexpr int T = kT0 > 32 ? 32 : (kT0 < 8 ? 8 : kT0);
-  static constexpr int S = 3;   // stages per warp
-  static constexpr int NW = 4;  // warps per CTA
-  static constexpr int kDPL = D / 32;
+  static constexpr int S = DSA_DECODE_STAGES;  // stages per warp
+  static constexpr int NW = DSA_DECODE_WARPS;  // warps per CTA
+  static constexpr int kVE = 16 / kElt;        // elements per 16-byte vector
+  static constexpr int kEPL = D / 8;           // elements of a row per lane
+  static constexpr int kNV = kEPL / kVE;       // 16-byte vectors of a row per lane
+  static constexpr int kRPL = T / 4;           // rows of a tile per lane
   static constexpr int kStageBytes = 2 * T * kRowBytes;
   static constexpr int kWarpBytes = S * kStageBytes;
   static constexpr int kBarOff = NW * kWarpBytes;
-  static constexpr int kPOff = kBarOff + NW * S * 8;
-  static constexpr int kMOff = kPOff + NW * G * T * 4;
+  static constexpr int kMOff = kBarOff + NW * S * 8;
   static constexpr int kSmem = kMOff + NW * G * (D + 2) * 4;
   static_assert(kStageBytes % 128 == 0, "stage alignment");
-  static_assert(kPOff % 16 == 0, "p buffer alignment");
+  static_assert(kEPL % kVE == 0 && kRowBytes % 128 == 0, "row vector layout");
+  // Element of a row held in slot w of vector u by lane j of a row group.
+  __device__ __forceinline__ static int elem(int u, int j, int w) {
+    return u * (128 / kElt) + j * kVE + w;
+  }
 };
+
+// acc += lo(k2)*lo(q2) + hi(k2)*hi(q2), bf16 operands, fp32 accumulation (the
+// product of two bf16 values is exact in fp32).
+__device__ __forceinline__ float fma2_bf16(uint32_t k2, uint32_t q2, float acc) {
+  asm("{\n\t.reg .b16 kl, kh, ql, qh;\n\t"
+      "mov.b32 {kl, kh}, %1;\n\t"
+      "mov.b32 {ql, qh}, %2;\n\t"
+      "fma.rn.f32.bf16 %0, kl, ql, %0;\n\t"
+      "fma.rn.f32.bf16 %0, kh, qh, %0;\n\t}"
+      : "+f"(acc)
+      : "r"(k2), "r"(q2));
+  return acc;
+}
+
+// The kVE elements of a 16-byte vector as fp32.
+template <typename KV>
+__device__ __forceinline__ void vec_to_f32(const uint4& v, float* o);
+template <>
+__device__ __forceinline__ void vec_to_f32<bf16_t>(const uint4& v, float* o) {
+  o[0] = bf16_lo(v.x);
+  o[1] = bf16_hi(v.x);
+  o[2] = bf16_lo(v.y);
+  o[3] = bf16_hi(v.y);
+  o[4] = bf16_lo(v.z);
+  o[5] = bf16_hi(v.z);
+  o[6] = bf16_lo(v.w);
+  o[7] = bf16_hi(v.w);
+}
+template <>
+__device__ __forceinline__ void vec_to_f32<float>(const uint4& v, float* o) {
+  o[0] = __uint_as_float(v.x);
+  o[1] = __uint_as_float(v.y);
+  o[2] = __uint_as_float(v.z);
+  o[3] = __uint_as_float(v.w);
+}
 
 // Rows of the work list of (b, hk), or a negative device error code.  Shared
 // by the decode and merge kernels so that both take the same decision.
@@ -61,11 +114,13 @@ __device__ __forceinline__ int request_rows(const DecodeLaunch& a, int b, int hk
   return n;
 }
 
-template <int D, typename KV, int G, bool SPARSE>
+// QMIX: q and K are bf16 and the dot products use the mixed-precision FMA.
+template <int D, typename KV, int G, bool SPARSE, bool QMIX>
 __global__ void __launch_bounds__(DecodeTiling<D, KV, G>::NW * 32)
     decode_kernel(const DecodeLaunch a) {
   using Tl = DecodeTiling<D, KV, G>;
-  constexpr int T = Tl::T, S = Tl::S, NW = Tl::NW, DPL = Tl::kDPL;
+  constexpr int T = Tl::T, S = Tl::S, NW = Tl::NW;
+  constexpr int EPL = Tl::kEPL, NV = Tl::kNV, VE = Tl::kVE, RPL = Tl::kRPL;
   constexpr int kRowBytes = Tl::kRowBytes;
   extern __shared__ __align__(128) unsigned char smem[];
 
@@ -93,8 +148,8 @@ __global__ void __launch_bounds__(DecodeTiling<D, KV, G>::NW * 32)
   KV* kst = reinterpret_cast<KV*>(smem + warp * Tl::kWarpBytes);  // [S][T][D]
   KV* vst = kst + S * T * D;                                      // [S][T][D]
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Tl::kBarOff) + warp * S;
-  float* pbuf = reinterpret_cast<float*>(smem + Tl::kPOff) + warp * G * T;  // [G][T]
-  float* mbuf = reinterpret_cast<float*>(smem + Tl::kMOff);                 // [NW][G][D+2]
+  float* mbuf = reinterpret_cast<float*>(smem + Tl::kMOff);  // [NW][G][D+2]
+  const int grp = lane >> 3, jl = lane & 7;                  // row group, lane in group
 
   if (lane == 0) {
 #pragma unroll
@@ -149,19 +204,42 @@ __global__ void __launch_bounds__(DecodeTiling<D, KV, G>::NW * 32)
     }
   };
 
-  float qv[G][DPL];
+  // this lane's elements of the G query vectors: packed bf16 pairs (QMIX) or fp32
+  constexpr int kQW = QMIX ? EPL / 2 : EPL;
+  uint32_t qv[G][kQW];
 #pragma unroll
-  for (int h = 0; h < G; ++h)
-    load_q<DPL>(a.q, a.q_bf16 != 0, (static_cast<size_t>(b) * a.hq + hk * G + h) * D + lane * DPL,
-                a.scale_log2, qv[h]);
+  for (int h = 0; h < G; ++h) {
+    const size_t qrow = (static_cast<size_t>(b) * a.hq + hk * G + h) * D;
+    if (QMIX) {
+      const uint4* q4 = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.q) + qrow);
+#pragma unroll
+      for (int u = 0; u < NV; ++u) {
+        const uint4 v = __ldg(q4 + u * 8 + jl);
+        qv[h][4 * u] = v.x;
+        qv[h][4 * u + 1] = v.y;
+        qv[h][4 * u + 2] = v.z;
+        qv[h][4 * u + 3] = v.w;
+      }
+    } else {
+#pragma unroll
+      for (int u = 0; u < NV; ++u)
+#pragma unroll
+        for (int w = 0; w < VE; ++w) {
+          const size_t e = qrow + Tl::elem(u, jl, w);
+          const float x = a.q_bf16 ? bf16_lo(reinterpret_cast<const uint16_t*>(a.q)[e])
+                                   : reinterpret_cast<const float*>(a.q)[e];
+          qv[h][u * VE + w] = __float_as_uint(x);
+        }
+    }
+  }
 
-  float m_run[G], l_run[G], acc[G][DPL];
+  float m_run[G], l_run[G], acc[G][EPL];
 #pragma unroll
   for (int h = 0; h < G; ++h) {
     m_run[h] = -INFINITY;
     l_run[h] = 0.f;
 #pragma unroll
-    for (int e = 0; e < DPL; ++e) acc[h][e] = 0.f;
+    for (int e = 0; e < EPL; ++e) acc[h][e] = 0.f;
   }
 
   // prologue: kept indices of tiles 0..S+1, page ids of tiles 0..S, copies of
@@ -176,8 +254,6 @@ __global__ void __launch_bounds__(DecodeTiling<D, KV, G>::NW * 32)
     if (t < my_tiles) issue(t, t, jr[t], pr[t]);
   int j0 = jr[S], pg0 = pr[S], j1 = jr[S + 1];  // next tile to issue: S
 
-  const int myrow = RowMap<T>::row(lane);
-  const bool own = RowMap<T>::owner(lane);
   int failed_at = -1;
   for (int t = 0; t < my_tiles; ++t) {
     const int stage = t % S;
@@ -186,54 +262,90 @@ __global__ void __launch_bounds__(DecodeTiling<D, KV, G>::NW * 32)
       break;
     }
     const int nrows = min(T, row1 - (row0 + (warp + t * NW) * T));
-    const KV* kt = kst + static_cast<size_t>(stage) * T * D + lane * DPL;
-    const KV* vt = vst + static_cast<size_t>(stage) * T * D + lane * DPL;
+    const unsigned char* kt = reinterpret_cast<const unsigned char*>(kst + static_cast<size_t>(stage) * T * D);
+    const unsigned char* vt = reinterpret_cast<const unsigned char*>(vst + static_cast<size_t>(stage) * T * D);
 
-    // scores: partial dot products over this lane's dimensions
-    float part[G][T];
+    // scores of this lane's rows (rows past nrows hold stale data: masked)
+    float sc[G][RPL];
 #pragma unroll
-    for (int r = 0; r < T; ++r) {
-      float kf[DPL];
-      Vec<KV, DPL>::load(kt + r * D, kf);
+    for (int i = 0; i < RPL; ++i) {
+      const int r = grp + 4 * i;
+      uint4 kv[NV];
+#pragma unroll
+      for (int u = 0; u < NV; ++u)
+        kv[u] = *reinterpret_cast<const uint4*>(kt + r * kRowBytes + 128 * u + 16 * jl);
 #pragma unroll
       for (int h = 0; h < G; ++h) {
-        float s = 0.f;
+        float d0 = 0.f, d1 = 0.f;
+        if (QMIX) {
 #pragma unroll
-        for (int e = 0; e < DPL; ++e) s = fmaf(qv[h][e], kf[e], s);
-        part[h][r] = s;
+          for (int u = 0; u < NV; ++u) {
+            d0 = fma2_bf16(kv[u].x, qv[h][4 * u], d0);
+            d1 = fma2_bf16(kv[u].y, qv[h][4 * u + 1], d1);
+            d0 = fma2_bf16(kv[u].z, qv[h][4 * u + 2], d0);
+            d1 = fma2_bf16(kv[u].w, qv[h][4 * u + 3], d1);
+          }
+        } else {
+#pragma unroll
+          for (int u = 0; u < NV; ++u) {
+            float kf[VE];
+            vec_to_f32<KV>(kv[u], kf);
+#pragma unroll
+            for (int w = 0; w < VE; w += 2) {
+              d0 = fmaf(__uint_as_float(qv[h][u * VE + w]), kf[w], d0);
+              d1 = fmaf(__uint_as_float(qv[h][u * VE + w + 1]), kf[w + 1], d1);
+            }
+          }
+        }
+        float d = d0 + d1;
+        d += __shfl_xor_sync(0xffffffffu, d, 4);
+        d += __shfl_xor_sync(0xffffffffu, d, 2);
+        d += __shfl_xor_sync(0xffffffffu, d, 1);
+        sc[h][i] = (r < nrows) ? d * a.scale_log2 : -INFINITY;
       }
     }
-    // online softmax (log2 domain); rows past nrows hold stale data and are masked
+    // online softmax (log2 domain); the max is over the whole warp's rows
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-      float s = reduce_scatter<T>(part[h], lane);
-      s = (myrow < nrows) ? s : -INFINITY;
-      const float mnew = fmaxf(m_run[h], warp_max(s));
+      float tmax = sc[h][0];
+#pragma unroll
+      for (int i = 1; i < RPL; ++i) tmax = fmaxf(tmax, sc[h][i]);
+      tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 8));
+      tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
+      const float mnew = fmaxf(m_run[h], tmax);
       const float alpha = exp2f(m_run[h] - mnew);
-      const float p = exp2f(s - mnew);
-      l_run[h] = l_run[h] * alpha + (own ? p : 0.f);
+      float psum = 0.f;
 #pragma unroll
-      for (int e = 0; e < DPL; ++e) acc[h][e] *= alpha;
+      for (int i = 0; i < RPL; ++i) {
+        sc[h][i] = exp2f(sc[h][i] - mnew);
+        psum += sc[h][i];
+      }
+      l_run[h] = l_run[h] * alpha + psum;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) acc[h][e] *= alpha;
       m_run[h] = mnew;
-      if (own) pbuf[h * T + myrow] = p;
     }
-    __syncwarp();
-    // acc += p_j v_j
-    auto pv_row = [&](int r) {
-      float vf[DPL];
-      Vec<KV, DPL>::load(vt + r * D, vf);
+    // acc += p_r v_r over this lane's rows
+    auto pv_row = [&](int i) {
+      const int r = grp + 4 * i;
 #pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float p = pbuf[h * T + r];
+      for (int u = 0; u < NV; ++u) {
+        const uint4 vv = *reinterpret_cast<const uint4*>(vt + r * kRowBytes + 128 * u + 16 * jl);
+        float vf[VE];
+        vec_to_f32<KV>(vv, vf);
 #pragma unroll
-        for (int e = 0; e < DPL; ++e) acc[h][e] = fmaf(p, vf[e], acc[h][e]);
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+          for (int w = 0; w < VE; ++w) acc[h][u * VE + w] = fmaf(sc[h][i], vf[w], acc[h][u * VE + w]);
       }
     };
     if (nrows == T) {
 #pragma unroll
-      for (int r = 0; r < T; ++r) pv_row(r);
+      for (int i = 0; i < RPL; ++i) pv_row(i);
     } else {
-      for (int r = 0; r < nrows; ++r) pv_row(r);
+#pragma unroll
+      for (int i = 0; i < RPL; ++i)
+        if (grp + 4 * i < nrows) pv_row(i);
     }
     __syncwarp();
     fence_proxy_async_smem();
@@ -250,13 +362,24 @@ __global__ void __launch_bounds__(DecodeTiling<D, KV, G>::NW * 32)
       mbar_wait(&bars[t % S], static_cast<uint32_t>(t / S) & 1u);
   }
 
-  // merge the warps of this CTA
+  // sum the 4 row groups of the warp, then merge the warps of this CTA
   float* mw = mbuf + static_cast<size_t>(warp) * G * (D + 2);
 #pragma unroll
   for (int h = 0; h < G; ++h) {
+    float l = l_run[h];
+    l += __shfl_xor_sync(0xffffffffu, l, 8);
+    l += __shfl_xor_sync(0xffffffffu, l, 16);
 #pragma unroll
-    for (int e = 0; e < DPL; ++e) mw[h * (D + 2) + lane * DPL + e] = acc[h][e];
-    const float l = warp_sum(l_run[h]);
+    for (int e = 0; e < EPL; ++e) {
+      acc[h][e] += __shfl_xor_sync(0xffffffffu, acc[h][e], 8);
+      acc[h][e] += __shfl_xor_sync(0xffffffffu, acc[h][e], 16);
+    }
+    if (grp == 0) {
+#pragma unroll
+      for (int u = 0; u < NV; ++u)
+#pragma unroll
+        for (int w = 0; w < VE; ++w) mw[h * (D + 2) + Tl::elem(u, jl, w)] = acc[h][u * VE + w];
+    }
     if (lane == 0) {
       mw[h * (D + 2) + D] = m_run[h];
       mw[h * (D + 2) + D + 1] = l;
@@ -325,10 +448,19 @@ __global__ void __launch_bounds__(128) merge_kernel(const DecodeLaunch a) {
   if (a.lse != nullptr && lane == 0) a.lse[gw] = (mstar + log2f(ls)) * kLn2;
 }
 
-template <int D, typename KV, int G, bool SPARSE>
+template <typename KV>
+struct IsBf16 {
+  static constexpr bool value = false;
+};
+template <>
+struct IsBf16<bf16_t> {
+  static constexpr bool value = true;
+};
+
+template <int D, typename KV, int G, bool SPARSE, bool QMIX>
 cudaError_t launch_decode_one(const DecodeLaunch& a, cudaStream_t s) {
   using Tl = DecodeTiling<D, KV, G>;
-  auto kern = decode_kernel<D, KV, G, SPARSE>;
+  auto kern = decode_kernel<D, KV, G, SPARSE, QMIX>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Tl::kSmem);
   if (e != cudaSuccess) return e;
@@ -340,8 +472,11 @@ cudaError_t launch_decode_one(const DecodeLaunch& a, cudaStream_t s) {
 template <typename KV, bool SPARSE>
 cudaError_t launch_decode_dispatch(const DecodeLaunch& a, cudaStream_t s) {
   const int g = a.hq / a.hkv;
-#define DSA_CASE(DD, GG) \
-  if (a.head_dim == DD && g == GG) return launch_decode_one<DD, KV, GG, SPARSE>(a, s);
+  const bool qmix = IsBf16<KV>::value && a.q_bf16 != 0;
+#define DSA_CASE(DD, GG)                                                             \
+  if (a.head_dim == DD && g == GG)                                                   \
+    return qmix ? launch_decode_one<DD, KV, GG, SPARSE, IsBf16<KV>::value>(a, s)     \
+                : launch_decode_one<DD, KV, GG, SPARSE, false>(a, s);
   DSA_CASE(64, 1)
   DSA_CASE(64, 2)
   DSA_CASE(64, 4)
@@ -376,7 +511,8 @@ int decode_ctas_per_sm_t(int head_dim, int group, bool sparse) {
 #define DSA_CASE(DD, GG)                                                                   \
   if (head_dim == DD && group == GG) {                                                     \
     using Tl = DecodeTiling<DD, KV, GG>;                                                   \
-    auto kern = sparse ? decode_kernel<DD, KV, GG, true> : decode_kernel<DD, KV, GG, false>; \
+    auto kern = sparse ? decode_kernel<DD, KV, GG, true, IsBf16<KV>::value>                  \
+                       : decode_kernel<DD, KV, GG, false, IsBf16<KV>::value>;                 \
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,            \
                              Tl::kSmem) != cudaSuccess)                                    \
       return 1;                                                                            \
