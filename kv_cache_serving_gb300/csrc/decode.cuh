@@ -37,7 +37,7 @@ namespace dsa {
 
 // Build-time tuning knobs: stages per warp and warps per CTA.
 #ifndef DSA_DECODE_STAGES
-#define DSA_DECODE_STAGES 3
+#define DSA_DECODE_STAGES 2
 #endif
 #ifndef DSA_DECODE_WARPS
 #define DSA_DECODE_WARPS 4

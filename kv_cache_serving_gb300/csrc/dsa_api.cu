@@ -11,6 +11,17 @@
 #include "dsa.h"
 #include "internal.h"
 
+// Build-time tuning knobs: waves of resident CTAs the chunking aims for.  Kept
+// lists are short and similar in length, so sparse decode wants few, long
+// chunks (little start-up and merge work); dense rows vary with seq_len, so
+// dense decode and attention mass want more, shorter chunks for balance.
+#ifndef DSA_SPARSE_WAVES
+#define DSA_SPARSE_WAVES 2
+#endif
+#ifndef DSA_DENSE_WAVES
+#define DSA_DENSE_WAVES 8
+#endif
+
 namespace dsa {
 namespace {
 
@@ -71,12 +82,12 @@ int sm_count() {
   return n;
 }
 
-// Rows per CTA: enough CTAs for ~8 waves of resident CTAs, at most kMaxChunks
-// chunks per (request, kv head), a multiple of the CTA's rows per pass.
-void choose_chunks(int64_t n_max, int64_t units, int resident, int quantum, int* chunk,
-                   int* num_chunks) {
+// Rows per CTA: enough CTAs for `waves` waves of resident CTAs, at most
+// kMaxChunks chunks per (request, kv head), a multiple of the CTA's rows per pass.
+void choose_chunks(int64_t n_max, int64_t units, int resident, int quantum, int waves,
+                   int* chunk, int* num_chunks) {
   if (quantum < kChunkQuantum) quantum = kChunkQuantum;
-  const int64_t target = 8LL * resident;
+  const int64_t target = static_cast<int64_t>(waves) * resident;
   int64_t c = ceil_div(n_max * units, target > 0 ? target : 1);
   const int64_t lo = ceil_div(n_max, kMaxChunks);
   if (c < lo) c = lo;
@@ -114,7 +125,7 @@ Plan decode_plan(const dsa_dims* d, bool sparse) {
   p.per_sm = kv_bf16 ? decode_ctas_per_sm_bf16(d->head_dim, g, sparse)
                      : decode_ctas_per_sm_f32(d->head_dim, g, sparse);
   choose_chunks(n_max, static_cast<int64_t>(d->batch) * d->hkv, sm_count() * p.per_sm, p.quantum,
-                &p.chunk, &p.num_chunks);
+                sparse ? DSA_SPARSE_WAVES : DSA_DENSE_WAVES, &p.chunk, &p.num_chunks);
   return p;
 }
 
@@ -268,7 +279,7 @@ dsa_status dsa_attention_mass(const dsa_dims* dims, const void* q, const void* k
   a.r_local = r_local;
   a.r_diag = r_diag;
   choose_chunks(n_max, static_cast<int64_t>(dims->batch) * dims->hkv, sm_count() * 2,
-                kChunkQuantum, &a.chunk, &a.num_chunks);
+                kChunkQuantum, DSA_DENSE_WAVES, &a.chunk, &a.num_chunks);
   a.scale_log2 = scale * kLog2e;
   a.mass = mass;
   a.offset_mass = offset_mass;
