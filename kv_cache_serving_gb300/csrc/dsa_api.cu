@@ -12,14 +12,17 @@
 #include "internal.h"
 
 // Build-time tuning knobs: waves of resident CTAs the chunking aims for.  Kept
-// lists are short and similar in length, so sparse decode wants few, long
-// chunks (little start-up and merge work); dense rows vary with seq_len, so
-// dense decode and attention mass want more, shorter chunks for balance.
+// lists are short, so sparse decode wants one chunk per (request, kv head)
+// where possible (no merge launch); dense rows vary with seq_len, so dense
+// decode and attention mass want more, shorter chunks for balance.
 #ifndef DSA_SPARSE_WAVES
-#define DSA_SPARSE_WAVES 2
+#define DSA_SPARSE_WAVES 1
 #endif
 #ifndef DSA_DENSE_WAVES
 #define DSA_DENSE_WAVES 8
+#endif
+#ifndef DSA_MASS_WAVES
+#define DSA_MASS_WAVES 16
 #endif
 
 namespace dsa {
@@ -279,7 +282,7 @@ dsa_status dsa_attention_mass(const dsa_dims* dims, const void* q, const void* k
   a.r_local = r_local;
   a.r_diag = r_diag;
   choose_chunks(n_max, static_cast<int64_t>(dims->batch) * dims->hkv, sm_count() * 2,
-                kChunkQuantum, DSA_DENSE_WAVES, &a.chunk, &a.num_chunks);
+                kChunkQuantum, DSA_MASS_WAVES, &a.chunk, &a.num_chunks);
   a.scale_log2 = scale * kLog2e;
   a.mass = mass;
   a.offset_mass = offset_mass;
