@@ -43,7 +43,7 @@ namespace dsa {
 #define DSA_DECODE_WARPS 4
 #endif
 
-template <int D, typename KV, int G>
+template <int D, typename KV, int G, bool MMA = false>
 struct DecodeTiling {
   static constexpr int kElt = static_cast<int>(sizeof(KV));
   static constexpr int kRowBytes = D * kElt;
@@ -55,11 +55,17 @@ struct DecodeTiling {
   static constexpr int kEPL = D / 8;           // elements of a row per lane
   static constexpr int kNV = kEPL / kVE;       // 16-byte vectors of a row per lane
   static constexpr int kRPL = T / 4;           // rows of a tile per lane
-  static constexpr int kStageBytes = 2 * T * kRowBytes;
+  // With tensor cores, shared-memory rows are padded by 16 bytes so that
+  // ldmatrix (8 rows at one column) is free of bank conflicts; the CUDA-core
+  // loads (8 lanes over 128 contiguous bytes) need no padding.
+  static constexpr int kRowStride = kRowBytes + (MMA ? 16 : 0);
+  static constexpr int kStageBytes = 2 * T * kRowStride;
   static constexpr int kWarpBytes = S * kStageBytes;
   static constexpr int kBarOff = NW * kWarpBytes;
-  static constexpr int kMOff = kBarOff + NW * S * 8;
-  static constexpr int kSmem = kMOff + NW * G * (D + 2) * 4;
+  static constexpr int kPsOff = kBarOff + NW * S * 8;  // [NW][hi, lo][8 heads][T] bf16
+  static constexpr int kSmem = kPsOff + (MMA ? NW * 2 * 8 * T * 2 : 0);
+  // a warp's end-of-CTA state [G][D+2] floats reuses the start of its own ring
+  static_assert(G * (D + 2) * 4 <= kWarpBytes, "merge slot fits the ring");
   static_assert(kStageBytes % 128 == 0, "stage alignment");
   static_assert(kEPL % kVE == 0 && kRowBytes % 128 == 0, "row vector layout");
   // Element of a row held in slot w of vector u by lane j of a row group.
@@ -103,6 +109,34 @@ __device__ __forceinline__ void vec_to_f32<float>(const uint4& v, float* o) {
   o[3] = __uint_as_float(v.w);
 }
 
+// ---- tensor-core helpers (mma.sync m16n8k16, bf16 inputs, fp32 accumulate) ----
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_addr(p))
+               : "memory");
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_addr(p))
+               : "memory");
+}
+// d (16x8, fp32) += a (16x16, bf16, row) * b (16x8, bf16, col)
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint16_t f32_to_bf16_rn(float x) {
+  uint16_t h;
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(h) : "f"(x));
+  return h;
+}
+
 // Rows of the work list of (b, hk), or a negative device error code.  Shared
 // by the decode and merge kernels so that both take the same decision.
 template <bool SPARSE>
@@ -116,9 +150,9 @@ __device__ __forceinline__ int request_rows(const DecodeLaunch& a, int b, int hk
 
 // QMIX: q and K are bf16 and the dot products use the mixed-precision FMA.
 template <int D, typename KV, int G, bool SPARSE, bool QMIX>
-__global__ void __launch_bounds__(DecodeTiling<D, KV, G>::NW * 32)
+__global__ void __launch_bounds__(DecodeTiling<D, KV, G, QMIX && G >= 2>::NW * 32)
     decode_kernel(const DecodeLaunch a) {
-  using Tl = DecodeTiling<D, KV, G>;
+  using Tl = DecodeTiling<D, KV, G, QMIX && G >= 2>;
   constexpr int T = Tl::T, S = Tl::S, NW = Tl::NW;
   constexpr int EPL = Tl::kEPL, NV = Tl::kNV, VE = Tl::kVE, RPL = Tl::kRPL;
   constexpr int kRowBytes = Tl::kRowBytes;
@@ -145,10 +179,15 @@ __global__ void __launch_bounds__(DecodeTiling<D, KV, G>::NW * 32)
   const int nchunks = (n + a.chunk - 1) / a.chunk;
   const int ntiles = (row1 - row0 + T - 1) / T;
 
-  KV* kst = reinterpret_cast<KV*>(smem + warp * Tl::kWarpBytes);  // [S][T][D]
-  KV* vst = kst + S * T * D;                                      // [S][T][D]
+  constexpr int kRowStride = Tl::kRowStride;
+  // grouped-query attention with bf16 operands runs QK^T and PV on tensor cores
+  constexpr bool kMMA = QMIX && G >= 2;
+  unsigned char* kst = smem + warp * Tl::kWarpBytes;  // [S][T] K rows, kRowStride apart
+  unsigned char* vst = kst + S * T * kRowStride;      // [S][T] V rows
+  uint16_t* ps = reinterpret_cast<uint16_t*>(smem + Tl::kPsOff) + warp * 2 * 8 * T;  // [2][8][T]
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Tl::kBarOff) + warp * S;
-  float* mbuf = reinterpret_cast<float*>(smem + Tl::kMOff);  // [NW][G][D+2]
+  // end-of-CTA state of warp w: [G][D+2] floats at the start of w's ring
+  auto mslot = [&](int w) { return reinterpret_cast<float*>(smem + w * Tl::kWarpBytes); };
   const int grp = lane >> 3, jl = lane & 7;                  // row group, lane in group
 
   if (lane == 0) {
@@ -198,48 +237,75 @@ __global__ void __launch_bounds__(DecodeTiling<D, KV, G>::NW * 32)
         pg = 0;
       }
       const size_t off = ((static_cast<size_t>(pg) * kPage + (j & (kPage - 1))) * a.hkv + hk) * D;
-      const size_t dst = (static_cast<size_t>(stage) * T + my_r) * D;
+      const size_t dst = (static_cast<size_t>(stage) * T + my_r) * kRowStride;
       if (T == 32 || lane < T) bulk_copy_g2s(kst + dst, kg + off, kRowBytes, &bars[stage]);
       if (T == 32 || lane >= T) bulk_copy_g2s(vst + dst, vg + off, kRowBytes, &bars[stage]);
     }
   };
 
-  // this lane's elements of the G query vectors: packed bf16 pairs (QMIX) or fp32
+  // CUDA-core path: this lane's elements of the G query vectors (packed bf16
+  // pairs with QMIX, else fp32) and per-head state over the lane's rows.
+  // Tensor-core path: q as mma B fragments (thread t holds head t/4, dims
+  // 16k + 2(t%4) + {0,1,8,9}) and the state of heads 2(t%4), 2(t%4)+1.
   constexpr int kQW = QMIX ? EPL / 2 : EPL;
-  uint32_t qv[G][kQW];
+  constexpr int GC = kMMA ? 1 : G;
+  constexpr int NK = D / 16;
+  uint32_t qv[GC][kMMA ? 1 : kQW];
+  uint32_t qf[kMMA ? NK : 1][2];
+  float m_run[GC], l_run[GC], acc[GC][kMMA ? 1 : EPL];
+  float m2[2], l2[2], oacc[kMMA ? NK : 1][4];
+  const int g4 = lane >> 2, tig = lane & 3;  // mma fragment row group / column pair
+  if constexpr (kMMA) {
+    const uint32_t* q32 = reinterpret_cast<const uint32_t*>(a.q) +
+                          (static_cast<size_t>(b) * a.hq + hk * G + (g4 < G ? g4 : 0)) * (D / 2);
 #pragma unroll
-  for (int h = 0; h < G; ++h) {
-    const size_t qrow = (static_cast<size_t>(b) * a.hq + hk * G + h) * D;
-    if (QMIX) {
-      const uint4* q4 = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.q) + qrow);
-#pragma unroll
-      for (int u = 0; u < NV; ++u) {
-        const uint4 v = __ldg(q4 + u * 8 + jl);
-        qv[h][4 * u] = v.x;
-        qv[h][4 * u + 1] = v.y;
-        qv[h][4 * u + 2] = v.z;
-        qv[h][4 * u + 3] = v.w;
-      }
-    } else {
-#pragma unroll
-      for (int u = 0; u < NV; ++u)
-#pragma unroll
-        for (int w = 0; w < VE; ++w) {
-          const size_t e = qrow + Tl::elem(u, jl, w);
-          const float x = a.q_bf16 ? bf16_lo(reinterpret_cast<const uint16_t*>(a.q)[e])
-                                   : reinterpret_cast<const float*>(a.q)[e];
-          qv[h][u * VE + w] = __float_as_uint(x);
-        }
+    for (int kk = 0; kk < NK; ++kk) {
+      qf[kk][0] = g4 < G ? __ldg(q32 + kk * 8 + tig) : 0u;
+      qf[kk][1] = g4 < G ? __ldg(q32 + kk * 8 + 4 + tig) : 0u;
     }
-  }
-
-  float m_run[G], l_run[G], acc[G][EPL];
 #pragma unroll
-  for (int h = 0; h < G; ++h) {
-    m_run[h] = -INFINITY;
-    l_run[h] = 0.f;
+    for (int j = 0; j < 2; ++j) {
+      m2[j] = -INFINITY;
+      l2[j] = 0.f;
+    }
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) acc[h][e] = 0.f;
+    for (int mt = 0; mt < NK; ++mt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) oacc[mt][e] = 0.f;
+  } else {
+#pragma unroll
+    for (int h = 0; h < GC; ++h) {
+      const size_t qrow = (static_cast<size_t>(b) * a.hq + hk * G + h) * D;
+      if (QMIX) {
+        const uint4* q4 =
+            reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.q) + qrow);
+#pragma unroll
+        for (int u = 0; u < NV; ++u) {
+          const uint4 v = __ldg(q4 + u * 8 + jl);
+          qv[h][4 * u] = v.x;
+          qv[h][4 * u + 1] = v.y;
+          qv[h][4 * u + 2] = v.z;
+          qv[h][4 * u + 3] = v.w;
+        }
+      } else {
+#pragma unroll
+        for (int u = 0; u < NV; ++u)
+#pragma unroll
+          for (int w = 0; w < VE; ++w) {
+            const size_t e = qrow + Tl::elem(u, jl, w);
+            const float x = a.q_bf16 ? bf16_lo(reinterpret_cast<const uint16_t*>(a.q)[e])
+                                     : reinterpret_cast<const float*>(a.q)[e];
+            qv[h][u * VE + w] = __float_as_uint(x);
+          }
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < GC; ++h) {
+      m_run[h] = -INFINITY;
+      l_run[h] = 0.f;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) acc[h][e] = 0.f;
+    }
   }
 
   // prologue: kept indices of tiles 0..S+1, page ids of tiles 0..S, copies of
@@ -262,9 +328,96 @@ __global__ void __launch_bounds__(DecodeTiling<D, KV, G>::NW * 32)
       break;
     }
     const int nrows = min(T, row1 - (row0 + (warp + t * NW) * T));
-    const unsigned char* kt = reinterpret_cast<const unsigned char*>(kst + static_cast<size_t>(stage) * T * D);
-    const unsigned char* vt = reinterpret_cast<const unsigned char*>(vst + static_cast<size_t>(stage) * T * D);
+    const unsigned char* kt = kst + static_cast<size_t>(stage) * T * kRowStride;
+    unsigned char* vt = vst + static_cast<size_t>(stage) * T * kRowStride;
 
+    if constexpr (kMMA) {
+      // ---- tensor cores: S = K q^T per 16-row block, then O^T += V^T P ----
+      constexpr int RB = T / 16;
+      float sm[RB][4];
+#pragma unroll
+      for (int rb = 0; rb < RB; ++rb) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sm[rb][e] = 0.f;
+        const unsigned char* arow =
+            kt + (rb * 16 + (lane & 7) + 8 * ((lane >> 3) & 1)) * kRowStride + 16 * (lane >> 4);
+#pragma unroll
+        for (int kk = 0; kk < NK; ++kk) {
+          uint32_t af[4];
+          ldsm_x4(af, arow + 32 * kk);
+          mma_bf16(sm[rb], af, qf[kk][0], qf[kk][1]);
+        }
+      }
+      // scale, mask rows past nrows (stale data), online softmax for the
+      // thread's two heads (rows spread over the 8 lanes of a column pair)
+      float alpha[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        float tmax = -INFINITY;
+#pragma unroll
+        for (int rb = 0; rb < RB; ++rb)
+#pragma unroll
+          for (int hi = 0; hi < 2; ++hi) {
+            const int r = rb * 16 + g4 + 8 * hi;
+            float& x = sm[rb][2 * hi + j];
+            x = (r < nrows) ? x * a.scale_log2 : -INFINITY;
+            tmax = fmaxf(tmax, x);
+          }
+        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 4));
+        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 8));
+        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
+        const float mnew = fmaxf(m2[j], tmax);
+        alpha[j] = exp2f(m2[j] - mnew);
+        m2[j] = mnew;
+        float psum = 0.f;
+#pragma unroll
+        for (int rb = 0; rb < RB; ++rb)
+#pragma unroll
+          for (int hi = 0; hi < 2; ++hi) {
+            float& x = sm[rb][2 * hi + j];
+            x = exp2f(x - mnew);
+            psum += x;
+          }
+        l2[j] = l2[j] * alpha[j] + psum;
+      }
+#pragma unroll
+      for (int mt = 0; mt < NK; ++mt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) oacc[mt][e] *= alpha[e & 1];
+      // P as bf16 hi + lo into the warp's [head][row] buffers (mma B operand)
+#pragma unroll
+      for (int rb = 0; rb < RB; ++rb)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int h = 2 * tig + (e & 1), r = rb * 16 + g4 + 8 * (e >> 1);
+          const float x = sm[rb][e];
+          const uint16_t xh = f32_to_bf16_rn(x);
+          ps[h * T + r] = xh;
+          ps[8 * T + h * T + r] = f32_to_bf16_rn(x - bf16_lo(xh));
+        }
+      // rows past nrows may hold stale shared memory: zero them so 0 * V stays 0
+      if (nrows < T) {
+        for (int r = nrows; r < T; ++r)
+          for (int x = lane * 16; x < kRowBytes; x += 32 * 16)
+            *reinterpret_cast<uint4*>(vt + r * kRowStride + x) = make_uint4(0u, 0u, 0u, 0u);
+      }
+      __syncwarp();
+#pragma unroll
+      for (int kb = 0; kb < RB; ++kb) {
+        const uint32_t* ph = reinterpret_cast<const uint32_t*>(ps + g4 * T + kb * 16 + 2 * tig);
+        const uint32_t* pl = reinterpret_cast<const uint32_t*>(ps + 8 * T + g4 * T + kb * 16 + 2 * tig);
+        const uint32_t bh0 = ph[0], bh1 = ph[4], bl0 = pl[0], bl1 = pl[4];
+        const unsigned char* vrow =
+            vt + (kb * 16 + (lane & 7) + 8 * (lane >> 4)) * kRowStride + 16 * ((lane >> 3) & 1);
+#pragma unroll
+        for (int mt = 0; mt < NK; ++mt) {
+          uint32_t af[4];
+          ldsm_x4_trans(af, vrow + 32 * mt);
+          mma_bf16(oacc[mt], af, bh0, bh1);
+          mma_bf16(oacc[mt], af, bl0, bl1);
+        }
+      }
+    } else {
     // scores of this lane's rows (rows past nrows hold stale data: masked)
     float sc[G][RPL];
 #pragma unroll
@@ -273,7 +426,7 @@ __global__ void __launch_bounds__(DecodeTiling<D, KV, G>::NW * 32)
       uint4 kv[NV];
 #pragma unroll
       for (int u = 0; u < NV; ++u)
-        kv[u] = *reinterpret_cast<const uint4*>(kt + r * kRowBytes + 128 * u + 16 * jl);
+        kv[u] = *reinterpret_cast<const uint4*>(kt + r * kRowStride + 128 * u + 16 * jl);
 #pragma unroll
       for (int h = 0; h < G; ++h) {
         float d0 = 0.f, d1 = 0.f;
@@ -330,7 +483,7 @@ __global__ void __launch_bounds__(DecodeTiling<D, KV, G>::NW * 32)
       const int r = grp + 4 * i;
 #pragma unroll
       for (int u = 0; u < NV; ++u) {
-        const uint4 vv = *reinterpret_cast<const uint4*>(vt + r * kRowBytes + 128 * u + 16 * jl);
+        const uint4 vv = *reinterpret_cast<const uint4*>(vt + r * kRowStride + 128 * u + 16 * jl);
         float vf[VE];
         vec_to_f32<KV>(vv, vf);
 #pragma unroll
@@ -347,6 +500,7 @@ __global__ void __launch_bounds__(DecodeTiling<D, KV, G>::NW * 32)
       for (int i = 0; i < RPL; ++i)
         if (grp + 4 * i < nrows) pv_row(i);
     }
+    }  // CUDA-core path
     __syncwarp();
     fence_proxy_async_smem();
     if (t + S < my_tiles) issue(t + S, stage, j0, pg0);
@@ -362,10 +516,32 @@ __global__ void __launch_bounds__(DecodeTiling<D, KV, G>::NW * 32)
       mbar_wait(&bars[t % S], static_cast<uint32_t>(t / S) & 1u);
   }
 
-  // sum the 4 row groups of the warp, then merge the warps of this CTA
-  float* mw = mbuf + static_cast<size_t>(warp) * G * (D + 2);
+  // sum the warp's partial states, then merge the warps of this CTA (each
+  // warp's ring is idle now: its copies have all landed)
+  float* mw = mslot(warp);
+  if constexpr (kMMA) {
 #pragma unroll
-  for (int h = 0; h < G; ++h) {
+    for (int j = 0; j < 2; ++j) {
+      float l = l2[j];
+      l += __shfl_xor_sync(0xffffffffu, l, 4);
+      l += __shfl_xor_sync(0xffffffffu, l, 8);
+      l += __shfl_xor_sync(0xffffffffu, l, 16);
+      const int h = 2 * tig + j;
+      if (h < G) {
+#pragma unroll
+        for (int mt = 0; mt < NK; ++mt) {
+          mw[h * (D + 2) + mt * 16 + g4] = oacc[mt][j];
+          mw[h * (D + 2) + mt * 16 + g4 + 8] = oacc[mt][j + 2];
+        }
+        if (g4 == 0) {
+          mw[h * (D + 2) + D] = m2[j];
+          mw[h * (D + 2) + D + 1] = l;
+        }
+      }
+    }
+  } else {
+#pragma unroll
+  for (int h = 0; h < GC; ++h) {
     float l = l_run[h];
     l += __shfl_xor_sync(0xffffffffu, l, 8);
     l += __shfl_xor_sync(0xffffffffu, l, 16);
@@ -385,16 +561,17 @@ __global__ void __launch_bounds__(DecodeTiling<D, KV, G>::NW * 32)
       mw[h * (D + 2) + D + 1] = l;
     }
   }
+  }  // CUDA-core path
   __syncthreads();
   for (int x = threadIdx.x; x < G * D; x += NW * 32) {
     const int h = x / D, d = x % D;
     float mstar = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < NW; ++w) mstar = fmaxf(mstar, mbuf[(w * G + h) * (D + 2) + D]);
+    for (int w = 0; w < NW; ++w) mstar = fmaxf(mstar, mslot(w)[h * (D + 2) + D]);
     float o = 0.f, ls = 0.f;
 #pragma unroll
     for (int w = 0; w < NW; ++w) {
-      const float* src = mbuf + (w * G + h) * (D + 2);
+      const float* src = mslot(w) + h * (D + 2);
       const float sc = src[D] == -INFINITY ? 0.f : exp2f(src[D] - mstar);
       o = fmaf(sc, src[d], o);
       ls = fmaf(sc, src[D + 1], ls);
@@ -459,7 +636,7 @@ struct IsBf16<bf16_t> {
 
 template <int D, typename KV, int G, bool SPARSE, bool QMIX>
 cudaError_t launch_decode_one(const DecodeLaunch& a, cudaStream_t s) {
-  using Tl = DecodeTiling<D, KV, G>;
+  using Tl = DecodeTiling<D, KV, G, QMIX && G >= 2>;
   auto kern = decode_kernel<D, KV, G, SPARSE, QMIX>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Tl::kSmem);
@@ -510,7 +687,7 @@ int decode_ctas_per_sm_t(int head_dim, int group, bool sparse) {
   int n = 0;
 #define DSA_CASE(DD, GG)                                                                   \
   if (head_dim == DD && group == GG) {                                                     \
-    using Tl = DecodeTiling<DD, KV, GG>;                                                   \
+    using Tl = DecodeTiling<DD, KV, GG, IsBf16<KV>::value && (GG >= 2)>;                   \
     auto kern = sparse ? decode_kernel<DD, KV, GG, true, IsBf16<KV>::value>                  \
                        : decode_kernel<DD, KV, GG, false, IsBf16<KV>::value>;                 \
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,            \
