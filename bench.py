@@ -158,11 +158,15 @@ def step_bytes(w, kept_idx, kept_cnt):
     q_b = B * Hq * D * q_elt
     out_b = B * Hq * D * 4 + B * Hq * 4
     sparse_decode = rows * 2 * D * elt + q_b + out_b + 4 * rows + 4 * pages + 4 * B * Hkv
-    index = (B * Hkv * w["mask_words"] * 4 + 3 * 4 * B) + 4 * rows + 4 * B * Hkv
+    mask_in = B * Hkv * w["mask_words"] * 4 + 3 * 4 * B
+    index = mask_in + 4 * rows + 4 * B * Hkv
+    # one call that builds the kept set in the kernel: no kept list in HBM
+    masked = sparse_decode - 4 * rows - 4 * B * Hkv + mask_in
     dense_rows = int(L.sum()) * Hkv
     dense = dense_rows * 2 * D * elt + q_b + out_b + 4 * int(((L + 15) // 16).sum())
     return dict(kv=rows * 2 * D * elt, sparse_decode=sparse_decode, index=index,
-                step=sparse_decode + index, dense=dense, rows=rows, dense_rows=dense_rows)
+                step=sparse_decode + index, masked=masked, dense=dense, rows=rows,
+                dense_rows=dense_rows)
 
 
 # ---------------------------------------------------------------------------
@@ -288,6 +292,15 @@ def run_ours(args):
         dsa.dsa_decode_sparse(d, bt.q, kp, vp, bt.page_table, bt.seq_len, bt.kept_idx,
                               bt.kept_cnt, bt.scale, bt.out, bt.lse, bt.ws, stream)
 
+    out_m = torch.empty_like(bt.out)
+    lse_m = torch.empty_like(bt.lse)
+
+    def masked_step(k):
+        kp, vp = pools[k % R]
+        dsa.dsa_decode_sparse_masked(d, bt.q, kp, vp, bt.page_table, bt.seq_len, bt.prompt_len,
+                                     bt.window, bt.keep_mask, bt.scale, out_m, lse_m, bt.ws,
+                                     stream)
+
     out_dense = torch.empty_like(bt.out)
     lse_dense = torch.empty_like(bt.lse)
 
@@ -299,14 +312,17 @@ def run_ours(args):
     # warm-up: W eager steps of each kind
     for k in range(W):
         sparse_step(k)
+        masked_step(k)
         dense_step(k)
     torch.cuda.synchronize()
     bt.check("warm-up")
+    masked_same = bool(torch.equal(out_m, bt.out) and torch.equal(lse_m, bt.lse))
 
     g_sparse = graph_of(sparse_step, K, stream)
     g_dec = graph_of(decode_only, K, stream)
+    g_masked = graph_of(masked_step, K, stream)
     g_dense = graph_of(dense_step, K, stream)
-    for g in (g_sparse, g_dec, g_dense):
+    for g in (g_sparse, g_dec, g_masked, g_dense):
         g.replay()  # graph upload + one more untimed pass
     torch.cuda.synchronize()
 
@@ -325,14 +341,16 @@ def run_ours(args):
     clocks = sampler.stop()
 
     t_dec = time_graph(g_dec, stream)
+    t_masked = time_graph(g_masked, stream)
     t_dense = time_graph(g_dense, stream)
     torch.cuda.synchronize()
     bt.check("timed region")
 
     if world > 1:
-        t = torch.tensor([t_sparse, t_dec, t_dense], device=device, dtype=torch.float64)
+        t = torch.tensor([t_sparse, t_dec, t_masked, t_dense], device=device,
+                         dtype=torch.float64)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        t_sparse, t_dec, t_dense = t.tolist()
+        t_sparse, t_dec, t_masked, t_dense = t.tolist()
 
     # end-to-end through the API with host buffers: inputs H2D, result D2H, every step
     pin = lambda t: t.cpu().pin_memory()  # noqa: E731
@@ -438,6 +456,14 @@ def run_ours(args):
             "kept_fraction": by["rows"] / by["dense_rows"],
             "dense_bytes": by["dense"],
             "dense_gbs": by["dense"] / (t_dense / K) / 1e9,
+        },
+        "fused_index_decode": {
+            "call": "dsa_decode_sparse_masked (kept set built in the decode kernel)",
+            "ms_per_step": 1e3 * t_masked / K,
+            "tokens_per_s": world * B / (t_masked / K),
+            "bytes": by["masked"],
+            "gbs": by["masked"] / (t_masked / K) / 1e9,
+            "same_bits_as_two_calls": masked_same,
         },
         "attention_mass_ms": mass_ms,
         "e2e": {"value": world * B / (t_e2e / K), "unit": "tokens/s",

@@ -154,6 +154,30 @@ dsa_status dsa_decode_sparse(const dsa_dims* dims, const void* q, const void* k_
                              void* ws, void* stream);
 
 /*
+ * dsa_decode_sparse_masked -- dsa_build_index followed by dsa_decode_sparse in
+ * one call, without the kept lists in device memory: each decode CTA reads
+ * the kept set K(b,hk) of its (request, kv head) straight from prompt_len,
+ * window and keep_mask (the same set, in the same ascending order, that
+ * dsa_build_index writes; same definition as there) and attends over it.  When
+ * dsa_decode_plan gives modes 1 and 2 the same chunk, out and lse equal those
+ * of the two-call path bit for bit.
+ *   q, k_pages, v_pages, page_table, seq_len, scale, out, lse  as in
+ *                     dsa_decode_sparse
+ *   prompt_len, window, keep_mask  as in dsa_build_index
+ * max_window must be <= 1024 (each warp holds the window's mask bits, one
+ * 32-bit word per lane), else DSA_ERR_UNSUPPORTED: use the two calls then.  Invalid per-request data
+ * (the DSA_DEV_BAD_SEQ_LEN / _PROMPT / _WINDOW / _COUNT cases of
+ * dsa_build_index) sets the workspace error word and NaN in that request's out
+ * and lse rows of the affected kv head.  The workspace also holds the kept
+ * count of every (request, kv head) for the LSE merge of split work.
+ */
+dsa_status dsa_decode_sparse_masked(const dsa_dims* dims, const void* q, const void* k_pages,
+                                    const void* v_pages, const int32_t* page_table,
+                                    const int32_t* seq_len, const int32_t* prompt_len,
+                                    const int32_t* window, const uint32_t* keep_mask, float scale,
+                                    float* out, float* lse, void* ws, void* stream);
+
+/*
  * dsa_decode_dense -- the dense causal baseline: the same as dsa_decode_sparse
  * with K(b,hk) = {0 .. L_b - 1} (the T_dense of the summary's speedup
  * T_dense / T_sparse, section 核心公式).  Arguments as above.
@@ -188,12 +212,14 @@ dsa_status dsa_attention_mass(const dsa_dims* dims, const void* q, const void* k
                               void* stream);
 
 /*
- * dsa_decode_plan -- how dsa_decode_sparse (sparse != 0) or dsa_decode_dense
- * (sparse == 0) will split its work on the CURRENT device: rows per CTA
- * (*chunk), CTAs per (request, kv head) at most (*num_chunks), and kernel
- * launches per call (*launches).  Host-only; any output pointer may be NULL.
+ * dsa_decode_plan -- how a decode call will split its work on the CURRENT
+ * device: rows per CTA (*chunk), CTAs per (request, kv head) at most
+ * (*num_chunks), and kernel launches per call (*launches).  mode selects the
+ * call: 0 dsa_decode_dense, 1 dsa_decode_sparse, 2 dsa_decode_sparse_masked
+ * (other values: DSA_ERR_INVALID_ARG).  Host-only; any output pointer may be
+ * NULL.
  */
-dsa_status dsa_decode_plan(const dsa_dims* dims, int32_t sparse, int32_t* chunk,
+dsa_status dsa_decode_plan(const dsa_dims* dims, int32_t mode, int32_t* chunk,
                            int32_t* num_chunks, int32_t* launches);
 
 /*

@@ -8,13 +8,38 @@
 // 具体技术细节示例), read causally, plus the prompt prefix the arXiv abstract
 // reports attention concentrates on.
 //
-// One warp per (b, hk).  Prompt rows are written as a plain range; window rows
-// are scanned 32 at a time in ascending j, kept lanes found with a ballot and
-// placed with a popcount prefix, so the list comes out sorted with no sort.
+// One warp per (b, hk).  Prompt rows are written as a plain range, window rows
+// by window_rows() (ballot + popcount prefix, sorted with no sort).
 #include "common.cuh"
 #include "internal.h"
 
 namespace dsa {
+
+// Window part of the kept set of decode query i (one warp, all lanes): the
+// ascending rows j in max(np, i - W) .. i whose offset o = i - j is 0 or has
+// mask bit o - 1 set, np = min(P, L) being the prompt rows kept before them.
+// Rows are scanned 32 at a time; a ballot finds the kept lanes and a popcount
+// prefix places them, so the list comes out sorted.  Writes the first `cap`
+// rows to out[0..] and returns the full count.
+__device__ __forceinline__ int window_rows(const uint32_t* mask, int i, int np, int W, int lane,
+                                           int32_t* out, int cap) {
+  int n = 0;
+  if (i < np) return 0;
+  const int lo = max(np, i - W);
+  for (int base = lo; base <= i; base += 32) {
+    const int j = base + lane;
+    bool keep = false;
+    if (j <= i) {
+      const int o = i - j;
+      keep = (o == 0) || ((__ldg(mask + ((o - 1) >> 5)) >> ((o - 1) & 31)) & 1u);
+    }
+    const unsigned ballot = __ballot_sync(0xffffffffu, keep);
+    const int pos = n + __popc(ballot & ((1u << lane) - 1u));
+    if (keep && pos < cap) out[pos] = j;
+    n += __popc(ballot);
+  }
+  return n;
+}
 
 __global__ void __launch_bounds__(256) compact_kernel(const CompactLaunch a) {
   const int lane = threadIdx.x & 31;
@@ -40,22 +65,8 @@ __global__ void __launch_bounds__(256) compact_kernel(const CompactLaunch a) {
   const int cap = a.max_kept;
 
   for (int j = lane; j < np && j < cap; j += 32) out[j] = j;
-  int n = np;
-  if (i >= np) {
-    const int lo = max(np, i - W);
-    for (int base = lo; base <= i; base += 32) {
-      const int j = base + lane;
-      bool keep = false;
-      if (j <= i) {
-        const int o = i - j;
-        keep = (o == 0) || ((__ldg(mask + ((o - 1) >> 5)) >> ((o - 1) & 31)) & 1u);
-      }
-      const unsigned ballot = __ballot_sync(0xffffffffu, keep);
-      const int pos = n + __popc(ballot & ((1u << lane) - 1u));
-      if (keep && pos < cap) out[pos] = j;
-      n += __popc(ballot);
-    }
-  }
+  const int n_win = window_rows(mask, i, np, W, lane, out + min(np, cap), max(0, cap - np));
+  int n = np + n_win;
   if (lane == 0) {
     if (n > cap) {
       set_error(a.err, DSA_DEV_BAD_COUNT);

@@ -139,17 +139,40 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rn(float x) {
 
 // Rows of the work list of (b, hk), or a negative device error code.  Shared
 // by the decode and merge kernels so that both take the same decision.
-template <bool SPARSE>
+// Row sources of the decode kernel (the launch modes of internal.h).
+constexpr int kRowsDense = kModeDense;  // rows 0..L-1
+constexpr int kRowsList = kModeList;    // the kept list written by dsa_build_index
+constexpr int kRowsMask = kModeMask;    // the kept set built in the kernel from the mask
+
+// Position (0..31) of the set bit of rank r (0-based, ascending) in w; any
+// value in 0..31 when w has no such bit.
+__device__ __forceinline__ int select_bit(unsigned w, int r) {
+  int pos = 0, c = __popc(w & 0xffffu);
+  if (r >= c) { r -= c; w >>= 16; pos += 16; }
+  c = __popc(w & 0xffu);
+  if (r >= c) { r -= c; w >>= 8; pos += 8; }
+  c = __popc(w & 0xfu);
+  if (r >= c) { r -= c; w >>= 4; pos += 4; }
+  c = __popc(w & 0x3u);
+  if (r >= c) { r -= c; w >>= 2; pos += 2; }
+  if (r >= static_cast<int>(w & 1u)) pos += 1;
+  return pos;
+}
+
+template <int MODE>
 __device__ __forceinline__ int request_rows(const DecodeLaunch& a, int b, int hk, int L) {
   if (L < 1 || L > a.max_pages * kPage) return -DSA_DEV_BAD_SEQ_LEN;
-  if (!SPARSE) return L;
-  const int n = a.kept_cnt[static_cast<size_t>(b) * a.hkv + hk];
+  if (MODE == kRowsDense) return L;
+  // kRowsMask: the count the decode CTAs of this unit recorded in the workspace
+  const int n = MODE == kRowsList ? a.kept_cnt[static_cast<size_t>(b) * a.hkv + hk]
+                                  : a.unit_rows[static_cast<size_t>(b) * a.hkv + hk];
+  if (MODE == kRowsMask && n < 0) return n;
   if (n < 1 || n > a.max_kept || n > L) return -DSA_DEV_BAD_COUNT;
   return n;
 }
 
 // QMIX: q and K are bf16 and the dot products use the mixed-precision FMA.
-template <int D, typename KV, int G, bool SPARSE, bool QMIX>
+template <int D, typename KV, int G, int MODE, bool QMIX>
 __global__ void __launch_bounds__(DecodeTiling<D, KV, G, QMIX && G >= 2>::NW * 32)
     decode_kernel(const DecodeLaunch a) {
   using Tl = DecodeTiling<D, KV, G, QMIX && G >= 2>;
@@ -161,7 +184,43 @@ __global__ void __launch_bounds__(DecodeTiling<D, KV, G, QMIX && G >= 2>::NW * 3
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int c = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
   const int L = a.seq_len[b];
-  const int n = request_rows<SPARSE>(a, b, hk, L);
+  // kRowsMask: the kept set is read straight from the keep mask.  Lane l holds
+  // the bits of window offsets 32l+1 .. 32l+32 that lie in 1..omax (wbits) and
+  // the inclusive prefix count of set bits over lanes 0..l (wincl).
+  int n, np = 0, wq = 0, wcnt = 0;
+  unsigned wbits = 0;
+  int wincl = 0;
+  if constexpr (MODE == kRowsMask) {
+    const uint32_t* mrow = a.keep_mask + (static_cast<size_t>(b) * a.hkv + hk) * a.mask_words;
+    const unsigned raw = lane < a.mask_words ? __ldg(mrow + lane) : 0u;  // issued with the sizes
+    const int P = a.prompt_len[b], W = a.window[b];
+    int code = 0;
+    if (L < 1 || L > a.max_pages * kPage) code = DSA_DEV_BAD_SEQ_LEN;
+    else if (P < 0) code = DSA_DEV_BAD_PROMPT;
+    else if (W < 0 || W > a.max_window) code = DSA_DEV_BAD_WINDOW;
+    if (code == 0) {
+      np = min(P, L);
+      wq = L - 1;
+      // window rows j = i-o, o = omax..0 (ascending j); none when the query is a prompt row
+      const int omax = wq >= np ? min(wq - np, W) : -1;
+      const int vb = min(max(omax - 32 * lane, 0), 32);
+      wbits = vb == 0 ? 0u : raw & (vb == 32 ? 0xffffffffu : (1u << vb) - 1u);
+      wincl = __popc(wbits);
+#pragma unroll
+      for (int s = 1; s < 32; s <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, wincl, s);
+        if (lane >= s) wincl += v;
+      }
+      wcnt = __shfl_sync(0xffffffffu, wincl, 31);
+      n = np + (omax >= 0 ? wcnt + 1 : 0);
+      if (n > a.max_kept) n = -DSA_DEV_BAD_COUNT;
+    } else {
+      n = -code;
+    }
+    if (c == 0 && threadIdx.x == 0) a.unit_rows[static_cast<size_t>(b) * a.hkv + hk] = n;
+  } else {
+    n = request_rows<MODE>(a, b, hk, L);
+  }
   if (n < 0) {
     if (c == 0) {
       if (threadIdx.x == 0) set_error(a.err, -n);
@@ -199,8 +258,9 @@ __global__ void __launch_bounds__(DecodeTiling<D, KV, G, QMIX && G >= 2>::NW * 3
 
   const KV* kg = reinterpret_cast<const KV*>(a.k);
   const KV* vg = reinterpret_cast<const KV*>(a.v);
-  const int32_t* idx = SPARSE ? a.kept_idx + (static_cast<size_t>(b) * a.hkv + hk) * a.max_kept
-                              : nullptr;
+  const int32_t* idx = MODE == kRowsList
+                           ? a.kept_idx + (static_cast<size_t>(b) * a.hkv + hk) * a.max_kept
+                           : nullptr;
   const int32_t* pt = a.page_table + static_cast<size_t>(b) * a.max_pages;
 
   const int my_tiles = warp < ntiles ? (ntiles - warp + NW - 1) / NW : 0;
@@ -213,10 +273,33 @@ __global__ void __launch_bounds__(DecodeTiling<D, KV, G, QMIX && G >= 2>::NW * 3
   const int my_r = lane & (T - 1);
   auto tile_r0 = [&](int t) { return row0 + (warp + t * NW) * T; };
   auto tile_rows = [&](int t) { return min(T, row1 - tile_r0(t)); };
+  // kRowsMask: row at position p of the ascending window rows (all lanes take
+  // part; p outside 0..wcnt gives an unused value).  Position wcnt is the query
+  // row; position p < wcnt is offset rank q = wcnt-1-p in ascending offset
+  // order, found by a binary search over the lanes' prefix counts, then the
+  // rank within that lane's word.
+  auto window_row = [&](int p) -> int {
+    const int q = wcnt - 1 - p;
+    int w = 0;
+#pragma unroll
+    for (int s = 16; s >= 1; s >>= 1)
+      if (__shfl_sync(0xffffffffu, wincl, w + s - 1) <= q) w += s;
+    const unsigned word = __shfl_sync(0xffffffffu, wbits, w);
+    const int below = __shfl_sync(0xffffffffu, wincl, w) - __popc(word);
+    return q < 0 ? wq : wq - (32 * w + select_bit(word, q - below) + 1);
+  };
   auto load_j = [&](int t) -> int {
-    if (t >= my_tiles || my_r >= tile_rows(t)) return 0;
+    if (t >= my_tiles) return 0;
     const int r = tile_r0(t) + my_r;
-    return SPARSE ? __ldg(idx + r) : r;
+    if constexpr (MODE == kRowsMask) {
+      if (tile_r0(t) + tile_rows(t) > np) {  // warp-uniform: the tile reaches window rows
+        const int jw = window_row(r - np);
+        return my_r >= tile_rows(t) ? 0 : (r < np ? r : jw);
+      }
+    }
+    if (my_r >= tile_rows(t)) return 0;
+    if constexpr (MODE == kRowsList) return __ldg(idx + r);
+    return r;
   };
   auto load_pg = [&](int t, int& j) -> int {
     if (t >= my_tiles || my_r >= tile_rows(t)) return 0;
@@ -323,8 +406,8 @@ __global__ void __launch_bounds__(DecodeTiling<D, KV, G, QMIX && G >= 2>::NW * 3
   int failed_at = -1;
   for (int t = 0; t < my_tiles; ++t) {
     const int stage = t % S;
-    if (!mbar_wait(&bars[stage], static_cast<uint32_t>(t / S) & 1u)) {
-      failed_at = t;
+    if (!__all_sync(0xffffffffu, mbar_wait(&bars[stage], static_cast<uint32_t>(t / S) & 1u))) {
+      failed_at = t;  // the whole warp leaves together
       break;
     }
     const int nrows = min(T, row1 - (row0 + (warp + t * NW) * T));
@@ -593,7 +676,7 @@ __global__ void __launch_bounds__(DecodeTiling<D, KV, G, QMIX && G >= 2>::NW * 3
 
 // One warp per (request, query head): combine the chunk partials by
 // log-sum-exp.  Heads whose rows fit one chunk were finished by decode_kernel.
-template <int D, bool SPARSE>
+template <int D, int MODE>
 __global__ void __launch_bounds__(128) merge_kernel(const DecodeLaunch a) {
   constexpr int DPL = D / 32;
   const int lane = threadIdx.x & 31;
@@ -601,7 +684,7 @@ __global__ void __launch_bounds__(128) merge_kernel(const DecodeLaunch a) {
   if (gw >= a.batch * a.hq) return;
   const int b = gw / a.hq, qh = gw % a.hq;
   const int hk = qh / (a.hq / a.hkv);
-  const int n = request_rows<SPARSE>(a, b, hk, a.seq_len[b]);
+  const int n = request_rows<MODE>(a, b, hk, a.seq_len[b]);
   if (n < 0) return;  // decode_kernel wrote NaN and the error code
   const int nch = (n + a.chunk - 1) / a.chunk;
   if (nch <= 1) return;
@@ -634,26 +717,25 @@ struct IsBf16<bf16_t> {
   static constexpr bool value = true;
 };
 
-template <int D, typename KV, int G, bool SPARSE, bool QMIX>
+template <int D, typename KV, int G, int MODE, bool QMIX>
 cudaError_t launch_decode_one(const DecodeLaunch& a, cudaStream_t s) {
-  using Tl = DecodeTiling<D, KV, G, QMIX && G >= 2>;
-  auto kern = decode_kernel<D, KV, G, SPARSE, QMIX>;
-  cudaError_t e =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Tl::kSmem);
+  auto kern = decode_kernel<D, KV, G, MODE, QMIX>;
+  const int smem = DecodeTiling<D, KV, G, QMIX && G >= 2>::kSmem;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const dim3 grid(a.num_chunks, a.hkv, a.batch);
-  kern<<<grid, Tl::NW * 32, Tl::kSmem, s>>>(a);
+  kern<<<grid, DecodeTiling<D, KV, G, QMIX && G >= 2>::NW * 32, smem, s>>>(a);
   return cudaGetLastError();
 }
 
-template <typename KV, bool SPARSE>
+template <typename KV, int MODE>
 cudaError_t launch_decode_dispatch(const DecodeLaunch& a, cudaStream_t s) {
   const int g = a.hq / a.hkv;
   const bool qmix = IsBf16<KV>::value && a.q_bf16 != 0;
-#define DSA_CASE(DD, GG)                                                             \
-  if (a.head_dim == DD && g == GG)                                                   \
-    return qmix ? launch_decode_one<DD, KV, GG, SPARSE, IsBf16<KV>::value>(a, s)     \
-                : launch_decode_one<DD, KV, GG, SPARSE, false>(a, s);
+#define DSA_CASE(DD, GG)                                                           \
+  if (a.head_dim == DD && g == GG)                                                 \
+    return qmix ? launch_decode_one<DD, KV, GG, MODE, IsBf16<KV>::value>(a, s)     \
+                : launch_decode_one<DD, KV, GG, MODE, false>(a, s);
   DSA_CASE(64, 1)
   DSA_CASE(64, 2)
   DSA_CASE(64, 4)
@@ -663,6 +745,16 @@ cudaError_t launch_decode_dispatch(const DecodeLaunch& a, cudaStream_t s) {
   DSA_CASE(128, 4)
   DSA_CASE(128, 8)
 #undef DSA_CASE
+  return cudaErrorInvalidValue;
+}
+
+template <typename KV>
+cudaError_t launch_decode_t(const DecodeLaunch& a, int mode, cudaStream_t s) {
+  switch (mode) {
+    case kRowsDense: return launch_decode_dispatch<KV, kRowsDense>(a, s);
+    case kRowsList: return launch_decode_dispatch<KV, kRowsList>(a, s);
+    case kRowsMask: return launch_decode_dispatch<KV, kRowsMask>(a, s);
+  }
   return cudaErrorInvalidValue;
 }
 
@@ -682,18 +774,19 @@ int decode_rows_per_pass_t(int head_dim, int group) {
   return 0;
 }
 
-template <typename KV>
-int decode_ctas_per_sm_t(int head_dim, int group, bool sparse) {
+// Occupancy of the decode kernel as launched with `mode`.
+template <typename KV, int MODE>
+int decode_ctas_per_sm_m(int head_dim, int group) {
   int n = 0;
 #define DSA_CASE(DD, GG)                                                                   \
   if (head_dim == DD && group == GG) {                                                     \
     using Tl = DecodeTiling<DD, KV, GG, IsBf16<KV>::value && (GG >= 2)>;                   \
-    auto kern = sparse ? decode_kernel<DD, KV, GG, true, IsBf16<KV>::value>                  \
-                       : decode_kernel<DD, KV, GG, false, IsBf16<KV>::value>;                 \
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,            \
-                             Tl::kSmem) != cudaSuccess)                                    \
+    auto kern = decode_kernel<DD, KV, GG, MODE, IsBf16<KV>::value>;                        \
+    const int smem = Tl::kSmem;                                                            \
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=   \
+        cudaSuccess)                                                                       \
       return 1;                                                                            \
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, Tl::NW * 32, Tl::kSmem) != \
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, Tl::NW * 32, smem) !=      \
         cudaSuccess)                                                                       \
       return 1;                                                                            \
     return n < 1 ? 1 : n;                                                                  \
@@ -707,6 +800,16 @@ int decode_ctas_per_sm_t(int head_dim, int group, bool sparse) {
   DSA_CASE(128, 4)
   DSA_CASE(128, 8)
 #undef DSA_CASE
+  return 1;
+}
+
+template <typename KV>
+int decode_ctas_per_sm_t(int head_dim, int group, int mode) {
+  switch (mode) {
+    case kRowsDense: return decode_ctas_per_sm_m<KV, kRowsDense>(head_dim, group);
+    case kRowsList: return decode_ctas_per_sm_m<KV, kRowsList>(head_dim, group);
+    case kRowsMask: return decode_ctas_per_sm_m<KV, kRowsMask>(head_dim, group);
+  }
   return 1;
 }
 

@@ -3,17 +3,16 @@
 
 namespace dsa {
 
-cudaError_t launch_decode_bf16(const DecodeLaunch& a, bool sparse, cudaStream_t s) {
-  return sparse ? launch_decode_dispatch<bf16_t, true>(a, s)
-                : launch_decode_dispatch<bf16_t, false>(a, s);
+cudaError_t launch_decode_bf16(const DecodeLaunch& a, int mode, cudaStream_t s) {
+  return launch_decode_t<bf16_t>(a, mode, s);
 }
 
 int decode_rows_per_pass_bf16(int head_dim, int group) {
   return decode_rows_per_pass_t<bf16_t>(head_dim, group);
 }
 
-int decode_ctas_per_sm_bf16(int head_dim, int group, bool sparse) {
-  return decode_ctas_per_sm_t<bf16_t>(head_dim, group, sparse);
+int decode_ctas_per_sm_bf16(int head_dim, int group, int mode) {
+  return decode_ctas_per_sm_t<bf16_t>(head_dim, group, mode);
 }
 
 }  // namespace dsa

@@ -4,21 +4,23 @@
 
 namespace dsa {
 
-cudaError_t launch_decode_f32(const DecodeLaunch& a, bool sparse, cudaStream_t s) {
-  return sparse ? launch_decode_dispatch<float, true>(a, s)
-                : launch_decode_dispatch<float, false>(a, s);
+cudaError_t launch_decode_f32(const DecodeLaunch& a, int mode, cudaStream_t s) {
+  return launch_decode_t<float>(a, mode, s);
 }
 
-cudaError_t launch_merge(const DecodeLaunch& a, bool sparse, cudaStream_t s) {
+template <int D>
+void launch_merge_d(const DecodeLaunch& a, int mode, int blocks, cudaStream_t s) {
+  if (mode == kRowsDense) merge_kernel<D, kRowsDense><<<blocks, 128, 0, s>>>(a);
+  else if (mode == kRowsList) merge_kernel<D, kRowsList><<<blocks, 128, 0, s>>>(a);
+  else merge_kernel<D, kRowsMask><<<blocks, 128, 0, s>>>(a);
+}
+
+cudaError_t launch_merge(const DecodeLaunch& a, int mode, cudaStream_t s) {
   const int pairs = a.batch * a.hq;
   if (pairs == 0 || a.num_chunks <= 1) return cudaSuccess;
   const int blocks = (pairs + 3) / 4;
-  if (a.head_dim == 64)
-    sparse ? merge_kernel<64, true><<<blocks, 128, 0, s>>>(a)
-           : merge_kernel<64, false><<<blocks, 128, 0, s>>>(a);
-  else
-    sparse ? merge_kernel<128, true><<<blocks, 128, 0, s>>>(a)
-           : merge_kernel<128, false><<<blocks, 128, 0, s>>>(a);
+  if (a.head_dim == 64) launch_merge_d<64>(a, mode, blocks, s);
+  else launch_merge_d<128>(a, mode, blocks, s);
   return cudaGetLastError();
 }
 
@@ -26,8 +28,8 @@ int decode_rows_per_pass_f32(int head_dim, int group) {
   return decode_rows_per_pass_t<float>(head_dim, group);
 }
 
-int decode_ctas_per_sm_f32(int head_dim, int group, bool sparse) {
-  return decode_ctas_per_sm_t<float>(head_dim, group, sparse);
+int decode_ctas_per_sm_f32(int head_dim, int group, int mode) {
+  return decode_ctas_per_sm_t<float>(head_dim, group, mode);
 }
 
 }  // namespace dsa

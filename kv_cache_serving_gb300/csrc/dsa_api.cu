@@ -112,40 +112,69 @@ float* partials(void* ws) {
   return reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(ws) + kWsHeader);
 }
 
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Partials region of the workspace, the same for every entry point.
+size_t partials_region(const dsa_dims* d) {
+  const size_t dec = partial_bytes(d, d->head_dim + 2);
+  const size_t mass = partial_bytes(d, 6);
+  return round_up(dec > mass ? dec : mass, 256);
+}
+
+// [batch][hkv] kept counts of dsa_decode_sparse_masked, after the partials.
+int32_t* unit_rows(const dsa_dims* d, void* ws) {
+  return reinterpret_cast<int32_t*>(reinterpret_cast<unsigned char*>(ws) + kWsHeader +
+                                    partials_region(d));
+}
+
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 struct Plan {
   int chunk, num_chunks, quantum, per_sm;
 };
 
-Plan decode_plan(const dsa_dims* d, bool sparse) {
+Plan decode_plan(const dsa_dims* d, int mode) {
   const bool kv_bf16 = d->kv_dtype == DSA_BF16;
   const int g = d->hq / d->hkv;
-  const int64_t n_max = sparse ? d->max_kept : dense_rows(d);
+  const int64_t n_max = mode == kModeDense ? dense_rows(d) : d->max_kept;
   Plan p{};
   p.quantum = kv_bf16 ? decode_rows_per_pass_bf16(d->head_dim, g)
                       : decode_rows_per_pass_f32(d->head_dim, g);
-  p.per_sm = kv_bf16 ? decode_ctas_per_sm_bf16(d->head_dim, g, sparse)
-                     : decode_ctas_per_sm_f32(d->head_dim, g, sparse);
+  p.per_sm = kv_bf16 ? decode_ctas_per_sm_bf16(d->head_dim, g, mode)
+                     : decode_ctas_per_sm_f32(d->head_dim, g, mode);
   choose_chunks(n_max, static_cast<int64_t>(d->batch) * d->hkv, sm_count() * p.per_sm, p.quantum,
-                sparse ? DSA_SPARSE_WAVES : DSA_DENSE_WAVES, &p.chunk, &p.num_chunks);
+                mode == kModeDense ? DSA_DENSE_WAVES : DSA_SPARSE_WAVES, &p.chunk,
+                &p.num_chunks);
   return p;
 }
 
-dsa_status decode_common(const dsa_dims* d, bool sparse, const void* q, const void* k,
+// Row sources of decode_common: the kept list (kModeList) or the per-request
+// prompt length, window and keep mask (kModeMask).
+struct RowSource {
+  const int32_t* kept_idx = nullptr;
+  const int32_t* kept_cnt = nullptr;
+  const int32_t* prompt_len = nullptr;
+  const int32_t* window = nullptr;
+  const uint32_t* keep_mask = nullptr;
+};
+
+dsa_status decode_common(const dsa_dims* d, int mode, const void* q, const void* k,
                          const void* v, const int32_t* page_table, const int32_t* seq_len,
-                         const int32_t* kept_idx, const int32_t* kept_cnt, float scale,
-                         float* out, float* lse, void* ws, void* stream) {
+                         const RowSource& rs, float scale, float* out, float* lse, void* ws,
+                         void* stream) {
   const dsa_status st = check_dims(d);
   if (st != DSA_OK) return st;
   if (!q || !k || !v || !page_table || !seq_len || !out || !ws) return DSA_ERR_INVALID_ARG;
-  if (sparse && (!kept_idx || !kept_cnt)) return DSA_ERR_INVALID_ARG;
+  if (mode == kModeList && (!rs.kept_idx || !rs.kept_cnt)) return DSA_ERR_INVALID_ARG;
+  if (mode == kModeMask && (!rs.prompt_len || !rs.window || !rs.keep_mask))
+    return DSA_ERR_INVALID_ARG;
+  if (mode == kModeMask && d->max_window > kMaskModeMaxWindow) return DSA_ERR_UNSUPPORTED;
   if (!(scale == scale) || !aligned(ws, 256) || !aligned(k, 16) || !aligned(v, 16) ||
       !aligned(q, 16))
     return DSA_ERR_INVALID_ARG;
   if (d->batch == 0) return DSA_OK;
   const bool kv_bf16 = d->kv_dtype == DSA_BF16;
-  const Plan plan = decode_plan(d, sparse);
+  const Plan plan = decode_plan(d, mode);
   DecodeLaunch a{};
   a.q = q;
   a.q_bf16 = d->q_dtype == DSA_BF16;
@@ -153,8 +182,14 @@ dsa_status decode_common(const dsa_dims* d, bool sparse, const void* q, const vo
   a.v = v;
   a.page_table = page_table;
   a.seq_len = seq_len;
-  a.kept_idx = kept_idx;
-  a.kept_cnt = kept_cnt;
+  a.kept_idx = rs.kept_idx;
+  a.kept_cnt = rs.kept_cnt;
+  a.prompt_len = rs.prompt_len;
+  a.window = rs.window;
+  a.keep_mask = rs.keep_mask;
+  a.unit_rows = mode == kModeMask ? unit_rows(d, ws) : nullptr;
+  a.max_window = d->max_window;
+  a.mask_words = d->mask_words;
   a.batch = d->batch;
   a.hq = d->hq;
   a.hkv = d->hkv;
@@ -170,9 +205,9 @@ dsa_status decode_common(const dsa_dims* d, bool sparse, const void* q, const vo
   a.part = partials(ws);
   a.err = err_word(ws);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = kv_bf16 ? launch_decode_bf16(a, sparse, s) : launch_decode_f32(a, sparse, s);
+  cudaError_t e = kv_bf16 ? launch_decode_bf16(a, mode, s) : launch_decode_f32(a, mode, s);
   if (e != cudaSuccess) return DSA_ERR_CUDA;
-  return from_cuda(launch_merge(a, sparse, s));
+  return from_cuda(launch_merge(a, mode, s));
 }
 
 }  // namespace
@@ -199,9 +234,8 @@ const char* dsa_status_string(dsa_status status) {
 
 size_t dsa_workspace_size(const dsa_dims* dims) {
   if (check_dims(dims) != DSA_OK) return 0;
-  const size_t dec = partial_bytes(dims, dims->head_dim + 2);
-  const size_t mass = partial_bytes(dims, 6);
-  return kWsHeader + (dec > mass ? dec : mass);
+  const size_t counts = static_cast<size_t>(dims->batch) * dims->hkv * sizeof(int32_t);
+  return kWsHeader + partials_region(dims) + round_up(counts, 256);
 }
 
 dsa_status dsa_build_index(const dsa_dims* dims, const int32_t* seq_len,
@@ -235,15 +269,31 @@ dsa_status dsa_decode_sparse(const dsa_dims* dims, const void* q, const void* k_
                              const int32_t* seq_len, const int32_t* kept_idx,
                              const int32_t* kept_cnt, float scale, float* out, float* lse,
                              void* ws, void* stream) {
-  return decode_common(dims, true, q, k_pages, v_pages, page_table, seq_len, kept_idx, kept_cnt,
-                       scale, out, lse, ws, stream);
+  RowSource rs;
+  rs.kept_idx = kept_idx;
+  rs.kept_cnt = kept_cnt;
+  return decode_common(dims, kModeList, q, k_pages, v_pages, page_table, seq_len, rs, scale, out,
+                       lse, ws, stream);
+}
+
+dsa_status dsa_decode_sparse_masked(const dsa_dims* dims, const void* q, const void* k_pages,
+                                    const void* v_pages, const int32_t* page_table,
+                                    const int32_t* seq_len, const int32_t* prompt_len,
+                                    const int32_t* window, const uint32_t* keep_mask, float scale,
+                                    float* out, float* lse, void* ws, void* stream) {
+  RowSource rs;
+  rs.prompt_len = prompt_len;
+  rs.window = window;
+  rs.keep_mask = keep_mask;
+  return decode_common(dims, kModeMask, q, k_pages, v_pages, page_table, seq_len, rs, scale, out,
+                       lse, ws, stream);
 }
 
 dsa_status dsa_decode_dense(const dsa_dims* dims, const void* q, const void* k_pages,
                             const void* v_pages, const int32_t* page_table,
                             const int32_t* seq_len, float scale, float* out, float* lse,
                             void* ws, void* stream) {
-  return decode_common(dims, false, q, k_pages, v_pages, page_table, seq_len, nullptr, nullptr,
+  return decode_common(dims, kModeDense, q, k_pages, v_pages, page_table, seq_len, RowSource{},
                        scale, out, lse, ws, stream);
 }
 
@@ -291,11 +341,13 @@ dsa_status dsa_attention_mass(const dsa_dims* dims, const void* q, const void* k
   return from_cuda(launch_mass(a, dims->kv_dtype == DSA_BF16, static_cast<cudaStream_t>(stream)));
 }
 
-dsa_status dsa_decode_plan(const dsa_dims* dims, int32_t sparse, int32_t* chunk,
+dsa_status dsa_decode_plan(const dsa_dims* dims, int32_t mode, int32_t* chunk,
                            int32_t* num_chunks, int32_t* launches) {
   const dsa_status st = check_dims(dims);
   if (st != DSA_OK) return st;
-  const Plan p = decode_plan(dims, sparse != 0);
+  if (mode < kModeDense || mode > kModeMask) return DSA_ERR_INVALID_ARG;
+  if (mode == kModeMask && dims->max_window > kMaskModeMaxWindow) return DSA_ERR_UNSUPPORTED;
+  const Plan p = decode_plan(dims, mode);
   if (chunk) *chunk = p.chunk;
   if (num_chunks) *num_chunks = p.num_chunks;
   if (launches) *launches = dims->batch == 0 ? 0 : (p.num_chunks > 1 ? 2 : 1);
@@ -366,7 +418,7 @@ extern "C" dsa_status dsa_decode_sparse_noalloc(const dsa_dims* dims, const void
     return DSA_ERR_INVALID_ARG;
   // Scratch this call needs: the header plus one partial per (request, query
   // head, chunk), counted even when a single chunk leaves it unused.
-  const Plan plan = decode_plan(dims, true);
+  const Plan plan = decode_plan(dims, kModeList);
   const size_t need = kWsHeader + static_cast<size_t>(dims->batch) * dims->hq *
                                       static_cast<size_t>(plan.num_chunks > 0 ? plan.num_chunks
                                                                               : 1) *
@@ -378,8 +430,11 @@ extern "C" dsa_status dsa_decode_sparse_noalloc(const dsa_dims* dims, const void
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // the error word (and the rest of the header) must start at zero
   if (cudaMemsetAsync(ws, 0, kWsHeader, s) != cudaSuccess) return DSA_ERR_CUDA;
-  const dsa_status rc = decode_common(dims, true, q, k_pages, v_pages, page_table, seq_len,
-                                      kept_idx, kept_cnt, scale, out, lse, ws, stream);
+  RowSource rs;
+  rs.kept_idx = kept_idx;
+  rs.kept_cnt = kept_cnt;
+  const dsa_status rc = decode_common(dims, kModeList, q, k_pages, v_pages, page_table, seq_len,
+                                      rs, scale, out, lse, ws, stream);
   if (rc != DSA_OK) return rc;
   if (dev_error != nullptr &&
       cudaMemcpyAsync(dev_error, ws, sizeof(int32_t), cudaMemcpyDeviceToDevice, s) != cudaSuccess)

@@ -20,9 +20,14 @@ struct DecodeLaunch {
   const void* v;
   const int32_t* page_table;
   const int32_t* seq_len;
-  const int32_t* kept_idx;  // sparse only
-  const int32_t* kept_cnt;  // sparse only
+  const int32_t* kept_idx;  // kRowsList only
+  const int32_t* kept_cnt;  // kRowsList only
+  const int32_t* prompt_len;  // kRowsMask only
+  const int32_t* window;      // kRowsMask only
+  const uint32_t* keep_mask;  // kRowsMask only: [batch][hkv][mask_words]
+  int32_t* unit_rows;         // kRowsMask only: [batch][hkv] kept count or -error
   int32_t batch, hq, hkv, head_dim, max_pages, num_pages, max_kept;
+  int32_t max_window, mask_words;  // kRowsMask only
   int32_t chunk, num_chunks;
   float scale_log2;  // softmax scale * log2(e)
   float* out;
@@ -61,11 +66,19 @@ struct CompactLaunch {
   int32_t* err;
 };
 
-// Each returns cudaSuccess or the launch error.  `sparse` selects the kept
-// list (true) or the dense range 0..L-1 (false).
-cudaError_t launch_decode_bf16(const DecodeLaunch& a, bool sparse, cudaStream_t s);
-cudaError_t launch_decode_f32(const DecodeLaunch& a, bool sparse, cudaStream_t s);
-cudaError_t launch_merge(const DecodeLaunch& a, bool sparse, cudaStream_t s);
+// Row sources of a decode launch (`mode` below).
+constexpr int kModeDense = 0;  // rows 0..L-1
+constexpr int kModeList = 1;   // kept_idx / kept_cnt from dsa_build_index
+constexpr int kModeMask = 2;   // kept set built in the kernel from keep_mask
+
+// Largest max_window of kModeMask: the kernel holds the window's mask bits one
+// 32-bit word per lane of a warp.
+constexpr int kMaskModeMaxWindow = 1024;
+
+// Each returns cudaSuccess or the launch error.
+cudaError_t launch_decode_bf16(const DecodeLaunch& a, int mode, cudaStream_t s);
+cudaError_t launch_decode_f32(const DecodeLaunch& a, int mode, cudaStream_t s);
+cudaError_t launch_merge(const DecodeLaunch& a, int mode, cudaStream_t s);
 cudaError_t launch_mass(const MassLaunch& a, bool kv_bf16, cudaStream_t s);
 cudaError_t launch_compact(const CompactLaunch& a, cudaStream_t s);
 
@@ -74,7 +87,7 @@ cudaError_t launch_compact(const CompactLaunch& a, cudaStream_t s);
 int decode_rows_per_pass_bf16(int head_dim, int group);
 int decode_rows_per_pass_f32(int head_dim, int group);
 // Resident CTAs per SM of the decode kernel for this instantiation (>= 1).
-int decode_ctas_per_sm_bf16(int head_dim, int group, bool sparse);
-int decode_ctas_per_sm_f32(int head_dim, int group, bool sparse);
+int decode_ctas_per_sm_bf16(int head_dim, int group, int mode);
+int decode_ctas_per_sm_f32(int head_dim, int group, int mode);
 
 }  // namespace dsa

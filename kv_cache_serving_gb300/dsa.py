@@ -65,6 +65,7 @@ def _load():
         "dsa_workspace_size": ([D], SZ),
         "dsa_build_index": ([D, P, P, P, P, P, P, P, P], I32),
         "dsa_decode_sparse": ([D, P, P, P, P, P, P, P, F32, P, P, P, P], I32),
+        "dsa_decode_sparse_masked": ([D, P, P, P, P, P, P, P, P, F32, P, P, P, P], I32),
         "dsa_decode_dense": ([D, P, P, P, P, P, F32, P, P, P, P], I32),
         "dsa_attention_mass": ([D, P, P, P, P, P, P, P, I32, I32, F32, P, P, P, P], I32),
         "dsa_decode_plan": ([D, I32, ctypes.POINTER(I32), ctypes.POINTER(I32),
@@ -166,6 +167,19 @@ def dsa_decode_sparse(dims, q, k_pages, v_pages, page_table, seq_len, kept_idx, 
         _ptr(lse, torch.float32, "lse"), _ptr(ws), _stream(stream)), "dsa_decode_sparse")
 
 
+def dsa_decode_sparse_masked(dims, q, k_pages, v_pages, page_table, seq_len, prompt_len, window,
+                             keep_mask, scale, out, lse, ws, stream=None):
+    """dsa_build_index + dsa_decode_sparse in one call: the kernels build each
+    (request, kv head)'s kept set from the mask themselves."""
+    _check(_load().dsa_decode_sparse_masked(
+        ctypes.byref(dims), _ptr(q, _QKV, "q"), _ptr(k_pages, _QKV, "k_pages"),
+        _ptr(v_pages, _QKV, "v_pages"), _ptr(page_table, _I32, "page_table"),
+        _ptr(seq_len, _I32, "seq_len"), _ptr(prompt_len, _I32, "prompt_len"),
+        _ptr(window, _I32, "window"), _ptr(keep_mask, _MASK, "keep_mask"), float(scale),
+        _ptr(out, torch.float32, "out"), _ptr(lse, torch.float32, "lse"), _ptr(ws),
+        _stream(stream)), "dsa_decode_sparse_masked")
+
+
 def dsa_decode_sparse_noalloc(dims, q, k_pages, v_pages, page_table, seq_len, kept_idx,
                               kept_cnt, scale, out, lse, dev_error=None, stream=None):
     """dsa_decode_sparse with the library's own fixed scratch instead of a caller
@@ -200,11 +214,15 @@ def dsa_attention_mass(dims, q, k_pages, page_table, seq_len, prompt_len, window
         _ptr(ws), _stream(stream)), "dsa_attention_mass")
 
 
-def dsa_decode_plan(dims, sparse: bool):
+PLAN_DENSE, PLAN_SPARSE, PLAN_MASKED = 0, 1, 2
+
+
+def dsa_decode_plan(dims, mode: int):
     """(rows per CTA, max CTAs per (request, kv head), kernel launches per call)
-    on the current device."""
+    on the current device for dsa_decode_dense (mode 0), dsa_decode_sparse (1)
+    or dsa_decode_sparse_masked (2)."""
     c, n, l = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
-    _check(_load().dsa_decode_plan(ctypes.byref(dims), int(sparse), ctypes.byref(c),
+    _check(_load().dsa_decode_plan(ctypes.byref(dims), int(mode), ctypes.byref(c),
                                    ctypes.byref(n), ctypes.byref(l)), "dsa_decode_plan")
     return c.value, n.value, l.value
 

@@ -72,6 +72,14 @@ class DecodeBatch:
                               self.ws, stream)
         return out, lse
 
+    def decode_sparse_masked(self, out=None, lse=None, stream=None):
+        out = self.out if out is None else out
+        lse = self.lse if lse is None else lse
+        dsa.dsa_decode_sparse_masked(self.dims, self.q, self.k_pages, self.v_pages,
+                                     self.page_table, self.seq_len, self.prompt_len, self.window,
+                                     self.keep_mask, self.scale, out, lse, self.ws, stream)
+        return out, lse
+
     def decode_dense(self, out=None, lse=None, stream=None):
         out = self.out if out is None else out
         lse = self.lse if lse is None else lse

@@ -15,6 +15,7 @@ import pytest
 import torch
 
 import oracle
+from kv_cache_serving_gb300 import dsa
 from kv_cache_serving_gb300 import workloads as wl
 from kv_cache_serving_gb300.session import DecodeBatch
 
@@ -71,19 +72,34 @@ def oracle_inputs(w, mask=None):
     return d
 
 
+def same_plan(bt):
+    """True when the two sparse calls split rows into the same chunks, so that
+    they sum in the same order."""
+    return (dsa.dsa_decode_plan(bt.dims, dsa.PLAN_SPARSE)[:2] ==
+            dsa.dsa_decode_plan(bt.dims, dsa.PLAN_MASKED)[:2])
+
+
 def run_both(w, mask=None, bh=None):
-    """GPU sparse + dense vs oracle on all (or the listed) (b, h) pairs."""
+    """GPU sparse (kept lists, and in-kernel from the mask) + dense vs oracle on
+    all (or the listed) (b, h) pairs."""
     bt = DecodeBatch.from_workload(w, keep_mask=mask)
     check_index(bt, w, mask)
     fp32 = w["dtype"] == "f32"
     inp = oracle_inputs(w, mask)
-    for sparse in (True, False):
-        out, lse = bt.decode_sparse() if sparse else bt.decode_dense()
+    listed = None
+    for mode in ("sparse", "masked", "dense"):
+        out, lse = {"sparse": bt.decode_sparse, "masked": bt.decode_sparse_masked,
+                    "dense": bt.decode_dense}[mode]()
         torch.cuda.synchronize()
         assert bt.device_error() == 0
         o = out.cpu().numpy().reshape(-1, w["head_dim"])
         l = lse.cpu().numpy().reshape(-1)
-        ref_o, ref_l = oracle.decode(inp, sparse=sparse, bh=bh)
+        if mode == "sparse":
+            listed = o.copy(), l.copy()
+        elif mode == "masked" and same_plan(bt):
+            # same kept set, same order, same chunks: the same bits
+            assert np.array_equal(o, listed[0]) and np.array_equal(l, listed[1])
+        ref_o, ref_l = oracle.decode(inp, sparse=mode != "dense", bh=bh)
         if bh is not None:
             sel = [b * w["hq"] + h for b, h in bh]
             o, l = o[sel], l[sel]
@@ -193,9 +209,14 @@ def test_skipped_rows_are_never_read():
         p = wl.poison_unread(w, lambda b, hk: kept[b, hk], value)
         bp = DecodeBatch.from_workload(p)
         bp.build_index()
-        out = bp.decode_sparse()[0]
+        out = bp.decode_sparse()[0].clone()
+        out_m = bp.decode_sparse_masked()[0]
         torch.cuda.synchronize()
         assert torch.equal(out, base)
+        if same_plan(bp):
+            assert torch.equal(out_m, base)
+        else:
+            assert torch.isfinite(out_m).all()
 
 
 def test_batch_zero_is_a_no_op():
@@ -297,7 +318,34 @@ def test_device_errors_are_flagged():
     bt.decode_sparse()
     torch.cuda.synchronize()
     assert bt.device_error() == 6
+    # the in-kernel kept set flags the window itself; request 3 is NaN, the rest exact
+    bt.ws.zero_()
+    bt.decode_sparse_masked()
+    torch.cuda.synchronize()
+    assert bt.device_error() == 3
+    assert torch.isnan(bt.out[3]).all() and torch.isnan(bt.lse[3]).all()
+    ref, _ = oracle.decode(w, sparse=True, bh=[(b, h) for b in range(3) for h in range(w["hq"])])
+    assert_outputs(bt.out[:3].cpu().numpy(), ref, fp32=False)
     bt.window[3] = int(w["window"][3])
+    bt.ws.zero_()
+
+    # masked: a negative prompt length, then more kept rows than max_kept
+    bt.prompt_len[0] = -1
+    bt.decode_sparse_masked()
+    torch.cuda.synchronize()
+    assert bt.device_error() == 2
+    assert torch.isnan(bt.out[0]).all()
+    bt.prompt_len[0] = int(w["prompt_len"][0])
+    bt.ws.zero_()
+    small = DecodeBatch.from_workload(dict(w, max_kept=2))
+    small.decode_sparse_masked()
+    torch.cuda.synchronize()
+    assert small.device_error() == 6
+    g = w["hq"] // w["hkv"]
+    out = small.out.cpu()
+    for (b, hk), rows in oracle_kept(w).items():
+        heads = out[b, hk * g:(hk + 1) * g]
+        assert bool(torch.isnan(heads).all() if len(rows) > 2 else torch.isfinite(heads).all())
     bt.ws.zero_()
 
     # a kept index past the end of the sequence
