@@ -2,8 +2,11 @@
 """Sparse decode-attention benchmark on GB300: tokens/s and effective KV GB/s.
 
 One step = one decode token for every request of the batch through the hot
-path: dsa_build_index (mask -> kept rows) + dsa_decode_sparse (gather the kept
-K/V rows, online softmax, split-KV merge).  Inputs are synthetic (seeded),
+path as one call, dsa_decode_sparse_masked: each decode CTA reads its kept set
+from the keep mask (index compaction), gathers the kept K/V rows, runs the
+online softmax and PV, and (when rows are split) the LSE merge follows.  The
+same step as two calls, dsa_build_index (kept lists to HBM) + dsa_decode_sparse,
+and that decode alone are timed beside it.  Inputs are synthetic (seeded),
 shaped like the LlamaGen-XL-like workload by default (--config 2); other
 workloads: --config 3|4|5.  The dense causal decode of the same batch and the
 attention-mass pass are timed beside it.
@@ -61,6 +64,11 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--busy-seconds", type=float, default=1.5,
                    help="GPU busy time around the timed region for clock sampling")
+    p.add_argument("--profile", choices=["index", "sparse", "masked", "dense", "mass"],
+                   help="no timing: run W + K eager launches of one call on one KV pool "
+                        "(a small, self-contained case for ncu) and exit")
+    p.add_argument("--batch", type=int, default=0,
+                   help="with --profile: override the workload's batch size")
     return p.parse_args()
 
 
@@ -262,6 +270,11 @@ def run_ours(args):
                                      band=cfg.band, frac=cfg.top_mass_frac)
         bt.set_keep_mask(mask)
         w["keep_mask"] = mask
+    # request order for the fused call (most kept rows first when the lengths
+    # vary), from the host-side lengths a serving host has when it builds the
+    # batch; the step's inputs and results live in packed buffers so that the
+    # end-to-end run moves them in one copy each way
+    io, order = bt.pack_io(bt.schedule_order())
     bt.build_index()
     torch.cuda.synchronize()
     bt.check("build_index")
@@ -280,26 +293,29 @@ def run_ours(args):
     d = bt.dims
     K, W = args.steps, args.warmup
 
-    def sparse_step(k):
+
+    def step(k):
+        """The hot path as one call: kept sets read from the masks inside the
+        decode kernel (index compaction fused), gather, softmax, PV, merge."""
+        kp, vp = pools[k % R]
+        dsa.dsa_decode_sparse_masked(d, bt.q, kp, vp, bt.page_table, bt.seq_len, bt.prompt_len,
+                                     bt.window, bt.keep_mask, bt.scale, bt.out, bt.lse, bt.ws,
+                                     stream, order)
+
+    out_2 = torch.empty_like(bt.out)
+    lse_2 = torch.empty_like(bt.lse)
+
+    def two_call_step(k):
         kp, vp = pools[k % R]
         dsa.dsa_build_index(d, bt.seq_len, bt.prompt_len, bt.window, bt.keep_mask, bt.kept_idx,
                             bt.kept_cnt, bt.ws, stream)
         dsa.dsa_decode_sparse(d, bt.q, kp, vp, bt.page_table, bt.seq_len, bt.kept_idx,
-                              bt.kept_cnt, bt.scale, bt.out, bt.lse, bt.ws, stream)
+                              bt.kept_cnt, bt.scale, out_2, lse_2, bt.ws, stream)
 
     def decode_only(k):
         kp, vp = pools[k % R]
         dsa.dsa_decode_sparse(d, bt.q, kp, vp, bt.page_table, bt.seq_len, bt.kept_idx,
-                              bt.kept_cnt, bt.scale, bt.out, bt.lse, bt.ws, stream)
-
-    out_m = torch.empty_like(bt.out)
-    lse_m = torch.empty_like(bt.lse)
-
-    def masked_step(k):
-        kp, vp = pools[k % R]
-        dsa.dsa_decode_sparse_masked(d, bt.q, kp, vp, bt.page_table, bt.seq_len, bt.prompt_len,
-                                     bt.window, bt.keep_mask, bt.scale, out_m, lse_m, bt.ws,
-                                     stream)
+                              bt.kept_cnt, bt.scale, out_2, lse_2, bt.ws, stream)
 
     out_dense = torch.empty_like(bt.out)
     lse_dense = torch.empty_like(bt.lse)
@@ -311,63 +327,55 @@ def run_ours(args):
 
     # warm-up: W eager steps of each kind
     for k in range(W):
-        sparse_step(k)
-        masked_step(k)
+        step(k)
+        two_call_step(k)
         dense_step(k)
     torch.cuda.synchronize()
     bt.check("warm-up")
-    masked_same = bool(torch.equal(out_m, bt.out) and torch.equal(lse_m, bt.lse))
+    same_plan = (dsa.dsa_decode_plan(d, dsa.PLAN_MASKED)[:2] ==
+                 dsa.dsa_decode_plan(d, dsa.PLAN_SPARSE)[:2])
+    same_bits = bool(torch.equal(bt.out, out_2) and torch.equal(bt.lse, lse_2))
 
-    g_sparse = graph_of(sparse_step, K, stream)
+    g_step = graph_of(step, K, stream)
+    g_two = graph_of(two_call_step, K, stream)
     g_dec = graph_of(decode_only, K, stream)
-    g_masked = graph_of(masked_step, K, stream)
     g_dense = graph_of(dense_step, K, stream)
-    for g in (g_sparse, g_dec, g_masked, g_dense):
+    for g in (g_step, g_two, g_dec, g_dense):
         g.replay()  # graph upload + one more untimed pass
     torch.cuda.synchronize()
 
-    probe = time_graph(g_sparse, stream)
+    probe = time_graph(g_step, stream)
     sampler = ClockSampler(local)
     sampler.start()
-    busy(g_sparse, args.busy_seconds, probe)
+    busy(g_step, args.busy_seconds, probe)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    t_sparse = time_graph(g_sparse, stream)
+    t_step = time_graph(g_step, stream)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    busy(g_sparse, args.busy_seconds / 3, probe)
+    busy(g_step, args.busy_seconds / 3, probe)
     clocks = sampler.stop()
 
+    t_two = time_graph(g_two, stream)
     t_dec = time_graph(g_dec, stream)
-    t_masked = time_graph(g_masked, stream)
     t_dense = time_graph(g_dense, stream)
     torch.cuda.synchronize()
     bt.check("timed region")
 
     if world > 1:
-        t = torch.tensor([t_sparse, t_dec, t_masked, t_dense], device=device,
-                         dtype=torch.float64)
+        t = torch.tensor([t_step, t_two, t_dec, t_dense], device=device, dtype=torch.float64)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        t_sparse, t_dec, t_masked, t_dense = t.tolist()
+        t_step, t_two, t_dec, t_dense = t.tolist()
 
     # end-to-end through the API with host buffers: inputs H2D, result D2H, every step
-    pin = lambda t: t.cpu().pin_memory()  # noqa: E731
-    host_in = [(pin(bt.q), bt.q), (pin(bt.seq_len), bt.seq_len),
-               (pin(bt.prompt_len), bt.prompt_len), (pin(bt.window), bt.window),
-               (pin(bt.keep_mask), bt.keep_mask), (pin(bt.page_table), bt.page_table)]
-    host_out = [(bt.out, torch.empty(bt.out.shape, dtype=bt.out.dtype).pin_memory()),
-                (bt.lse, torch.empty(bt.lse.shape, dtype=bt.lse.dtype).pin_memory())]
-    h2d = sum(h.numel() * h.element_size() for h, _ in host_in)
-    d2h = sum(h.numel() * h.element_size() for _, h in host_out)
+    h2d, d2h = io.h2d_bytes, io.d2h_bytes
 
     def e2e_step(k):
-        for h, dv in host_in:
-            dv.copy_(h, non_blocking=True)
-        sparse_step(k)
-        for dv, h in host_out:
-            h.copy_(dv, non_blocking=True)
+        io.upload()
+        step(k)
+        io.download()
 
     for k in range(min(W, 3)):
         e2e_step(k)
@@ -405,14 +413,15 @@ def run_ours(args):
         mass_ms = 1e3 * time_graph(g_mass, stream) / min(K, 50)
 
     B = w["batch"]
-    ms_step = 1e3 * t_sparse / K
-    tokens = world * B / (t_sparse / K)
+    step_s = t_step / K
+    tokens = world * B / step_s
     peak, peak_src = hbm_peak()
-    dec_s = t_dec / K
-    achieved = by["sparse_decode"] / dec_s / 1e9
-    _, _, launches_dec = dsa.dsa_decode_plan(d, True)
-    _, _, launches_dense = dsa.dsa_decode_plan(d, False)
-    chunk, nch, _ = dsa.dsa_decode_plan(d, True)
+    chunk, nch, launches = dsa.dsa_decode_plan(d, dsa.PLAN_MASKED)
+    _, _, launches_two = dsa.dsa_decode_plan(d, dsa.PLAN_SPARSE)
+    achieved = by["masked"] / step_s / 1e9
+    kernel = "decode_kernel, kept set read from the keep mask (dsa_decode_sparse_masked)"
+    if launches > 1:
+        kernel += " + LSE merge kernel"
 
     result = {
         "metric": METRIC,
@@ -421,7 +430,7 @@ def run_ours(args):
         "n_gpus": world,
         "steps": K,
         "warmup": W,
-        "ms_per_step": ms_step,
+        "ms_per_step": 1e3 * step_s,
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -436,40 +445,47 @@ def run_ours(args):
             "l2": f"inputs larger than L2: {R} rotating KV pool copies, "
                   f"{R * by['kv'] / 1e6:.0f} MB of kept rows per rotation (L2 {l2 / 1e6:.0f} MB)",
             "parallelism": f"replicas x{world}",
+            "step": "dsa_decode_sparse_masked: index compaction + gather + softmax + PV "
+                    "(+ merge) in one call",
+            "request_order": "longest first" if order is not None else "batch order",
             "decode_chunk_rows": chunk, "decode_chunks_max": nch,
         },
-        "effective_kv_gbs": by["step"] / (t_sparse / K) / 1e9,
-        "pct_of_hbm_peak": 100.0 * by["step"] / (t_sparse / K) / 1e9 / peak,
-        "step_bytes": by["step"],
+        "effective_kv_gbs": by["masked"] / step_s / 1e9,
+        "pct_of_hbm_peak": 100.0 * by["masked"] / step_s / 1e9 / peak,
+        "step_bytes": by["masked"],
         "roofline": {
-            "kernel": "dsa_decode_sparse (decode + LSE merge kernels)",
+            "kernel": kernel,
             "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
             "frac": achieved / peak, "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
             if peak_src == "measured" else "fallback 6.8 TB/s",
             "traffic": None,
-            "bytes_per_launch": by["sparse_decode"], "launch_us": 1e6 * dec_s,
+            "bytes_per_launch": by["masked"], "launch_us": 1e6 * step_s,
+        },
+        "two_call_step": {
+            "calls": "dsa_build_index + dsa_decode_sparse (kept lists through HBM)",
+            "ms_per_step": 1e3 * t_two / K,
+            "tokens_per_s": world * B / (t_two / K),
+            "bytes": by["step"],
+            "gbs": by["step"] / (t_two / K) / 1e9,
+            "decode_only_us": 1e6 * t_dec / K,
+            "decode_only_gbs": by["sparse_decode"] / (t_dec / K) / 1e9,
+            "decode_only_frac": by["sparse_decode"] / (t_dec / K) / 1e9 / peak,
+            "launches_per_step": 1 + launches_two,
+            "same_bits_as_fused": same_bits if same_plan else None,
         },
         "sparse_vs_dense": {
             "dense_ms_per_step": 1e3 * t_dense / K,
             "dense_tokens_per_s": world * B / (t_dense / K),
-            "speedup": t_dense / t_sparse,
+            "speedup": t_dense / t_step,
             "kept_fraction": by["rows"] / by["dense_rows"],
             "dense_bytes": by["dense"],
             "dense_gbs": by["dense"] / (t_dense / K) / 1e9,
-        },
-        "fused_index_decode": {
-            "call": "dsa_decode_sparse_masked (kept set built in the decode kernel)",
-            "ms_per_step": 1e3 * t_masked / K,
-            "tokens_per_s": world * B / (t_masked / K),
-            "bytes": by["masked"],
-            "gbs": by["masked"] / (t_masked / K) / 1e9,
-            "same_bits_as_two_calls": masked_same,
         },
         "attention_mass_ms": mass_ms,
         "e2e": {"value": world * B / (t_e2e / K), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": 1e3 * t_e2e / K},
-        "gpu_launches": K * (1 + launches_dec),
+        "gpu_launches": K * launches,
         "clocks": clocks,
     }
 
@@ -538,9 +554,40 @@ def run_reference(args):
     }), flush=True)
 
 
+def run_profile(args):
+    """W + K eager launches of one library call on one KV pool, for a profiler
+    to capture (launch j of the call is the j-th launch of its kernel)."""
+    device = torch.device("cuda", 0)
+    cfg = wl.CONFIGS[args.config]
+    if args.batch > 0:
+        cfg = wl.scaled(cfg, batch=args.batch)
+    w = wl.generate(cfg, device=str(device))
+    bt = DecodeBatch.from_workload(w, device=device)
+    if cfg.mask == "top_mass":
+        _, om = bt.attention_mass(r_local=2, r_diag=2)
+        bt.set_keep_mask(wl.top_mass_keep_mask(om.cpu().numpy(), w["window"], w["hkv"],
+                                               w["mask_words"], band=cfg.band,
+                                               frac=cfg.top_mass_frac))
+    bt.build_index()
+    order = bt.schedule_order()
+    order = None if order is None else torch.as_tensor(order).to(device)
+    call = {"index": bt.build_index, "sparse": bt.decode_sparse,
+            "masked": lambda: bt.decode_sparse_masked(request_order=order),
+            "dense": bt.decode_dense,
+            "mass": lambda: bt.attention_mass(r_local=2, r_diag=2)}[args.profile]
+    for _ in range(args.warmup + args.steps):
+        call()
+    torch.cuda.synchronize()
+    bt.check(args.profile)
+    print(json.dumps({"profile": args.profile, "workload": cfg.name, "batch": cfg.batch,
+                      "launches": args.warmup + args.steps}), flush=True)
+
+
 def main():
     args = parse_args()
-    if args.impl == "reference":
+    if args.profile:
+        run_profile(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -84,7 +84,8 @@ enum {
   DSA_DEV_BAD_INDEX = 5,    /* kept index outside 0..seq_len-1             */
   DSA_DEV_BAD_COUNT = 6,    /* kept count < 1 or > max_kept                */
   DSA_DEV_TIMEOUT = 7,      /* a bounded wait for an async copy gave up    */
-  DSA_DEV_BAD_GRID_W = 8    /* grid width < 1 (attention mass)             */
+  DSA_DEV_BAD_GRID_W = 8,   /* grid width < 1 (attention mass)             */
+  DSA_DEV_BAD_ORDER = 9     /* request_order entry outside 0..batch-1      */
 };
 
 /* Problem sizes, shared by all calls on one KV cache. */
@@ -164,6 +165,15 @@ dsa_status dsa_decode_sparse(const dsa_dims* dims, const void* q, const void* k_
  *   q, k_pages, v_pages, page_table, seq_len, scale, out, lse  as in
  *                     dsa_decode_sparse
  *   prompt_len, window, keep_mask  as in dsa_build_index
+ *   request_order     [batch] int32 (device), or NULL: a permutation of
+ *                     0..batch-1 giving the order in which requests are handed
+ *                     to the GPU (NULL: 0, 1, ...).  Results do not depend on
+ *                     it; scheduling the requests with the most kept rows
+ *                     first (e.g. by min(P,L) + min(W, L-1-min(P,L))) shortens
+ *                     the tail of a batch with mixed lengths.  An entry
+ *                     outside 0..batch-1 sets DSA_DEV_BAD_ORDER and is
+ *                     skipped; a request missing from a non-permutation is
+ *                     left unspecified.
  * max_window must be <= 1024 (each warp holds the window's mask bits, one
  * 32-bit word per lane), else DSA_ERR_UNSUPPORTED: use the two calls then.  Invalid per-request data
  * (the DSA_DEV_BAD_SEQ_LEN / _PROMPT / _WINDOW / _COUNT cases of
@@ -174,8 +184,9 @@ dsa_status dsa_decode_sparse(const dsa_dims* dims, const void* q, const void* k_
 dsa_status dsa_decode_sparse_masked(const dsa_dims* dims, const void* q, const void* k_pages,
                                     const void* v_pages, const int32_t* page_table,
                                     const int32_t* seq_len, const int32_t* prompt_len,
-                                    const int32_t* window, const uint32_t* keep_mask, float scale,
-                                    float* out, float* lse, void* ws, void* stream);
+                                    const int32_t* window, const uint32_t* keep_mask,
+                                    const int32_t* request_order, float scale, float* out,
+                                    float* lse, void* ws, void* stream);
 
 /*
  * dsa_decode_dense -- the dense causal baseline: the same as dsa_decode_sparse

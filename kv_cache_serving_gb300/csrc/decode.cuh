@@ -32,6 +32,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "mma.cuh"
 
 namespace dsa {
 
@@ -109,34 +110,6 @@ __device__ __forceinline__ void vec_to_f32<float>(const uint4& v, float* o) {
   o[3] = __uint_as_float(v.w);
 }
 
-// ---- tensor-core helpers (mma.sync m16n8k16, bf16 inputs, fp32 accumulate) ----
-__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(smem_addr(p))
-               : "memory");
-}
-__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], const void* p) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(smem_addr(p))
-               : "memory");
-}
-// d (16x8, fp32) += a (16x16, bf16, row) * b (16x8, bf16, col)
-__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-      "{%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-__device__ __forceinline__ uint16_t f32_to_bf16_rn(float x) {
-  uint16_t h;
-  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(h) : "f"(x));
-  return h;
-}
-
 // Rows of the work list of (b, hk), or a negative device error code.  Shared
 // by the decode and merge kernels so that both take the same decision.
 // Row sources of the decode kernel (the launch modes of internal.h).
@@ -182,7 +155,12 @@ __global__ void __launch_bounds__(DecodeTiling<D, KV, G, QMIX && G >= 2>::NW * 3
   extern __shared__ __align__(128) unsigned char smem[];
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int c = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
+  const int c = blockIdx.x, hk = blockIdx.y;
+  const int b = a.order != nullptr ? __ldg(a.order + blockIdx.z) : static_cast<int>(blockIdx.z);
+  if (static_cast<unsigned>(b) >= static_cast<unsigned>(a.batch)) {
+    if (c == 0 && hk == 0 && threadIdx.x == 0) set_error(a.err, DSA_DEV_BAD_ORDER);
+    return;
+  }
   const int L = a.seq_len[b];
   // kRowsMask: the kept set is read straight from the keep mask.  Lane l holds
   // the bits of window offsets 32l+1 .. 32l+32 that lie in 1..omax (wbits) and

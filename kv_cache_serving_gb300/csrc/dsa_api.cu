@@ -156,6 +156,7 @@ struct RowSource {
   const int32_t* prompt_len = nullptr;
   const int32_t* window = nullptr;
   const uint32_t* keep_mask = nullptr;
+  const int32_t* order = nullptr;
 };
 
 dsa_status decode_common(const dsa_dims* d, int mode, const void* q, const void* k,
@@ -188,6 +189,7 @@ dsa_status decode_common(const dsa_dims* d, int mode, const void* q, const void*
   a.window = rs.window;
   a.keep_mask = rs.keep_mask;
   a.unit_rows = mode == kModeMask ? unit_rows(d, ws) : nullptr;
+  a.order = rs.order;
   a.max_window = d->max_window;
   a.mask_words = d->mask_words;
   a.batch = d->batch;
@@ -279,12 +281,14 @@ dsa_status dsa_decode_sparse(const dsa_dims* dims, const void* q, const void* k_
 dsa_status dsa_decode_sparse_masked(const dsa_dims* dims, const void* q, const void* k_pages,
                                     const void* v_pages, const int32_t* page_table,
                                     const int32_t* seq_len, const int32_t* prompt_len,
-                                    const int32_t* window, const uint32_t* keep_mask, float scale,
-                                    float* out, float* lse, void* ws, void* stream) {
+                                    const int32_t* window, const uint32_t* keep_mask,
+                                    const int32_t* request_order, float scale, float* out,
+                                    float* lse, void* ws, void* stream) {
   RowSource rs;
   rs.prompt_len = prompt_len;
   rs.window = window;
   rs.keep_mask = keep_mask;
+  rs.order = request_order;
   return decode_common(dims, kModeMask, q, k_pages, v_pages, page_table, seq_len, rs, scale, out,
                        lse, ws, stream);
 }
@@ -331,8 +335,12 @@ dsa_status dsa_attention_mass(const dsa_dims* dims, const void* q, const void* k
   a.max_window = dims->max_window;
   a.r_local = r_local;
   a.r_diag = r_diag;
-  choose_chunks(n_max, static_cast<int64_t>(dims->batch) * dims->hkv, sm_count() * 2,
-                kChunkQuantum, DSA_MASS_WAVES, &a.chunk, &a.num_chunks);
+  const bool kv_bf16 = dims->kv_dtype == DSA_BF16, q_bf16 = dims->q_dtype == DSA_BF16;
+  const int g = dims->hq / dims->hkv;
+  choose_chunks(n_max, static_cast<int64_t>(dims->batch) * dims->hkv,
+                sm_count() * mass_ctas_per_sm(dims->head_dim, g, kv_bf16, q_bf16),
+                mass_rows_per_pass(dims->head_dim, g, kv_bf16, q_bf16), DSA_MASS_WAVES, &a.chunk,
+                &a.num_chunks);
   a.scale_log2 = scale * kLog2e;
   a.mass = mass;
   a.offset_mass = offset_mass;

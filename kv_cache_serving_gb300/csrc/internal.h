@@ -26,6 +26,7 @@ struct DecodeLaunch {
   const int32_t* window;      // kRowsMask only
   const uint32_t* keep_mask;  // kRowsMask only: [batch][hkv][mask_words]
   int32_t* unit_rows;         // kRowsMask only: [batch][hkv] kept count or -error
+  const int32_t* order;       // [batch] request scheduled at each grid z, or null (z itself)
   int32_t batch, hq, hkv, head_dim, max_pages, num_pages, max_kept;
   int32_t max_window, mask_words;  // kRowsMask only
   int32_t chunk, num_chunks;
@@ -80,6 +81,10 @@ cudaError_t launch_decode_bf16(const DecodeLaunch& a, int mode, cudaStream_t s);
 cudaError_t launch_decode_f32(const DecodeLaunch& a, int mode, cudaStream_t s);
 cudaError_t launch_merge(const DecodeLaunch& a, int mode, cudaStream_t s);
 cudaError_t launch_mass(const MassLaunch& a, bool kv_bf16, cudaStream_t s);
+// Rows one pass of all warps of an attention-mass CTA covers, and its resident
+// CTAs per SM (>= 1), for the host's chunk choice.
+int mass_rows_per_pass(int head_dim, int group, bool kv_bf16, bool q_bf16);
+int mass_ctas_per_sm(int head_dim, int group, bool kv_bf16, bool q_bf16);
 cudaError_t launch_compact(const CompactLaunch& a, cudaStream_t s);
 
 // Rows one pass of all warps of a decode CTA covers (warps x tile rows), for

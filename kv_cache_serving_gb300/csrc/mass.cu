@@ -14,10 +14,15 @@
 // sums, all rescaled together like the online-softmax sum.  Window rows store
 // their raw log2-domain score into offset_mass; mass_merge_kernel combines the
 // chunks by log-sum-exp and turns raw scores into weights exp2(s - lse2).
+//
+// Two score engines: mass_mma_kernel (bf16 q and K, grouped-query heads) puts
+// the G dot products of 16-row blocks on the tensor cores; mass_kernel (every
+// other case) sums per-lane partial dot products with a reduce-scatter.
 #include <math.h>
 
 #include "common.cuh"
 #include "internal.h"
+#include "mma.cuh"
 
 namespace dsa {
 
@@ -52,6 +57,17 @@ __device__ __forceinline__ int mass_request_check(const MassLaunch& a, int b, in
   if (*W < 0 || *W > a.max_window) return DSA_DEV_BAD_WINDOW;
   if (*w < 1) return DSA_DEV_BAD_GRID_W;
   return 0;
+}
+
+// Bin of row j (offset o = i - j) under the rule in the file comment.
+__device__ __forceinline__ int mass_bin(const MassLaunch& a, int j, int o, int P, int W, int w) {
+  if (j < P) return 0;
+  if (o <= a.r_local) return 1;
+  if (o <= W) {
+    const int k0 = o / w;
+    if ((k0 >= 1 && o - k0 * w <= a.r_diag) || ((k0 + 1) * w - o <= a.r_diag)) return 2;
+  }
+  return 3;
 }
 
 template <int D, typename KV, int G>
@@ -128,8 +144,8 @@ __global__ void __launch_bounds__(MassTiling<D, KV, G>::NW * 32) mass_kernel(con
   int failed_at = -1;
   for (int t = 0; t < my_tiles; ++t) {
     const int stage = t % S;
-    if (!mbar_wait(&bars[stage], static_cast<uint32_t>(t / S) & 1u)) {
-      failed_at = t;
+    if (!__all_sync(0xffffffffu, mbar_wait(&bars[stage], static_cast<uint32_t>(t / S) & 1u))) {
+      failed_at = t;  // the whole warp leaves together
       break;
     }
     const int tr0 = row0 + (warp + t * NW) * T;
@@ -151,15 +167,7 @@ __global__ void __launch_bounds__(MassTiling<D, KV, G>::NW * 32) mass_kernel(con
     // bin of this lane's row
     const int j = tr0 + myrow;
     const int o = i - j;
-    int bin = 3;
-    if (j < P) {
-      bin = 0;
-    } else if (o <= a.r_local) {
-      bin = 1;
-    } else if (o <= W) {
-      const int k0 = o / w;
-      if ((k0 >= 1 && o - k0 * w <= a.r_diag) || ((k0 + 1) * w - o <= a.r_diag)) bin = 2;
-    }
+    const int bin = mass_bin(a, j, o, P, W, w);
     const bool valid = myrow < nrows;
 #pragma unroll
     for (int h = 0; h < G; ++h) {
@@ -197,6 +205,244 @@ __global__ void __launch_bounds__(MassTiling<D, KV, G>::NW * 32) mass_kernel(con
       mw[1] = l;
 #pragma unroll
       for (int k = 0; k < 4; ++k) mw[2 + k] = bs[k];
+    }
+  }
+  __syncthreads();
+  for (int x = threadIdx.x; x < G * kMassPart; x += NW * 32) {
+    const int h = x / kMassPart, f = x % kMassPart;
+    float mstar = -INFINITY;
+#pragma unroll
+    for (int ww = 0; ww < NW; ++ww) mstar = fmaxf(mstar, mbuf[(ww * G + h) * kMassPart]);
+    float v = mstar;
+    if (f > 0) {
+      v = 0.f;
+#pragma unroll
+      for (int ww = 0; ww < NW; ++ww) {
+        const float* src = mbuf + (ww * G + h) * kMassPart;
+        const float sc = src[0] == -INFINITY ? 0.f : exp2f(src[0] - mstar);
+        v = fmaf(sc, src[f], v);
+      }
+    }
+    const size_t qh = static_cast<size_t>(b) * a.hq + hk * G + h;
+    a.part[(qh * a.num_chunks + c) * kMassPart + f] = v;
+  }
+}
+
+// Tensor-core tiling: K rows only, T rows per tile, rows padded by 16 bytes so
+// that the ldmatrix row addresses of one 8x8 tile fall in distinct banks.
+template <int D>
+struct MassMmaTiling {
+  static constexpr int kRowBytes = D * 2;
+  static constexpr int T = 8192 / kRowBytes > 64 ? 64 : 8192 / kRowBytes;
+  static constexpr int S = 2;
+  static constexpr int NW = 4;
+  static constexpr int kRowStride = kRowBytes + 16;
+  static constexpr int kStageBytes = T * kRowStride;
+  static constexpr int kWarpBytes = S * kStageBytes;
+  static constexpr int kBarOff = NW * kWarpBytes;
+  static constexpr int kMOff = kBarOff + NW * S * 8;
+  static constexpr int kSmem = kMOff + NW * 8 * kMassPart * 4;
+};
+
+// Scores S = K q^T of a 16-row block with mma.sync m16n8k16 (A: 16 K rows x
+// 16 dims via ldmatrix, B: q of the G <= 8 heads as columns).  Thread (g4 =
+// lane/4, tig = lane%4) ends with rows g4 and g4+8 of the block for heads
+// 2 tig and 2 tig + 1, the layout of the mma accumulator.
+template <int D, int G>
+__global__ void __launch_bounds__(MassMmaTiling<D>::NW * 32)
+    mass_mma_kernel(const MassLaunch a) {
+  using Tl = MassMmaTiling<D>;
+  constexpr int T = Tl::T, S = Tl::S, NW = Tl::NW, RB = T / 16, NK = D / 16, RPL = T / 32;
+  constexpr int kRowBytes = Tl::kRowBytes, kRowStride = Tl::kRowStride;
+  extern __shared__ __align__(128) unsigned char smem[];
+
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int c = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
+  int L, P, W, w;
+  const int code = mass_request_check(a, b, &L, &P, &W, &w);
+  if (code != 0) {
+    if (c == 0 && threadIdx.x == 0) set_error(a.err, code);
+    return;
+  }
+  const int i = L - 1;
+  const int row0 = c * a.chunk;
+  if (row0 >= L) return;
+  const int row1 = min(L, row0 + a.chunk);
+  const int ntiles = (row1 - row0 + T - 1) / T;
+  const int my_tiles = warp < ntiles ? (ntiles - warp + NW - 1) / NW : 0;
+
+  unsigned char* kst = smem + warp * Tl::kWarpBytes;  // [S][T] K rows, kRowStride apart
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Tl::kBarOff) + warp * S;
+  float* mbuf = reinterpret_cast<float*>(smem + Tl::kMOff);  // [NW][G][6]
+  if (lane == 0) {
+#pragma unroll
+    for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+
+  const bf16_t* kg = reinterpret_cast<const bf16_t*>(a.k);
+  const int32_t* pt = a.page_table + static_cast<size_t>(b) * a.max_pages;
+  auto tile_r0 = [&](int t) { return row0 + (warp + t * NW) * T; };
+  // page ids of this lane's rows (lane + 32 u) of tile t, loaded a tile ahead
+  auto load_pg = [&](int t, int (&pg)[RPL]) {
+#pragma unroll
+    for (int u = 0; u < RPL; ++u) {
+      const int j = tile_r0(t) + lane + 32 * u;
+      pg[u] = (t < my_tiles && j < row1) ? __ldg(pt + (j >> 4)) : 0;
+    }
+  };
+  auto issue = [&](int t, int stage, const int (&pg)[RPL]) {
+    const int tr0 = tile_r0(t);
+    const int nrows = min(T, row1 - tr0);
+    if (lane == 0) mbar_arrive_expect_tx(&bars[stage], static_cast<uint32_t>(nrows * kRowBytes));
+    __syncwarp();
+#pragma unroll
+    for (int u = 0; u < RPL; ++u) {
+      const int r = lane + 32 * u;
+      if (r < nrows) {
+        int p = pg[u];
+        if (static_cast<unsigned>(p) >= static_cast<unsigned>(a.num_pages)) {
+          set_error(a.err, DSA_DEV_BAD_PAGE);
+          p = 0;
+        }
+        const int j = tr0 + r;
+        const size_t off = ((static_cast<size_t>(p) * kPage + (j & (kPage - 1))) * a.hkv + hk) * D;
+        bulk_copy_g2s(kst + (static_cast<size_t>(stage) * T + r) * kRowStride, kg + off, kRowBytes,
+                      &bars[stage]);
+      }
+    }
+  };
+
+  const int g4 = lane >> 2, tig = lane & 3;
+  uint32_t qf[NK][2];
+  {
+    const uint32_t* q32 = reinterpret_cast<const uint32_t*>(a.q) +
+                          (static_cast<size_t>(b) * a.hq + hk * G + (g4 < G ? g4 : 0)) * (D / 2);
+#pragma unroll
+    for (int kk = 0; kk < NK; ++kk) {
+      qf[kk][0] = g4 < G ? __ldg(q32 + kk * 8 + tig) : 0u;
+      qf[kk][1] = g4 < G ? __ldg(q32 + kk * 8 + 4 + tig) : 0u;
+    }
+  }
+  float m2[2], l2[2], bins[2][4];
+#pragma unroll
+  for (int jj = 0; jj < 2; ++jj) {
+    m2[jj] = -INFINITY;
+    l2[jj] = 0.f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) bins[jj][k] = 0.f;
+  }
+
+  int pgn[RPL];
+#pragma unroll
+  for (int t = 0; t < S; ++t) {
+    if (t < my_tiles) {
+      load_pg(t, pgn);
+      issue(t, t, pgn);
+    }
+  }
+  load_pg(S, pgn);
+
+  const size_t om_stride = static_cast<size_t>(a.max_window) + 1;
+  int failed_at = -1;
+  for (int t = 0; t < my_tiles; ++t) {
+    const int stage = t % S;
+    if (!__all_sync(0xffffffffu, mbar_wait(&bars[stage], static_cast<uint32_t>(t / S) & 1u))) {
+      failed_at = t;  // the whole warp leaves together
+      break;
+    }
+    const int tr0 = tile_r0(t);
+    const int nrows = min(T, row1 - tr0);
+    const unsigned char* kt = kst + static_cast<size_t>(stage) * T * kRowStride;
+    float sm[RB][4];
+#pragma unroll
+    for (int rb = 0; rb < RB; ++rb) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sm[rb][e] = 0.f;
+      const unsigned char* arow =
+          kt + (rb * 16 + (lane & 7) + 8 * ((lane >> 3) & 1)) * kRowStride + 16 * (lane >> 4);
+#pragma unroll
+      for (int kk = 0; kk < NK; ++kk) {
+        uint32_t af[4];
+        ldsm_x4(af, arow + 32 * kk);
+        mma_bf16(sm[rb], af, qf[kk][0], qf[kk][1]);
+      }
+    }
+    // bins and window offsets of the thread's rows (shared by its two heads)
+    int rbin[RB][2], roff[RB][2];
+#pragma unroll
+    for (int rb = 0; rb < RB; ++rb)
+#pragma unroll
+      for (int hi = 0; hi < 2; ++hi) {
+        const int r = rb * 16 + g4 + 8 * hi;
+        const int j = tr0 + r;
+        roff[rb][hi] = r < nrows ? i - j : -1;
+        rbin[rb][hi] = r < nrows ? mass_bin(a, j, i - j, P, W, w) : 3;
+      }
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
+      const int h = 2 * tig + jj;
+      float tmax = -INFINITY;
+#pragma unroll
+      for (int rb = 0; rb < RB; ++rb)
+#pragma unroll
+        for (int hi = 0; hi < 2; ++hi) {
+          float& x = sm[rb][2 * hi + jj];
+          x = roff[rb][hi] >= 0 ? x * a.scale_log2 : -INFINITY;
+          tmax = fmaxf(tmax, x);
+          if (h < G && roff[rb][hi] >= 0 && roff[rb][hi] <= W && a.offset_mass != nullptr)
+            a.offset_mass[(static_cast<size_t>(b) * a.hq + hk * G + h) * om_stride +
+                          roff[rb][hi]] = x;
+        }
+      tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 4));
+      tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 8));
+      tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
+      const float mnew = fmaxf(m2[jj], tmax);
+      const float alpha = exp2f(m2[jj] - mnew);
+      m2[jj] = mnew;
+      float psum = 0.f, pb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int rb = 0; rb < RB; ++rb)
+#pragma unroll
+        for (int hi = 0; hi < 2; ++hi) {
+          const float p = exp2f(sm[rb][2 * hi + jj] - mnew);
+          psum += p;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) pb[k] += rbin[rb][hi] == k ? p : 0.f;
+        }
+      l2[jj] = l2[jj] * alpha + psum;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) bins[jj][k] = bins[jj][k] * alpha + pb[k];
+    }
+    __syncwarp();
+    fence_proxy_async_smem();
+    if (t + S < my_tiles) issue(t + S, stage, pgn);
+    load_pg(t + S + 1, pgn);
+  }
+  if (failed_at >= 0) {
+    // Give the copies still in flight a bounded chance to land before exiting.
+    if (lane == 0) set_error(a.err, DSA_DEV_TIMEOUT);
+    for (int t = failed_at; t < my_tiles && t < failed_at + S; ++t)
+      mbar_wait(&bars[t % S], static_cast<uint32_t>(t / S) & 1u);
+  }
+
+  // the 8 lanes of a column pair share m; sum their l and bins
+#pragma unroll
+  for (int jj = 0; jj < 2; ++jj) {
+    float v[5] = {l2[jj], bins[jj][0], bins[jj][1], bins[jj][2], bins[jj][3]};
+#pragma unroll
+    for (int f = 0; f < 5; ++f) {
+      v[f] += __shfl_xor_sync(0xffffffffu, v[f], 4);
+      v[f] += __shfl_xor_sync(0xffffffffu, v[f], 8);
+      v[f] += __shfl_xor_sync(0xffffffffu, v[f], 16);
+    }
+    const int h = 2 * tig + jj;
+    if (g4 == 0 && h < G) {
+      float* mw = mbuf + (warp * G + h) * kMassPart;
+      mw[0] = m2[jj];
+#pragma unroll
+      for (int f = 0; f < 5; ++f) mw[1 + f] = v[f];
     }
   }
   __syncthreads();
@@ -260,14 +506,17 @@ __global__ void __launch_bounds__(128) mass_merge_kernel(const MassLaunch a) {
   }
 }
 
-template <int D, typename KV, int G>
-cudaError_t launch_mass_one(const MassLaunch& a, cudaStream_t s) {
-  using Tl = MassTiling<D, KV, G>;
-  auto kern = mass_kernel<D, KV, G>;
-  cudaError_t e =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Tl::kSmem);
+// Tensor cores for bf16 q and K with grouped-query heads.
+inline bool mass_uses_mma(bool kv_bf16, bool q_bf16, int group) {
+  return kv_bf16 && q_bf16 && group >= 2;
+}
+
+template <typename Kern>
+cudaError_t launch_mass_kernel(Kern kern, int smem, int threads, const MassLaunch& a,
+                               cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<dim3(a.num_chunks, a.hkv, a.batch), Tl::NW * 32, Tl::kSmem, s>>>(a);
+  kern<<<dim3(a.num_chunks, a.hkv, a.batch), threads, smem, s>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int pairs = a.batch * a.hq;
@@ -275,25 +524,78 @@ cudaError_t launch_mass_one(const MassLaunch& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-template <typename KV>
-cudaError_t launch_mass_t(const MassLaunch& a, cudaStream_t s) {
-  const int g = a.hq / a.hkv;
-#define DSA_CASE(DD, GG) \
-  if (a.head_dim == DD && g == GG) return launch_mass_one<DD, KV, GG>(a, s);
-  DSA_CASE(64, 1)
-  DSA_CASE(64, 2)
-  DSA_CASE(64, 4)
-  DSA_CASE(64, 8)
-  DSA_CASE(128, 1)
-  DSA_CASE(128, 2)
-  DSA_CASE(128, 4)
-  DSA_CASE(128, 8)
+// Calls f(kernel, dynamic smem, threads per CTA, rows per CTA pass) for the
+// instantiation that serves (head_dim, group, dtypes); returns `fallback` when
+// none does.
+template <typename F, typename R>
+R with_mass_kernel(int head_dim, int group, bool kv_bf16, bool q_bf16, F f, R fallback) {
+#define DSA_MMA_CASE(DD, GG)                                                            \
+  if (head_dim == DD && group == GG) {                                                  \
+    using Tl = MassMmaTiling<DD>;                                                       \
+    return f(mass_mma_kernel<DD, GG>, Tl::kSmem, Tl::NW * 32, Tl::NW * Tl::T);          \
+  }
+#define DSA_CASE(KV, DD, GG)                                                            \
+  if (head_dim == DD && group == GG) {                                                  \
+    using Tl = MassTiling<DD, KV, GG>;                                                  \
+    return f(mass_kernel<DD, KV, GG>, Tl::kSmem, Tl::NW * 32, Tl::NW * Tl::T);          \
+  }
+  if (mass_uses_mma(kv_bf16, q_bf16, group)) {
+    DSA_MMA_CASE(64, 2)
+    DSA_MMA_CASE(64, 4)
+    DSA_MMA_CASE(64, 8)
+    DSA_MMA_CASE(128, 2)
+    DSA_MMA_CASE(128, 4)
+    DSA_MMA_CASE(128, 8)
+  } else if (kv_bf16) {
+    DSA_CASE(bf16_t, 64, 1)
+    DSA_CASE(bf16_t, 64, 2)
+    DSA_CASE(bf16_t, 64, 4)
+    DSA_CASE(bf16_t, 64, 8)
+    DSA_CASE(bf16_t, 128, 1)
+    DSA_CASE(bf16_t, 128, 2)
+    DSA_CASE(bf16_t, 128, 4)
+    DSA_CASE(bf16_t, 128, 8)
+  } else {
+    DSA_CASE(float, 64, 1)
+    DSA_CASE(float, 64, 2)
+    DSA_CASE(float, 64, 4)
+    DSA_CASE(float, 64, 8)
+    DSA_CASE(float, 128, 1)
+    DSA_CASE(float, 128, 2)
+    DSA_CASE(float, 128, 4)
+    DSA_CASE(float, 128, 8)
+  }
+#undef DSA_MMA_CASE
 #undef DSA_CASE
-  return cudaErrorInvalidValue;
+  return fallback;
 }
 
 cudaError_t launch_mass(const MassLaunch& a, bool kv_bf16, cudaStream_t s) {
-  return kv_bf16 ? launch_mass_t<bf16_t>(a, s) : launch_mass_t<float>(a, s);
+  return with_mass_kernel(
+      a.head_dim, a.hq / a.hkv, kv_bf16, a.q_bf16 != 0,
+      [&](auto kern, int smem, int threads, int) {
+        return launch_mass_kernel(kern, smem, threads, a, s);
+      },
+      cudaErrorInvalidValue);
+}
+
+int mass_rows_per_pass(int head_dim, int group, bool kv_bf16, bool q_bf16) {
+  return with_mass_kernel(
+      head_dim, group, kv_bf16, q_bf16, [](auto, int, int, int rows) { return rows; }, 0);
+}
+
+int mass_ctas_per_sm(int head_dim, int group, bool kv_bf16, bool q_bf16) {
+  return with_mass_kernel(
+      head_dim, group, kv_bf16, q_bf16,
+      [](auto kern, int smem, int threads, int) {
+        int n = 0;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+                cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, smem) != cudaSuccess)
+          return 1;
+        return n < 1 ? 1 : n;
+      },
+      1);
 }
 
 }  // namespace dsa

@@ -18,6 +18,68 @@ def _i32(x, device):
     return torch.as_tensor(np.ascontiguousarray(x, dtype=np.int32)).to(device)
 
 
+def estimated_kept_rows(lengths) -> np.ndarray:
+    """Upper estimate of each request's kept rows, min(P,L) + min(W, L-1-min(P,L)) + 1,
+    from host arrays (seq_len, prompt_len, window)."""
+    L, P, W = (np.asarray(x, dtype=np.int64) for x in lengths)
+    npr = np.minimum(P, L)
+    return npr + np.minimum(np.maximum(L - 1 - npr, 0), W) + 1
+
+
+def longest_first_order(lengths) -> np.ndarray:
+    """int32 permutation of the requests by decreasing estimated kept rows (ties
+    by index)."""
+    return np.argsort(-estimated_kept_rows(lengths), kind="stable").astype(np.int32)
+
+
+def schedule_order(lengths, spread: float = 1.25):
+    """The request_order a serving host would pass: longest first when the
+    estimated kept rows of the batch vary (max > spread * mean), else None
+    (batch order; an order costs each CTA one dependent load)."""
+    est = estimated_kept_rows(lengths)
+    if est.size == 0 or est.max() <= spread * est.mean():
+        return None
+    return longest_first_order(lengths)
+
+
+class PackedIO:
+    """One pinned host buffer and one device buffer per direction, so that a
+    step's inputs go up in one copy and its results come back in one.  The
+    batch's tensors become views into the device buffers."""
+
+    def __init__(self, inputs: dict, outputs: dict, device):
+        def layout(tensors):
+            offs, at = {}, 0
+            for name, t in tensors.items():
+                offs[name] = at
+                at += (t.numel() * t.element_size() + 255) // 256 * 256
+            return offs, max(at, 256)
+        self._in_off, n_in = layout(inputs)
+        self._out_off, n_out = layout(outputs)
+        self.dev_in = torch.empty(n_in, dtype=torch.uint8, device=device)
+        self.dev_out = torch.empty(n_out, dtype=torch.uint8, device=device)
+        self.host_in = torch.empty(n_in, dtype=torch.uint8).pin_memory()
+        self.host_out = torch.empty(n_out, dtype=torch.uint8).pin_memory()
+        self.dev, self.host = {}, {}
+        for offs, dbuf, hbuf, tensors in ((self._in_off, self.dev_in, self.host_in, inputs),
+                                          (self._out_off, self.dev_out, self.host_out, outputs)):
+            for name, t in tensors.items():
+                nb = t.numel() * t.element_size()
+                o = offs[name]
+                self.dev[name] = dbuf[o:o + nb].view(t.dtype).view(t.shape)
+                self.host[name] = hbuf[o:o + nb].view(t.dtype).view(t.shape)
+                self.dev[name].copy_(t)
+                self.host[name].copy_(t.cpu())
+        self.h2d_bytes = n_in
+        self.d2h_bytes = n_out
+
+    def upload(self):
+        self.dev_in.copy_(self.host_in, non_blocking=True)
+
+    def download(self):
+        self.host_out.copy_(self.dev_out, non_blocking=True)
+
+
 class DecodeBatch:
     def __init__(self, *, q, k_pages, v_pages, page_table, seq_len, prompt_len, window,
                  grid_w, keep_mask, max_window, mask_words, max_kept, device="cuda"):
@@ -30,6 +92,8 @@ class DecodeBatch:
         self.prompt_len = _i32(prompt_len, self.device)
         self.window = _i32(window, self.device)
         self.grid_w = _i32(grid_w, self.device)
+        self._host_lengths = tuple(np.array(x, dtype=np.int32, copy=True)
+                                   for x in (seq_len, prompt_len, window))
         B, Hq, D = self.q.shape
         num_pages, page, Hkv, _ = self.k_pages.shape
         self.batch, self.hq, self.hkv, self.head_dim = B, Hq, Hkv, D
@@ -72,13 +136,40 @@ class DecodeBatch:
                               self.ws, stream)
         return out, lse
 
-    def decode_sparse_masked(self, out=None, lse=None, stream=None):
+    def decode_sparse_masked(self, out=None, lse=None, stream=None, request_order=None):
         out = self.out if out is None else out
         lse = self.lse if lse is None else lse
         dsa.dsa_decode_sparse_masked(self.dims, self.q, self.k_pages, self.v_pages,
                                      self.page_table, self.seq_len, self.prompt_len, self.window,
-                                     self.keep_mask, self.scale, out, lse, self.ws, stream)
+                                     self.keep_mask, self.scale, out, lse, self.ws, stream,
+                                     request_order)
         return out, lse
+
+    def longest_first_order(self):
+        """Requests by decreasing estimated kept rows: the request_order that
+        shortens the tail of a mixed batch (host-side; the serving host knows
+        these lengths when it builds the batch)."""
+        return longest_first_order(self._host_lengths)
+
+    def schedule_order(self):
+        """longest_first_order() when the batch's lengths vary, else None."""
+        return schedule_order(self._host_lengths)
+
+    def pack_io(self, order=None) -> PackedIO:
+        """Move the step's inputs (q, lengths, masks, page table, order) and
+        results (out, lse) into packed buffers; returns the PackedIO and the
+        device order tensor (or None)."""
+        inputs = {"q": self.q, "seq_len": self.seq_len, "prompt_len": self.prompt_len,
+                  "window": self.window, "keep_mask": self.keep_mask,
+                  "page_table": self.page_table}
+        if order is not None:
+            inputs["order"] = torch.as_tensor(np.asarray(order, dtype=np.int32))
+        io = PackedIO(inputs, {"out": self.out, "lse": self.lse}, self.device)
+        self.q, self.seq_len, self.prompt_len = io.dev["q"], io.dev["seq_len"], io.dev["prompt_len"]
+        self.window, self.keep_mask = io.dev["window"], io.dev["keep_mask"]
+        self.page_table = io.dev["page_table"]
+        self.out, self.lse = io.dev["out"], io.dev["lse"]
+        return io, io.dev.get("order")
 
     def decode_dense(self, out=None, lse=None, stream=None):
         out = self.out if out is None else out

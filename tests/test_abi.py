@@ -86,11 +86,11 @@ def test_null_pointers_rejected_before_launch():
     assert lib.dsa_decode_dense(D, fake, fake, fake, fake, fake, 0.1, fake, None,
                                 ctypes.c_void_p((1 << 20) + 8), None) == dsa.DSA_ERR_INVALID_ARG
     # masked decode: a missing keep mask, then a window too long for the in-kernel list
-    assert lib.dsa_decode_sparse_masked(D, fake, fake, fake, fake, fake, fake, fake, None, 0.1,
-                                        fake, None, fake, None) == dsa.DSA_ERR_INVALID_ARG
+    assert lib.dsa_decode_sparse_masked(D, fake, fake, fake, fake, fake, fake, fake, None, None,
+                                        0.1, fake, None, fake, None) == dsa.DSA_ERR_INVALID_ARG
     big = dsa.make_dims(2, 8, 4, 128, 10, 4, 1025, 33, 50, "bf16", "bf16")
     assert lib.dsa_decode_sparse_masked(ctypes.byref(big), fake, fake, fake, fake, fake, fake,
-                                        fake, fake, 0.1, fake, None, fake, None) == \
+                                        fake, fake, None, 0.1, fake, None, fake, None) == \
         dsa.DSA_ERR_UNSUPPORTED
     assert lib.dsa_decode_plan(ctypes.byref(d), 3, None, None, None) == dsa.DSA_ERR_INVALID_ARG
     code = ctypes.c_int32(0)

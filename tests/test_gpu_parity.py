@@ -96,9 +96,17 @@ def run_both(w, mask=None, bh=None):
         l = lse.cpu().numpy().reshape(-1)
         if mode == "sparse":
             listed = o.copy(), l.copy()
-        elif mode == "masked" and same_plan(bt):
-            # same kept set, same order, same chunks: the same bits
-            assert np.array_equal(o, listed[0]) and np.array_equal(l, listed[1])
+        elif mode == "masked":
+            if same_plan(bt):
+                # same kept set, same order, same chunks: the same bits
+                assert np.array_equal(o, listed[0]) and np.array_equal(l, listed[1])
+            # the request order changes only the schedule
+            order = torch.as_tensor(bt.longest_first_order()[::-1].copy()).to(bt.device)
+            o2, l2 = bt.decode_sparse_masked(out=torch.empty_like(out),
+                                             lse=torch.empty_like(lse), request_order=order)
+            torch.cuda.synchronize()
+            assert bt.device_error() == 0
+            assert torch.equal(o2, out) and torch.equal(l2, lse)
         ref_o, ref_l = oracle.decode(inp, sparse=mode != "dense", bh=bh)
         if bh is not None:
             sel = [b * w["hq"] + h for b, h in bh]
@@ -280,6 +288,26 @@ def test_attention_mass_parity(cid, batch, r_local, r_diag):
     assert np.abs(om.cpu().numpy().reshape(ref_om.shape) - ref_om).max() <= MASS_MAX
 
 
+@pytest.mark.parametrize("D,G,dtype", [(64, 1, "bf16"), (64, 2, "bf16"), (64, 8, "bf16"),
+                                       (128, 2, "bf16"), (128, 8, "bf16"), (128, 4, "f32"),
+                                       (64, 4, "mixed")])
+def test_attention_mass_every_engine(D, G, dtype):
+    """Both score engines (tensor cores for bf16 q and K with G >= 2, CUDA
+    cores otherwise), several tiles per chunk and ragged tails."""
+    w = wl.generate(small_cfg(D, G, "f32" if dtype == "f32" else "bf16", batch=4, Lmax=1500,
+                              W=40, seed=30 + D + G))
+    if dtype == "mixed":
+        w["q"] = torch.randn(w["q"].shape, generator=torch.Generator().manual_seed(31))
+    bt = DecodeBatch.from_workload(w)
+    mass, om = bt.attention_mass(r_local=2, r_diag=1)
+    torch.cuda.synchronize()
+    assert bt.device_error() == 0
+    ref_m, ref_om = oracle.mass(w, r_local=2, r_diag=1)
+    m = mass.cpu().numpy().reshape(-1, 4)
+    assert np.abs(m - ref_m).max() <= MASS_MAX
+    assert np.abs(om.cpu().numpy().reshape(ref_om.shape) - ref_om).max() <= MASS_MAX
+
+
 # ---------------------------------------------------------------------------
 # invalid per-request data: flagged on the device, no fault
 # ---------------------------------------------------------------------------
@@ -336,6 +364,12 @@ def test_device_errors_are_flagged():
     assert bt.device_error() == 2
     assert torch.isnan(bt.out[0]).all()
     bt.prompt_len[0] = int(w["prompt_len"][0])
+    bt.ws.zero_()
+    # a request order entry outside the batch
+    bad = torch.tensor([0, 1, 2, 7], dtype=torch.int32, device=bt.device)
+    bt.decode_sparse_masked(request_order=bad)
+    torch.cuda.synchronize()
+    assert bt.device_error() == 9
     bt.ws.zero_()
     small = DecodeBatch.from_workload(dict(w, max_kept=2))
     small.decode_sparse_masked()
