@@ -67,6 +67,9 @@ def parse_args():
     p.add_argument("--profile", choices=["index", "sparse", "masked", "dense", "mass"],
                    help="no timing: run W + K eager launches of one call on one KV pool "
                         "(a small, self-contained case for ncu) and exit")
+    p.add_argument("--sparse-cluster", type=int, default=-1,
+                   help="CTAs per thread-block cluster of sparse decode (0: chosen per call, "
+                        "default: the library's setting)")
     p.add_argument("--batch", type=int, default=0,
                    help="with --profile: override the workload's batch size")
     return p.parse_args()
@@ -249,6 +252,8 @@ def to_cpu_workload(w, bt):
 
 
 def run_ours(args):
+    if args.sparse_cluster >= 0:
+        dsa.dsa_set_sparse_cluster(args.sparse_cluster)
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
@@ -449,6 +454,8 @@ def run_ours(args):
                     "(+ merge) in one call",
             "request_order": "longest first" if order is not None else "batch order",
             "decode_chunk_rows": chunk, "decode_chunks_max": nch,
+            "sparse_cluster": dsa.dsa_decode_plan(d, dsa.PLAN_MASKED)[1]
+            if dsa.dsa_decode_plan(d, dsa.PLAN_MASKED)[2] == 1 else 1,
         },
         "effective_kv_gbs": by["masked"] / step_s / 1e9,
         "pct_of_hbm_peak": 100.0 * by["masked"] / step_s / 1e9 / peak,
@@ -557,6 +564,8 @@ def run_reference(args):
 def run_profile(args):
     """W + K eager launches of one library call on one KV pool, for a profiler
     to capture (launch j of the call is the j-th launch of its kernel)."""
+    if args.sparse_cluster >= 0:
+        dsa.dsa_set_sparse_cluster(args.sparse_cluster)
     device = torch.device("cuda", 0)
     cfg = wl.CONFIGS[args.config]
     if args.batch > 0:

@@ -274,6 +274,25 @@ dsa_status dsa_decode_sparse_noalloc(const dsa_dims* dims, const void* q, const 
                                      float* lse, int32_t* dev_error, void* stream);
 
 /*
+ * dsa_set_sparse_cluster -- process-wide tuning of dsa_decode_sparse and
+ * dsa_decode_sparse_masked (not in the paper: a scheduling choice).  With
+ * ctas >= 2, the rows of each (request, kv head) are split evenly over `ctas`
+ * CTAs launched as one thread-block cluster, which combine their partial
+ * softmax states through distributed shared memory (no merge launch, no
+ * partials in device memory); with 1, a (request, kv head) whose kept rows fit
+ * one chunk runs in one CTA and longer ones are split into chunks merged by a
+ * second kernel; with 0 (the default) each call picks: clusters of 2, 4 or 8
+ * only when the batch has too few (request, kv head) pairs to fill half of the
+ * GPU's resident CTA slots, else 1.  Results equal the oracle's within the same
+ * bounds either way, but the floating-point summation order depends on the
+ * split.  ctas in 0..8, else DSA_ERR_INVALID_ARG.  Takes effect for calls
+ * issued afterwards; not synchronised with calls in flight on other host
+ * threads.  dsa_get_sparse_cluster returns the current value.
+ */
+dsa_status dsa_set_sparse_cluster(int32_t ctas);
+int32_t dsa_get_sparse_cluster(void);
+
+/*
  * Waits for `stream`, then reads the workspace error word into *code_out (one of
  * DSA_DEV_*).  Returns DSA_OK when the word is 0, DSA_ERR_TIMEOUT when it is
  * DSA_DEV_TIMEOUT, DSA_ERR_DEVICE for any other code, DSA_ERR_CUDA if the copy

@@ -153,6 +153,8 @@ __global__ void __launch_bounds__(DecodeTiling<D, KV, G, QMIX && G >= 2>::NW * 3
   constexpr int EPL = Tl::kEPL, NV = Tl::kNV, VE = Tl::kVE, RPL = Tl::kRPL;
   constexpr int kRowBytes = Tl::kRowBytes;
   extern __shared__ __align__(128) unsigned char smem[];
+  static_assert(kMaxCluster * G * (D + 2) * 4 <= Tl::NW * Tl::kWarpBytes,
+                "cluster merge buffer must fit the staging rings");
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int c = blockIdx.x, hk = blockIdx.y;
@@ -210,10 +212,22 @@ __global__ void __launch_bounds__(DecodeTiling<D, KV, G, QMIX && G >= 2>::NW * 3
     }
     return;
   }
-  const int row0 = c * a.chunk;
-  if (row0 >= n) return;
-  const int row1 = min(n, row0 + a.chunk);
-  const int nchunks = (n + a.chunk - 1) / a.chunk;
+  // Rows of this CTA.  Cluster mode: the a.cluster CTAs of a cluster split the
+  // unit's rows evenly (tile-aligned) and every one of them reaches the cluster
+  // merge, rows or not.  Otherwise: fixed chunks, partials merged by merge_kernel.
+  const int ncl = a.cluster;
+  int row0, row1, nchunks;
+  if (ncl > 1) {
+    const int per = ((n + ncl - 1) / ncl + T - 1) / T * T;
+    row0 = min(n, c * per);
+    row1 = min(n, row0 + per);
+    nchunks = 1;
+  } else {
+    row0 = c * a.chunk;
+    if (row0 >= n) return;
+    row1 = min(n, row0 + a.chunk);
+    nchunks = (n + a.chunk - 1) / a.chunk;
+  }
   const int ntiles = (row1 - row0 + T - 1) / T;
 
   constexpr int kRowStride = Tl::kRowStride;
@@ -624,29 +638,89 @@ __global__ void __launch_bounds__(DecodeTiling<D, KV, G, QMIX && G >= 2>::NW * 3
   }
   }  // CUDA-core path
   __syncthreads();
-  for (int x = threadIdx.x; x < G * D; x += NW * 32) {
-    const int h = x / D, d = x % D;
-    float mstar = -INFINITY;
+  // CTA merge of the warps' states: item k of this thread is x = tid + k*NW*32
+  constexpr int kItems = (G * D + NW * 32 - 1) / (NW * 32);
+  float it_o[kItems], it_m[kItems], it_l[kItems];
 #pragma unroll
-    for (int w = 0; w < NW; ++w) mstar = fmaxf(mstar, mslot(w)[h * (D + 2) + D]);
-    float o = 0.f, ls = 0.f;
+  for (int k = 0; k < kItems; ++k) {
+    const int x = threadIdx.x + k * NW * 32;
+    it_o[k] = 0.f;
+    it_m[k] = -INFINITY;
+    it_l[k] = 0.f;
+    if (x < G * D) {
+      const int h = x / D, d = x % D;
+      float mstar = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < NW; ++w) {
-      const float* src = mslot(w) + h * (D + 2);
-      const float sc = src[D] == -INFINITY ? 0.f : exp2f(src[D] - mstar);
-      o = fmaf(sc, src[d], o);
-      ls = fmaf(sc, src[D + 1], ls);
+      for (int w = 0; w < NW; ++w) mstar = fmaxf(mstar, mslot(w)[h * (D + 2) + D]);
+#pragma unroll
+      for (int w = 0; w < NW; ++w) {
+        const float* src = mslot(w) + h * (D + 2);
+        const float sc = src[D] == -INFINITY ? 0.f : exp2f(src[D] - mstar);
+        it_o[k] = fmaf(sc, src[d], it_o[k]);
+        it_l[k] = fmaf(sc, src[D + 1], it_l[k]);
+      }
+      it_m[k] = mstar;
     }
-    const size_t qh = static_cast<size_t>(b) * a.hq + hk * G + h;
-    if (nchunks == 1) {
-      a.out[qh * D + d] = o / ls;
-      if (a.lse != nullptr && d == 0) a.lse[qh] = (mstar + log2f(ls)) * kLn2;
-    } else {
-      float* pp = a.part + (qh * a.num_chunks + c) * (D + 2);
-      pp[d] = o;
-      if (d == 0) {
-        pp[D] = mstar;
-        pp[D + 1] = ls;
+  }
+  if (ncl > 1) {
+    // Cluster merge through distributed shared memory: once every CTA of the
+    // cluster is past its own reads of shared memory, each writes its state
+    // into slot `rank` of rank 0's buffer [ncl][G][D+2]; rank 0 combines them.
+    const uint32_t rank = cluster_ctarank();
+    float* recv = reinterpret_cast<float*>(smem);
+    cluster_sync();
+#pragma unroll
+    for (int k = 0; k < kItems; ++k) {
+      const int x = threadIdx.x + k * NW * 32;
+      if (x < G * D) {
+        const int h = x / D, d = x % D;
+        float* slot = recv + (rank * G + h) * (D + 2);
+        st_cluster_f32(map_cluster_rank(slot + d, 0), it_o[k]);
+        if (d == 0) {
+          st_cluster_f32(map_cluster_rank(slot + D, 0), it_m[k]);
+          st_cluster_f32(map_cluster_rank(slot + D + 1, 0), it_l[k]);
+        }
+      }
+    }
+    cluster_sync();
+    if (rank != 0) return;
+#pragma unroll
+    for (int k = 0; k < kItems; ++k) {
+      const int x = threadIdx.x + k * NW * 32;
+      if (x < G * D) {
+        const int h = x / D, d = x % D;
+        float mstar = -INFINITY;
+        for (int r = 0; r < ncl; ++r) mstar = fmaxf(mstar, recv[(r * G + h) * (D + 2) + D]);
+        float o = 0.f, ls = 0.f;
+        for (int r = 0; r < ncl; ++r) {
+          const float* src = recv + (r * G + h) * (D + 2);
+          const float sc = src[D] == -INFINITY ? 0.f : exp2f(src[D] - mstar);
+          o = fmaf(sc, src[d], o);
+          ls = fmaf(sc, src[D + 1], ls);
+        }
+        const size_t qh = static_cast<size_t>(b) * a.hq + hk * G + h;
+        a.out[qh * D + d] = o / ls;
+        if (a.lse != nullptr && d == 0) a.lse[qh] = (mstar + log2f(ls)) * kLn2;
+      }
+    }
+    return;
+  }
+#pragma unroll
+  for (int k = 0; k < kItems; ++k) {
+    const int x = threadIdx.x + k * NW * 32;
+    if (x < G * D) {
+      const int h = x / D, d = x % D;
+      const size_t qh = static_cast<size_t>(b) * a.hq + hk * G + h;
+      if (nchunks == 1) {
+        a.out[qh * D + d] = it_o[k] / it_l[k];
+        if (a.lse != nullptr && d == 0) a.lse[qh] = (it_m[k] + log2f(it_l[k])) * kLn2;
+      } else {
+        float* pp = a.part + (qh * a.num_chunks + c) * (D + 2);
+        pp[d] = it_o[k];
+        if (d == 0) {
+          pp[D] = it_m[k];
+          pp[D + 1] = it_l[k];
+        }
       }
     }
   }
@@ -702,7 +776,24 @@ cudaError_t launch_decode_one(const DecodeLaunch& a, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const dim3 grid(a.num_chunks, a.hkv, a.batch);
-  kern<<<grid, DecodeTiling<D, KV, G, QMIX && G >= 2>::NW * 32, smem, s>>>(a);
+  const dim3 block(DecodeTiling<D, KV, G, QMIX && G >= 2>::NW * 32);
+  if (a.cluster > 1) {
+    // the CTAs of one (request, kv head) form one cluster along x
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(a.cluster);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a);
+  }
+  kern<<<grid, block, smem, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -1,6 +1,7 @@
 // dsa_api.cu -- the extern "C" entry points of libdsa (declared in dsa.h):
 // host-side validation, work-chunk sizing, and kernel dispatch.  Nothing here
 // computes attention; every step of the path runs in the kernels.
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <mutex>
@@ -24,11 +25,20 @@
 #ifndef DSA_MASS_WAVES
 #define DSA_MASS_WAVES 16
 #endif
+// CTAs that share one (request, kv head) of sparse decode as a thread-block
+// cluster, merging through distributed shared memory (1: no cluster, 0: chosen
+// per call by sparse_cluster_auto()).
+#ifndef DSA_SPARSE_CLUSTER
+#define DSA_SPARSE_CLUSTER 0
+#endif
 
 namespace dsa {
 namespace {
 
 constexpr int kMaxDevices = 64;
+
+// Process-wide: CTAs per cluster of sparse decode (dsa_set_sparse_cluster).
+std::atomic<int> g_sparse_cluster{DSA_SPARSE_CLUSTER};
 
 bool dims_valid(const dsa_dims* d) {
   if (d == nullptr) return false;
@@ -130,8 +140,19 @@ int32_t* unit_rows(const dsa_dims* d, void* ws) {
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 struct Plan {
-  int chunk, num_chunks, quantum, per_sm;
+  int chunk, num_chunks, quantum, per_sm, cluster;
 };
+
+// Automatic cluster size: a CTA's fixed latency (first copies, end-of-CTA
+// merge) makes short CTAs slow, so split units over clusters only when there
+// are too few of them to occupy the GPU -- the largest size in {2, 4, 8} whose
+// CTAs still fit in half of the resident slots, else 1.
+int sparse_cluster_auto(int64_t units, int64_t slots) {
+  int best = 1;
+  for (int c = 2; c <= kMaxCluster; c *= 2)
+    if (units * c <= slots / 2) best = c;
+  return best;
+}
 
 Plan decode_plan(const dsa_dims* d, int mode) {
   const bool kv_bf16 = d->kv_dtype == DSA_BF16;
@@ -142,6 +163,17 @@ Plan decode_plan(const dsa_dims* d, int mode) {
                       : decode_rows_per_pass_f32(d->head_dim, g);
   p.per_sm = kv_bf16 ? decode_ctas_per_sm_bf16(d->head_dim, g, mode)
                      : decode_ctas_per_sm_f32(d->head_dim, g, mode);
+  p.cluster = 1;
+  const int64_t units = static_cast<int64_t>(d->batch) * d->hkv;
+  int ncl = g_sparse_cluster.load(std::memory_order_relaxed);
+  if (ncl == 0) ncl = sparse_cluster_auto(units, sm_count() * p.per_sm);
+  if (mode != kModeDense && ncl > 1 && ncl <= kMaxCluster && n_max > p.quantum) {
+    // the rows of a unit split evenly over a cluster of ncl CTAs
+    p.cluster = ncl;
+    p.num_chunks = ncl;
+    p.chunk = static_cast<int>(ceil_div(n_max, ncl));
+    return p;
+  }
   choose_chunks(n_max, static_cast<int64_t>(d->batch) * d->hkv, sm_count() * p.per_sm, p.quantum,
                 mode == kModeDense ? DSA_DENSE_WAVES : DSA_SPARSE_WAVES, &p.chunk,
                 &p.num_chunks);
@@ -201,6 +233,7 @@ dsa_status decode_common(const dsa_dims* d, int mode, const void* q, const void*
   a.max_kept = d->max_kept;
   a.chunk = plan.chunk;
   a.num_chunks = plan.num_chunks;
+  a.cluster = plan.cluster;
   a.scale_log2 = scale * kLog2e;
   a.out = out;
   a.lse = lse;
@@ -209,6 +242,7 @@ dsa_status decode_common(const dsa_dims* d, int mode, const void* q, const void*
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = kv_bf16 ? launch_decode_bf16(a, mode, s) : launch_decode_f32(a, mode, s);
   if (e != cudaSuccess) return DSA_ERR_CUDA;
+  if (a.cluster > 1) return DSA_OK;  // merged inside the clusters
   return from_cuda(launch_merge(a, mode, s));
 }
 
@@ -358,9 +392,18 @@ dsa_status dsa_decode_plan(const dsa_dims* dims, int32_t mode, int32_t* chunk,
   const Plan p = decode_plan(dims, mode);
   if (chunk) *chunk = p.chunk;
   if (num_chunks) *num_chunks = p.num_chunks;
-  if (launches) *launches = dims->batch == 0 ? 0 : (p.num_chunks > 1 ? 2 : 1);
+  if (launches)
+    *launches = dims->batch == 0 ? 0 : (p.num_chunks > 1 && p.cluster <= 1 ? 2 : 1);
   return DSA_OK;
 }
+
+dsa_status dsa_set_sparse_cluster(int32_t ctas) {
+  if (ctas < 0 || ctas > kMaxCluster) return DSA_ERR_INVALID_ARG;
+  g_sparse_cluster.store(ctas, std::memory_order_relaxed);
+  return DSA_OK;
+}
+
+int32_t dsa_get_sparse_cluster(void) { return g_sparse_cluster.load(std::memory_order_relaxed); }
 
 dsa_status dsa_get_device_error(const void* ws, void* stream, int32_t* code_out) {
   if (!ws || !code_out) return DSA_ERR_INVALID_ARG;

@@ -11,6 +11,8 @@ namespace dsa {
 // Rows of one decode / mass work unit are split into chunks of `chunk` rows;
 // each chunk is one CTA.  At most kMaxChunks chunks per (request, kv head).
 constexpr int kMaxChunks = 32;
+// Largest cluster of decode CTAs sharing one (request, kv head).
+constexpr int kMaxCluster = 8;
 constexpr int kChunkQuantum = 64;  // chunk sizes are multiples of this
 
 struct DecodeLaunch {
@@ -30,6 +32,7 @@ struct DecodeLaunch {
   int32_t batch, hq, hkv, head_dim, max_pages, num_pages, max_kept;
   int32_t max_window, mask_words;  // kRowsMask only
   int32_t chunk, num_chunks;
+  int32_t cluster;   // > 1: the num_chunks (== cluster) CTAs of a unit merge in a cluster
   float scale_log2;  // softmax scale * log2(e)
   float* out;
   float* lse;

@@ -71,6 +71,8 @@ def _load():
         "dsa_decode_plan": ([D, I32, ctypes.POINTER(I32), ctypes.POINTER(I32),
                              ctypes.POINTER(I32)], I32),
         "dsa_decode_sparse_noalloc": ([D, P, P, P, P, P, P, P, F32, P, P, P, P], I32),
+        "dsa_set_sparse_cluster": ([I32], I32),
+        "dsa_get_sparse_cluster": ([], I32),
         "dsa_get_device_error": ([P, P, ctypes.POINTER(I32)], I32),
         "dsa_clear_device_error": ([P, P], I32),
     }
@@ -227,6 +229,16 @@ def dsa_decode_plan(dims, mode: int):
     _check(_load().dsa_decode_plan(ctypes.byref(dims), int(mode), ctypes.byref(c),
                                    ctypes.byref(n), ctypes.byref(l)), "dsa_decode_plan")
     return c.value, n.value, l.value
+
+
+def dsa_set_sparse_cluster(ctas: int) -> None:
+    """CTAs per (request, kv head) cluster of sparse decode (1 = no cluster,
+    0 = chosen per call from the batch size)."""
+    _check(_load().dsa_set_sparse_cluster(int(ctas)), "dsa_set_sparse_cluster")
+
+
+def dsa_get_sparse_cluster() -> int:
+    return int(_load().dsa_get_sparse_cluster())
 
 
 def dsa_get_device_error(ws, stream=None) -> int:

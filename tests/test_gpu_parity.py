@@ -113,6 +113,26 @@ def run_both(w, mask=None, bh=None):
             o, l = o[sel], l[sel]
         assert_outputs(o, ref_o, fp32)
         assert np.abs(l - ref_l).max() <= LSE_MAX
+        if mode == "sparse":
+            ref_sparse = ref_o, ref_l
+    # sparse decode split over thread-block clusters (merged in shared memory)
+    saved = dsa.dsa_get_sparse_cluster()
+    try:
+        for ctas in (2, 4):
+            dsa.dsa_set_sparse_cluster(ctas)
+            o1, l1 = [t.clone() for t in bt.decode_sparse()]
+            o2, l2 = bt.decode_sparse_masked()
+            torch.cuda.synchronize()
+            assert bt.device_error() == 0
+            assert torch.equal(o1, o2) and torch.equal(l1, l2)   # same rows, same split
+            o = o2.cpu().numpy().reshape(-1, w["head_dim"])
+            l = l2.cpu().numpy().reshape(-1)
+            if bh is not None:
+                o, l = o[sel], l[sel]
+            assert_outputs(o, ref_sparse[0], fp32)
+            assert np.abs(l - ref_sparse[1]).max() <= LSE_MAX
+    finally:
+        dsa.dsa_set_sparse_cluster(saved)
     return bt
 
 
