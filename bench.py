@@ -27,6 +27,8 @@ from __future__ import annotations
 
 import argparse
 import csv
+import glob
+import hashlib
 import io
 import json
 import math
@@ -50,6 +52,39 @@ from kv_cache_serving_gb300.session import DecodeBatch  # noqa: E402
 
 METRIC = "sparse decode-attn tokens/s and effective KV GB/s (% of GB300 HBM peak)"
 FALLBACK_HBM_GBS = 6800.0
+
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the
+# step's decode kernel, per workload, from one ncu capture of
+# `bench.py --config C --profile masked --warmup 2 --steps 1` (the same launch
+# on the same batch; the summaries are under profiles/).  They describe the
+# kernel sources whose digest is `digest` and are reported as null otherwise.
+NCU_TRAFFIC = {
+    "digest": "be994dc902120793",
+    "bytes": {
+        "llamagen-xl-like-24x24": 21430272,
+        "janus-pro-7b-like-32x32": 316717056,
+        "emu3-8b-like-90x90-gqa4": 3282688,
+        "mixed-serving-gqa4": 168441344,
+    },
+}
+
+
+def kernel_digest() -> str:
+    """sha256 over the kernel sources (csrc/ and the public header)."""
+    h = hashlib.sha256()
+    files = sorted(glob.glob(os.path.join(ROOT, "kv_cache_serving_gb300", "csrc", "*")))
+    files.append(os.path.join(ROOT, "include", "dsa.h"))
+    for f in files:
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str):
+    if kernel_digest() != NCU_TRAFFIC["digest"]:
+        return None
+    return NCU_TRAFFIC["bytes"].get(workload)
 
 
 def parse_args():
@@ -465,7 +500,9 @@ def run_ours(args):
             "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
             "frac": achieved / peak, "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
             if peak_src == "measured" else "fallback 6.8 TB/s",
-            "traffic": None,
+            "traffic": ncu_traffic(cfg.name),
+            "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum, one launch of "
+                              "this kernel on this workload (null once the kernel changed)",
             "bytes_per_launch": by["masked"], "launch_us": 1e6 * step_s,
         },
         "two_call_step": {
