@@ -121,6 +121,21 @@ def dist_env():
     return rank, world, local
 
 
+def rank_seed(cfg, rank: int) -> int:
+    """Each rank draws its own batch (weak scaling: the per-GPU work is fixed)."""
+    return cfg.seed + 1000 * rank
+
+
+def max_over_ranks(values, device):
+    """Element-wise max of a list of floats over all ranks (the job's time is
+    its slowest rank's); identity without a process group."""
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return list(values)
+    t = torch.tensor(list(values), device=device, dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return t.tolist()
+
+
 def hbm_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -295,7 +310,7 @@ def run_ours(args):
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=device)
     cfg = wl.CONFIGS[args.config]
-    w = wl.generate(cfg, seed=cfg.seed + 1000 * rank, device=str(device))
+    w = wl.generate(cfg, seed=rank_seed(cfg, rank), device=str(device))
     bt = DecodeBatch.from_workload(w, device=device)
     torch.cuda.synchronize()
     # one non-default stream for everything (graph capture needs one)
@@ -404,10 +419,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     bt.check("timed region")
 
-    if world > 1:
-        t = torch.tensor([t_step, t_two, t_dec, t_dense], device=device, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        t_step, t_two, t_dec, t_dense = t.tolist()
+    t_step, t_two, t_dec, t_dense = max_over_ranks([t_step, t_two, t_dec, t_dense], device)
 
     # end-to-end through the API with host buffers: inputs H2D, result D2H, every step
     h2d, d2h = io.h2d_bytes, io.d2h_bytes
@@ -430,10 +442,7 @@ def run_ours(args):
     e1.record(stream)
     e1.synchronize()
     t_e2e = e0.elapsed_time(e1) / 1e3
-    if world > 1:
-        t = torch.tensor([t_e2e], device=device, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        t_e2e = t.item()
+    (t_e2e,) = max_over_ranks([t_e2e], device)
 
     # attention-mass pass (the characterisation kernel), timed alone
     if K > 0:
