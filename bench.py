@@ -7,8 +7,8 @@ from the keep mask (index compaction), gathers the kept K/V rows, runs the
 online softmax and PV, and (when rows are split) the LSE merge follows.  The
 same step as two calls, dsa_build_index (kept lists to HBM) + dsa_decode_sparse,
 and that decode alone are timed beside it.  Inputs are synthetic (seeded),
-shaped like the LlamaGen-XL-like workload by default (--config 2); other
-workloads: --config 3|4|5.  The dense causal decode of the same batch and the
+shaped like the LlamaGen-XL-like workload by default (--workload llamagen-xl);
+others: --workload janus-pro-7b | emu3-8b | mixed-serving.  The dense causal decode of the same batch and the
 attention-mass pass are timed beside it.
 
 Timing: W eager warm-up steps, then K steps captured in one CUDA graph and
@@ -17,7 +17,7 @@ rotate through R copies of the KV pool, R chosen so that the rows touched by R
 steps exceed 4x the L2, so every step streams its rows from HBM.  nvidia-smi
 samples clocks over a busy window that encloses the timed replay.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--config C]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
     python bench.py --impl reference ...   # the fp64 CPU oracle, timed
 Multi-GPU (torchrun): every rank runs its own batch (weak scaling, replicas
 only: the path has no exchange step); the timed region is bracketed by
@@ -55,7 +55,7 @@ FALLBACK_HBM_GBS = 6800.0
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the
 # step's decode kernel, per workload, from one ncu capture of
-# `bench.py --config C --profile masked --warmup 2 --steps 1` (the same launch
+# `bench.py --workload NAME --profile masked --warmup 2 --steps 1` (the same launch
 # on the same batch; the summaries are under profiles/).  They describe the
 # kernel sources whose digest is `digest` and are reported as null otherwise.
 NCU_TRAFFIC = {
@@ -92,7 +92,8 @@ def parse_args():
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=10)
-    p.add_argument("--config", type=int, default=2, choices=[2, 3, 4, 5])
+    p.add_argument("--workload", default="llamagen-xl",
+                   choices=["llamagen-xl", "janus-pro-7b", "emu3-8b", "mixed-serving"])
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="CPU time budget of the oracle baseline sample")
@@ -309,7 +310,7 @@ def run_ours(args):
     device = torch.device("cuda", local)
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=device)
-    cfg = wl.CONFIGS[args.config]
+    cfg = wl.WORKLOADS[args.workload]
     w = wl.generate(cfg, seed=rank_seed(cfg, rank), device=str(device))
     bt = DecodeBatch.from_workload(w, device=device)
     torch.cuda.synchronize()
@@ -563,7 +564,7 @@ def run_reference(args):
     if rank != 0:
         return
     import oracle
-    cfg = wl.CONFIGS[args.config]
+    cfg = wl.WORKLOADS[args.workload]
     w = wl.generate(cfg)
     if cfg.mask == "top_mass":
         # the same selection rule as the GPU arm, applied to the oracle's mass
@@ -613,7 +614,7 @@ def run_profile(args):
     if args.sparse_cluster >= 0:
         dsa.dsa_set_sparse_cluster(args.sparse_cluster)
     device = torch.device("cuda", 0)
-    cfg = wl.CONFIGS[args.config]
+    cfg = wl.WORKLOADS[args.workload]
     if args.batch > 0:
         cfg = wl.scaled(cfg, batch=args.batch)
     w = wl.generate(cfg, device=str(device))

@@ -5,7 +5,7 @@ attention arithmetic: it draws random tensors, lays them out in a paged KV
 pool, and encodes keep masks as bits.  The workloads stand in for the model
 runs behind "Understanding and Exploiting Diagonal Attention Sparsity in
 Autoregressive Image Generation" (LlamaGen, Janus-Pro and Emu3 shapes; the
-weights, prompts and image datasets are not available), see ``CONFIGS``.
+weights, prompts and image datasets are not available), see ``WORKLOADS``.
 
 Layouts (all row-major, all sizes in elements):
   q           [B, Hq, D]                    f32 or bf16
@@ -51,21 +51,21 @@ class Config:
     extra: dict = field(default_factory=dict)
 
 
-CONFIGS = {
+WORKLOADS = {
     # Tiny fp32 check: 16 prompt tokens, an 8x8 image decoded step by step.
-    1: Config("tiny-fp32-8x8", 1, 2, 2, 64, "f32", (16, 16), (8,), None, 16,
+    "tiny-fp32": Config("tiny-fp32-8x8", 1, 2, 2, 64, "f32", (16, 16), (8,), None, 16,
               ("abs", 17, 80), "offsets", band=2, row_ks=(1, 2), row_r=1, seed=1),
     # LlamaGen-XL-like: 24x24 grid, W = 2 rows.
-    2: Config("llamagen-xl-like-24x24", 32, 20, 20, 64, "bf16", (120, 120), (24,), 2, None,
+    "llamagen-xl": Config("llamagen-xl-like-24x24", 32, 20, 20, 64, "bf16", (120, 120), (24,), 2, None,
               ("after_prompt", 1, 576), "offsets", band=4, row_ks=(1, 2), row_r=1, seed=2),
     # Janus-Pro-7B-like: 32x32 grid, W = 3 rows, per-head random masks.
-    3: Config("janus-pro-7b-like-32x32", 64, 32, 32, 128, "bf16", (256, 256), (32,), 3, None,
+    "janus-pro-7b": Config("janus-pro-7b-like-32x32", 64, 32, 32, 128, "bf16", (256, 256), (32,), 3, None,
               ("after_prompt", 64, 1024), "random", band=8, seed=3),
     # Emu3-8B-like GQA: 90x90 grid plus one row-end token per row (w = 91), W = 360.
-    4: Config("emu3-8b-like-90x90-gqa4", 8, 32, 8, 128, "bf16", (64, 64), (91,), None, 360,
+    "emu3-8b": Config("emu3-8b-like-90x90-gqa4", 8, 32, 8, 128, "bf16", (64, 64), (91,), None, 360,
               ("abs", 8000, 8250), "offsets", band=16, row_ks=(1, 2, 3), row_r=2, seed=4),
     # Mixed serving batch, GQA, shuffled pages, masks from the top-mass rule.
-    5: Config("mixed-serving-gqa4", 128, 32, 8, 128, "bf16", (32, 512), (24, 32, 64), 3, None,
+    "mixed-serving": Config("mixed-serving-gqa4", 128, 32, 8, 128, "bf16", (32, 512), (24, 32, 64), 3, None,
               ("after_prompt", 1, 4096), "top_mass", band=8, seed=5),
 }
 

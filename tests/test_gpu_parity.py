@@ -172,7 +172,7 @@ def test_many_units_single_chunk_path():
 # ---------------------------------------------------------------------------
 
 def test_tiny_fp32_every_decode_step():
-    cfg = wl.scaled(wl.CONFIGS[1], seq=("abs", 80, 80))
+    cfg = wl.scaled(wl.WORKLOADS["tiny-fp32"], seq=("abs", 80, 80))
     w = wl.generate(cfg)
     golden = {}
     with open(os.path.join(os.path.dirname(__file__), "golden", "tiny_fp32_kept_sets.txt")) as f:
@@ -190,10 +190,10 @@ def test_tiny_fp32_every_decode_step():
             assert bt.kept_idx[0, 0, :n].cpu().tolist() == expand_ranges(golden[L])
 
 
-@pytest.mark.parametrize("cid", [2, 3, 4])
-def test_workload_reduced_batch(cid):
-    cfg = wl.CONFIGS[cid]
-    w = wl.generate(wl.scaled(cfg, batch=3 if cid == 4 else 6))
+@pytest.mark.parametrize("name", ["llamagen-xl", "janus-pro-7b", "emu3-8b"])
+def test_workload_reduced_batch(name):
+    cfg = wl.WORKLOADS[name]
+    w = wl.generate(wl.scaled(cfg, batch=3 if name == "emu3-8b" else 6))
     run_both(w)
 
 
@@ -205,18 +205,18 @@ def top_mass_masks_from_oracle(w):
 
 
 def test_mixed_serving_reduced_batch():
-    w = wl.generate(wl.scaled(wl.CONFIGS[5], batch=6))
+    w = wl.generate(wl.scaled(wl.WORKLOADS["mixed-serving"], batch=6))
     run_both(w, mask=top_mass_masks_from_oracle(w))
 
 
-@pytest.mark.parametrize("cid", [2, 3, 4, 5])
-def test_workload_full_size_sampled(cid):
+@pytest.mark.parametrize("name", ["llamagen-xl", "janus-pro-7b", "emu3-8b", "mixed-serving"])
+def test_workload_full_size_sampled(name):
     """Full-size batches in the launch configuration the benchmark uses; kept lists compared in full, outputs on 48 sampled (b, h) pairs."""
-    w = wl.generate(wl.CONFIGS[cid])
-    rng = np.random.default_rng(100 + cid)
+    w = wl.generate(wl.WORKLOADS[name])
+    rng = np.random.default_rng(100 + list(wl.WORKLOADS).index(name))
     bh = [(int(rng.integers(w["batch"])), int(rng.integers(w["hq"]))) for _ in range(48)]
     mask = None
-    if cid == 5:
+    if name == "mixed-serving":
         _, om = oracle.mass(w, bh=None, with_offsets=True)
         om = om.reshape(w["batch"], w["hq"], -1)
         mask = wl.top_mass_keep_mask(om, w["window"], w["hkv"], w["mask_words"])
@@ -228,7 +228,7 @@ def test_workload_full_size_sampled(cid):
 # ---------------------------------------------------------------------------
 
 def test_skipped_rows_are_never_read():
-    w = wl.generate(wl.scaled(wl.CONFIGS[3], batch=4), spare_pages=5)
+    w = wl.generate(wl.scaled(wl.WORKLOADS["janus-pro-7b"], batch=4), spare_pages=5)
     kept = oracle_kept(w)
     bt = DecodeBatch.from_workload(w)
     bt.build_index()
@@ -293,10 +293,12 @@ def test_large_window_many_mask_words():
 # attention mass
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("cid,batch,r_local,r_diag", [(2, 4, 2, 2), (4, 2, 1, 2), (5, 5, 2, 1),
-                                                      (1, 1, 2, 1)])
-def test_attention_mass_parity(cid, batch, r_local, r_diag):
-    w = wl.generate(wl.scaled(wl.CONFIGS[cid], batch=batch))
+@pytest.mark.parametrize("name,batch,r_local,r_diag", [("llamagen-xl", 4, 2, 2),
+                                                       ("emu3-8b", 2, 1, 2),
+                                                       ("mixed-serving", 5, 2, 1),
+                                                      ("tiny-fp32", 1, 2, 1)])
+def test_attention_mass_parity(name, batch, r_local, r_diag):
+    w = wl.generate(wl.scaled(wl.WORKLOADS[name], batch=batch))
     bt = DecodeBatch.from_workload(w)
     mass, om = bt.attention_mass(r_local=r_local, r_diag=r_diag)
     torch.cuda.synchronize()

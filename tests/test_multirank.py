@@ -32,7 +32,7 @@ def _worker(rank, world, port, out):
     try:
         r, wsz, local = bench.dist_env()
         times = bench.max_over_ranks([1.0 + rank, 10.0 - rank, 0.5 * rank], "cpu")
-        cfg = wl.CONFIGS[2]
+        cfg = wl.WORKLOADS["llamagen-xl"]
         w = wl.generate(cfg, seed=bench.rank_seed(cfg, r), with_kv=False)
         # every rank sees every rank's first sequence length (to compare batches)
         first = torch.tensor([float(w["seq_len"][0]), float(w["seq_len"].sum())])

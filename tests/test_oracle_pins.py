@@ -142,7 +142,7 @@ def test_kept_set_equals_causal_rows_of_literal_band():
 
 
 def test_kept_set_tiny_fp32_golden():
-    cfg = wl.CONFIGS[1]
+    cfg = wl.WORKLOADS["tiny-fp32"]
     P, W, w = cfg.prompt[0], cfg.window, cfg.grid_w[0]
     offs = wl.band_row_offsets(cfg.band, w, cfg.row_ks, cfg.row_r)
     bits = wl.offsets_to_bits(offs, W, 1)

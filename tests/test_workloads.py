@@ -13,15 +13,15 @@ def test_offset_bits_roundtrip():
 
 def test_config_masks_match_their_descriptions():
     # LlamaGen-XL-like: band 4 plus {24, 48} +- 1 inside W = 48 (49 dropped)
-    w2 = wl.generate(wl.scaled(wl.CONFIGS[2], batch=3), with_kv=False)
+    w2 = wl.generate(wl.scaled(wl.WORKLOADS["llamagen-xl"], batch=3), with_kv=False)
     assert wl.bits_to_offsets(w2["keep_mask"][0, 0]) == [1, 2, 3, 4, 23, 24, 25, 47, 48]
     # Emu3-like: band 16 plus 91k +- 2, k = 1..3, all inside W = 360
-    w4 = wl.generate(wl.scaled(wl.CONFIGS[4], batch=2), with_kv=False)
+    w4 = wl.generate(wl.scaled(wl.WORKLOADS["emu3-8b"], batch=2), with_kv=False)
     offs = wl.bits_to_offsets(w4["keep_mask"][1, 3])
     assert offs == list(range(1, 17)) + [89, 90, 91, 92, 93, 180, 181, 182, 183, 184,
                                          271, 272, 273, 274, 275]
     # Janus-like: band 8 always kept, 25-50% of the other offsets on average
-    w3 = wl.generate(wl.scaled(wl.CONFIGS[3], batch=8), with_kv=False)
+    w3 = wl.generate(wl.scaled(wl.WORKLOADS["janus-pro-7b"], batch=8), with_kv=False)
     fr = []
     for b in range(8):
         for hk in range(32):
@@ -31,9 +31,9 @@ def test_config_masks_match_their_descriptions():
     assert 0.25 < np.mean(fr) < 0.5
 
 
-@pytest.mark.parametrize("cid", [1, 2, 3, 4, 5])
-def test_generated_shapes_and_page_tables(cid):
-    cfg = wl.CONFIGS[cid]
+@pytest.mark.parametrize("name", list(wl.WORKLOADS))
+def test_generated_shapes_and_page_tables(name):
+    cfg = wl.WORKLOADS[name]
     w = wl.generate(wl.scaled(cfg, batch=min(cfg.batch, 6)), with_kv=False)
     L, P, W, t = w["seq_len"], w["prompt_len"], w["window"], w["page_table"]
     assert (L >= 1).all() and (P >= 0).all() and (W <= w["max_window"]).all()
@@ -44,15 +44,15 @@ def test_generated_shapes_and_page_tables(cid):
         used += list(t[b, :n])
     assert sorted(used) == list(range(w["num_pages"]))      # each page used once
     assert w["max_kept"] >= max(min(int(L[b]), int(P[b]) + int(W[b]) + 1) for b in range(len(L)))
-    if cid == 4:
+    if name == "emu3-8b":
         assert (L >= 8000).all() and (L <= 8250).all()
-    if cid == 5:
+    if name == "mixed-serving":
         assert set(np.unique(w["grid_w"])) <= {24, 32, 64} and (W == 3 * w["grid_w"]).all()
 
 
 def test_generation_is_seeded():
-    a = wl.generate(wl.scaled(wl.CONFIGS[2], batch=2))
-    b = wl.generate(wl.scaled(wl.CONFIGS[2], batch=2))
+    a = wl.generate(wl.scaled(wl.WORKLOADS["llamagen-xl"], batch=2))
+    b = wl.generate(wl.scaled(wl.WORKLOADS["llamagen-xl"], batch=2))
     assert np.array_equal(a["page_table"], b["page_table"])
     assert (a["k_pages"].float() == b["k_pages"].float()).all()
 

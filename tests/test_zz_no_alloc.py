@@ -34,11 +34,11 @@ def test_noalloc_rejects_batches_beyond_its_scratch():
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("cid,batch", [(3, 12), (5, 16)])
-def test_noalloc_matches_workspace_entry_point(cid, batch):
+@pytest.mark.parametrize("name,batch", [("janus-pro-7b", 12), ("mixed-serving", 16)])
+def test_noalloc_matches_workspace_entry_point(name, batch):
     from kv_cache_serving_gb300.session import DecodeBatch
     assert torch.cuda.is_available()
-    w = wl.generate(wl.scaled(wl.CONFIGS[cid], batch=batch))
+    w = wl.generate(wl.scaled(wl.WORKLOADS[name], batch=batch))
     mask = w["keep_mask"]
     if mask is None:   # mixed-serving masks: band plus a fixed pattern of offsets
         mask = np.zeros((w["batch"], w["hkv"], w["mask_words"]), np.uint32)
