@@ -67,6 +67,10 @@ struct DecodeTiling {
   static constexpr int kSmem = kPsOff + (MMA ? NW * 2 * 8 * T * 2 : 0);
   // a warp's end-of-CTA state [G][D+2] floats reuses the start of its own ring
   static_assert(G * (D + 2) * 4 <= kWarpBytes, "merge slot fits the ring");
+  // Largest cluster whose merge buffer [cluster][G][D+2] floats fits the rings.
+  static constexpr int kClusterFit = NW * kWarpBytes / (G * (D + 2) * 4);
+  static constexpr int kMaxClusterHere = kClusterFit >= 8 ? 8 : kClusterFit >= 4 ? 4
+                                         : kClusterFit >= 2 ? 2 : 1;
   static_assert(kStageBytes % 128 == 0, "stage alignment");
   static_assert(kEPL % kVE == 0 && kRowBytes % 128 == 0, "row vector layout");
   // Element of a row held in slot w of vector u by lane j of a row group.
@@ -153,8 +157,6 @@ __global__ void __launch_bounds__(DecodeTiling<D, KV, G, QMIX && G >= 2>::NW * 3
   constexpr int EPL = Tl::kEPL, NV = Tl::kNV, VE = Tl::kVE, RPL = Tl::kRPL;
   constexpr int kRowBytes = Tl::kRowBytes;
   extern __shared__ __align__(128) unsigned char smem[];
-  static_assert(kMaxCluster * G * (D + 2) * 4 <= Tl::NW * Tl::kWarpBytes,
-                "cluster merge buffer must fit the staging rings");
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int c = blockIdx.x, hk = blockIdx.y;
@@ -164,6 +166,21 @@ __global__ void __launch_bounds__(DecodeTiling<D, KV, G, QMIX && G >= 2>::NW * 3
     return;
   }
   const int L = a.seq_len[b];
+  // Page ids of this lane's rows in the warp's first S+1 tiles, loaded
+  // speculatively with the request's sizes (they need only b and the CTA's
+  // first row): a row that is its own kept index -- every dense row, and the
+  // prompt rows of a kept set -- then needs no dependent page-table load
+  // before its first copy.
+  constexpr bool kSpec = MODE != kRowsList;
+  const int spec_row0 = a.cluster > 1 ? (c == 0 ? 0 : -1) : c * a.chunk;
+  int spec_pg[Tl::S + 1];
+#pragma unroll
+  for (int t = 0; t <= Tl::S; ++t) {
+    const int r = spec_row0 + (warp + t * Tl::NW) * Tl::T + (lane & (Tl::T - 1));
+    spec_pg[t] = (kSpec && spec_row0 >= 0 && (r >> 4) < a.max_pages)
+                     ? __ldg(a.page_table + static_cast<size_t>(b) * a.max_pages + (r >> 4))
+                     : 0;
+  }
   // kRowsMask: the kept set is read straight from the keep mask.  Lane l holds
   // the bits of window offsets 32l+1 .. 32l+32 that lie in 1..omax (wbits) and
   // the inclusive prefix count of set bits over lanes 0..l (wincl).
@@ -389,7 +406,13 @@ __global__ void __launch_bounds__(DecodeTiling<D, KV, G, QMIX && G >= 2>::NW * 3
 #pragma unroll
   for (int t = 0; t < S + 2; ++t) jr[t] = load_j(t);
 #pragma unroll
-  for (int t = 0; t < S + 1; ++t) pr[t] = load_pg(t, jr[t]);
+  for (int t = 0; t < S + 1; ++t) {
+    const int rr = tile_r0(t) + my_r;
+    if (kSpec && row0 == spec_row0 && jr[t] == rr)
+      pr[t] = (t < my_tiles && my_r < tile_rows(t)) ? spec_pg[t] : 0;
+    else
+      pr[t] = load_pg(t, jr[t]);
+  }
 #pragma unroll
   for (int t = 0; t < S; ++t)
     if (t < my_tiles) issue(t, t, jr[t], pr[t]);
@@ -825,6 +848,24 @@ cudaError_t launch_decode_t(const DecodeLaunch& a, int mode, cudaStream_t s) {
     case kRowsMask: return launch_decode_dispatch<KV, kRowsMask>(a, s);
   }
   return cudaErrorInvalidValue;
+}
+
+template <typename KV>
+int decode_cluster_limit_t(int head_dim, int group) {
+#define DSA_CASE(DD, GG)                                                                   \
+  if (head_dim == DD && group == GG)                                                       \
+    return IsBf16<KV>::value && GG >= 2 ? DecodeTiling<DD, KV, GG, true>::kMaxClusterHere  \
+                                        : DecodeTiling<DD, KV, GG, false>::kMaxClusterHere;
+  DSA_CASE(64, 1)
+  DSA_CASE(64, 2)
+  DSA_CASE(64, 4)
+  DSA_CASE(64, 8)
+  DSA_CASE(128, 1)
+  DSA_CASE(128, 2)
+  DSA_CASE(128, 4)
+  DSA_CASE(128, 8)
+#undef DSA_CASE
+  return 1;
 }
 
 template <typename KV>

@@ -24,6 +24,10 @@ cudaError_t launch_merge(const DecodeLaunch& a, int mode, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+int decode_cluster_limit_f32(int head_dim, int group) {
+  return decode_cluster_limit_t<float>(head_dim, group);
+}
+
 int decode_rows_per_pass_f32(int head_dim, int group) {
   return decode_rows_per_pass_t<float>(head_dim, group);
 }

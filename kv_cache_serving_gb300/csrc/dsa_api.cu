@@ -167,7 +167,10 @@ Plan decode_plan(const dsa_dims* d, int mode) {
   const int64_t units = static_cast<int64_t>(d->batch) * d->hkv;
   int ncl = g_sparse_cluster.load(std::memory_order_relaxed);
   if (ncl == 0) ncl = sparse_cluster_auto(units, sm_count() * p.per_sm);
-  if (mode != kModeDense && ncl > 1 && ncl <= kMaxCluster && n_max > p.quantum) {
+  const int limit = kv_bf16 ? decode_cluster_limit_bf16(d->head_dim, g)
+                            : decode_cluster_limit_f32(d->head_dim, g);
+  while (ncl > limit) ncl /= 2;
+  if (mode != kModeDense && ncl > 1 && n_max > p.quantum) {
     // the rows of a unit split evenly over a cluster of ncl CTAs
     p.cluster = ncl;
     p.num_chunks = ncl;

@@ -90,6 +90,9 @@ int mass_rows_per_pass(int head_dim, int group, bool kv_bf16, bool q_bf16);
 int mass_ctas_per_sm(int head_dim, int group, bool kv_bf16, bool q_bf16);
 cudaError_t launch_compact(const CompactLaunch& a, cudaStream_t s);
 
+// Largest cluster of decode CTAs whose merge buffer fits the CTA's rings.
+int decode_cluster_limit_bf16(int head_dim, int group);
+int decode_cluster_limit_f32(int head_dim, int group);
 // Rows one pass of all warps of a decode CTA covers (warps x tile rows), for
 // the host's chunk choice.
 int decode_rows_per_pass_bf16(int head_dim, int group);
