@@ -388,8 +388,9 @@ def run_ours(args):
         dense_step(k)
     torch.cuda.synchronize()
     bt.check("warm-up")
-    same_plan = (dsa.dsa_decode_plan(d, dsa.PLAN_MASKED)[:2] ==
-                 dsa.dsa_decode_plan(d, dsa.PLAN_SPARSE)[:2])
+    plan_m = dsa.dsa_decode_plan(d, dsa.PLAN_MASKED)
+    plan_s = dsa.dsa_decode_plan(d, dsa.PLAN_SPARSE)
+    same_plan = (plan_m[0], plan_m[1], plan_m[3]) == (plan_s[0], plan_s[1], plan_s[3])
     same_bits = bool(torch.equal(bt.out, out_2) and torch.equal(bt.lse, lse_2))
 
     g_step = graph_of(step, K, stream)
@@ -466,8 +467,8 @@ def run_ours(args):
     step_s = t_step / K
     tokens = world * B / step_s
     peak, peak_src = hbm_peak()
-    chunk, nch, launches = dsa.dsa_decode_plan(d, dsa.PLAN_MASKED)
-    _, _, launches_two = dsa.dsa_decode_plan(d, dsa.PLAN_SPARSE)
+    chunk, nch, launches, warps = dsa.dsa_decode_plan(d, dsa.PLAN_MASKED)
+    launches_two = dsa.dsa_decode_plan(d, dsa.PLAN_SPARSE)[2]
     achieved = by["masked"] / step_s / 1e9
     kernel = "decode_kernel, kept set read from the keep mask (dsa_decode_sparse_masked)"
     if launches > 1:
@@ -499,8 +500,8 @@ def run_ours(args):
                     "(+ merge) in one call",
             "request_order": "longest first" if order is not None else "batch order",
             "decode_chunk_rows": chunk, "decode_chunks_max": nch,
-            "sparse_cluster": dsa.dsa_decode_plan(d, dsa.PLAN_MASKED)[1]
-            if dsa.dsa_decode_plan(d, dsa.PLAN_MASKED)[2] == 1 else 1,
+            "sparse_cluster": nch if launches == 1 else 1,
+            "warps_per_cta": warps,
         },
         "effective_kv_gbs": by["masked"] / step_s / 1e9,
         "pct_of_hbm_peak": 100.0 * by["masked"] / step_s / 1e9 / peak,

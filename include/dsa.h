@@ -160,7 +160,7 @@ dsa_status dsa_decode_sparse(const dsa_dims* dims, const void* q, const void* k_
  * the kept set K(b,hk) of its (request, kv head) straight from prompt_len,
  * window and keep_mask (the same set, in the same ascending order, that
  * dsa_build_index writes; same definition as there) and attends over it.  When
- * dsa_decode_plan gives modes 1 and 2 the same chunk, out and lse equal those
+ * dsa_decode_plan gives modes 1 and 2 the same plan, out and lse equal those
  * of the two-call path bit for bit.
  *   q, k_pages, v_pages, page_table, seq_len, scale, out, lse  as in
  *                     dsa_decode_sparse
@@ -225,13 +225,14 @@ dsa_status dsa_attention_mass(const dsa_dims* dims, const void* q, const void* k
 /*
  * dsa_decode_plan -- how a decode call will split its work on the CURRENT
  * device: rows per CTA (*chunk), CTAs per (request, kv head) at most
- * (*num_chunks), and kernel launches per call (*launches).  mode selects the
- * call: 0 dsa_decode_dense, 1 dsa_decode_sparse, 2 dsa_decode_sparse_masked
- * (other values: DSA_ERR_INVALID_ARG).  Host-only; any output pointer may be
- * NULL.
+ * (*num_chunks), kernel launches per call (*launches) and warps per CTA
+ * (*warps).  mode selects the call: 0 dsa_decode_dense, 1 dsa_decode_sparse,
+ * 2 dsa_decode_sparse_masked (other values: DSA_ERR_INVALID_ARG).  Two calls
+ * with the same plan sum in the same order.  Host-only; any output pointer may
+ * be NULL.
  */
 dsa_status dsa_decode_plan(const dsa_dims* dims, int32_t mode, int32_t* chunk,
-                           int32_t* num_chunks, int32_t* launches);
+                           int32_t* num_chunks, int32_t* launches, int32_t* warps);
 
 /*
  * dsa_decode_sparse_noalloc -- dsa_decode_sparse for callers that cannot

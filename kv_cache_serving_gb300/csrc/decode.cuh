@@ -36,7 +36,16 @@
 
 namespace dsa {
 
-// Build-time tuning knobs: stages per warp and warps per CTA.
+// Build-time tuning knobs: stages per warp, warps per CTA (DSA_DECODE_WARPS_BIG:
+// the fused call on batches of more than two waves of units), bytes of K+V per
+// stage.
+#ifndef DSA_DECODE_WARPS_BIG
+#define DSA_DECODE_WARPS_BIG 3
+#endif
+static_assert(DSA_DECODE_WARPS_BIG == dsa::kDecodeWarpsBig, "host and device agree on the big build");
+#ifndef DSA_DECODE_STAGE_BYTES
+#define DSA_DECODE_STAGE_BYTES 8192
+#endif
 #ifndef DSA_DECODE_STAGES
 #define DSA_DECODE_STAGES 2
 #endif
@@ -44,14 +53,14 @@ namespace dsa {
 #define DSA_DECODE_WARPS 4
 #endif
 
-template <int D, typename KV, int G, bool MMA = false>
+template <int D, typename KV, int G, bool MMA = false, int NWARPS = DSA_DECODE_WARPS>
 struct DecodeTiling {
   static constexpr int kElt = static_cast<int>(sizeof(KV));
   static constexpr int kRowBytes = D * kElt;
-  static constexpr int kT0 = 8192 / (2 * kRowBytes);  // K+V of one stage = 8 KB
+  static constexpr int kT0 = DSA_DECODE_STAGE_BYTES / (2 * kRowBytes);  // K+V of one stage
   static constexpr int T = kT0 > 32 ? 32 : (kT0 < 8 ? 8 : kT0);
   static constexpr int S = DSA_DECODE_STAGES;  // stages per warp
-  static constexpr int NW = DSA_DECODE_WARPS;  // warps per CTA
+  static constexpr int NW = NWARPS;            // warps per CTA
   static constexpr int kVE = 16 / kElt;        // elements per 16-byte vector
   static constexpr int kEPL = D / 8;           // elements of a row per lane
   static constexpr int kNV = kEPL / kVE;       // 16-byte vectors of a row per lane
@@ -72,6 +81,10 @@ struct DecodeTiling {
   static constexpr int kMaxClusterHere = kClusterFit >= 8 ? 8 : kClusterFit >= 4 ? 4
                                          : kClusterFit >= 2 ? 2 : 1;
   static_assert(kStageBytes % 128 == 0, "stage alignment");
+  // lane l serves row l % T of a tile: T must be a power of two of at most 32,
+  // and a multiple of the 16-row mma blocks on the tensor-core path
+  static_assert((T & (T - 1)) == 0 && T <= 32, "tile rows: a power of two <= 32");
+  static_assert(!MMA || T % 16 == 0, "tile rows: whole 16-row mma blocks");
   static_assert(kEPL % kVE == 0 && kRowBytes % 128 == 0, "row vector layout");
   // Element of a row held in slot w of vector u by lane j of a row group.
   __device__ __forceinline__ static int elem(int u, int j, int w) {
@@ -149,10 +162,9 @@ __device__ __forceinline__ int request_rows(const DecodeLaunch& a, int b, int hk
 }
 
 // QMIX: q and K are bf16 and the dot products use the mixed-precision FMA.
-template <int D, typename KV, int G, int MODE, bool QMIX>
-__global__ void __launch_bounds__(DecodeTiling<D, KV, G, QMIX && G >= 2>::NW * 32)
-    decode_kernel(const DecodeLaunch a) {
-  using Tl = DecodeTiling<D, KV, G, QMIX && G >= 2>;
+template <int D, typename KV, int G, int MODE, bool QMIX, int NWARPS = DSA_DECODE_WARPS>
+__global__ void __launch_bounds__(NWARPS * 32) decode_kernel(const DecodeLaunch a) {
+  using Tl = DecodeTiling<D, KV, G, QMIX && G >= 2, NWARPS>;
   constexpr int T = Tl::T, S = Tl::S, NW = Tl::NW;
   constexpr int EPL = Tl::kEPL, NV = Tl::kNV, VE = Tl::kVE, RPL = Tl::kRPL;
   constexpr int kRowBytes = Tl::kRowBytes;
@@ -435,6 +447,9 @@ __global__ void __launch_bounds__(DecodeTiling<D, KV, G, QMIX && G >= 2>::NW * 3
       float sm[RB][4];
 #pragma unroll
       for (int rb = 0; rb < RB; ++rb) {
+        // two accumulator chains (even / odd 16-dim slices) halve the
+        // dependent mma latency; summed once at the end
+        float s2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int e = 0; e < 4; ++e) sm[rb][e] = 0.f;
         const unsigned char* arow =
@@ -443,8 +458,13 @@ __global__ void __launch_bounds__(DecodeTiling<D, KV, G, QMIX && G >= 2>::NW * 3
         for (int kk = 0; kk < NK; ++kk) {
           uint32_t af[4];
           ldsm_x4(af, arow + 32 * kk);
-          mma_bf16(sm[rb], af, qf[kk][0], qf[kk][1]);
+          if (kk & 1)
+            mma_bf16(s2, af, qf[kk][0], qf[kk][1]);
+          else
+            mma_bf16(sm[rb], af, qf[kk][0], qf[kk][1]);
         }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sm[rb][e] += s2[e];
       }
       // scale, mask rows past nrows (stale data), online softmax for the
       // thread's two heads (rows spread over the 8 lanes of a column pair)
@@ -792,14 +812,15 @@ struct IsBf16<bf16_t> {
   static constexpr bool value = true;
 };
 
-template <int D, typename KV, int G, int MODE, bool QMIX>
+template <int D, typename KV, int G, int MODE, bool QMIX, int NWARPS>
 cudaError_t launch_decode_one(const DecodeLaunch& a, cudaStream_t s) {
-  auto kern = decode_kernel<D, KV, G, MODE, QMIX>;
-  const int smem = DecodeTiling<D, KV, G, QMIX && G >= 2>::kSmem;
+  using Tl = DecodeTiling<D, KV, G, QMIX && G >= 2, NWARPS>;
+  auto kern = decode_kernel<D, KV, G, MODE, QMIX, NWARPS>;
+  const int smem = Tl::kSmem;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const dim3 grid(a.num_chunks, a.hkv, a.batch);
-  const dim3 block(DecodeTiling<D, KV, G, QMIX && G >= 2>::NW * 32);
+  const dim3 block(Tl::NW * 32);
   if (a.cluster > 1) {
     // the CTAs of one (request, kv head) form one cluster along x
     cudaLaunchConfig_t cfg = {};
@@ -820,107 +841,76 @@ cudaError_t launch_decode_one(const DecodeLaunch& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-template <typename KV, int MODE>
+// Calls f.template operator()<D, G>() for the built (head_dim, group), or
+// returns `fallback`.
+#define DSA_FOR_SHAPE(HEAD_DIM, GROUP, BODY)      \
+  do {                                            \
+    const int hd_ = (HEAD_DIM), g_ = (GROUP);     \
+    if (hd_ == 64 && g_ == 1) { BODY(64, 1) }     \
+    if (hd_ == 64 && g_ == 2) { BODY(64, 2) }     \
+    if (hd_ == 64 && g_ == 4) { BODY(64, 4) }     \
+    if (hd_ == 64 && g_ == 8) { BODY(64, 8) }     \
+    if (hd_ == 128 && g_ == 1) { BODY(128, 1) }   \
+    if (hd_ == 128 && g_ == 2) { BODY(128, 2) }   \
+    if (hd_ == 128 && g_ == 4) { BODY(128, 4) }   \
+    if (hd_ == 128 && g_ == 8) { BODY(128, 8) }   \
+  } while (0)
+
+template <typename KV, int MODE, int NWARPS>
 cudaError_t launch_decode_dispatch(const DecodeLaunch& a, cudaStream_t s) {
-  const int g = a.hq / a.hkv;
   const bool qmix = IsBf16<KV>::value && a.q_bf16 != 0;
-#define DSA_CASE(DD, GG)                                                           \
-  if (a.head_dim == DD && g == GG)                                                 \
-    return qmix ? launch_decode_one<DD, KV, GG, MODE, IsBf16<KV>::value>(a, s)     \
-                : launch_decode_one<DD, KV, GG, MODE, false>(a, s);
-  DSA_CASE(64, 1)
-  DSA_CASE(64, 2)
-  DSA_CASE(64, 4)
-  DSA_CASE(64, 8)
-  DSA_CASE(128, 1)
-  DSA_CASE(128, 2)
-  DSA_CASE(128, 4)
-  DSA_CASE(128, 8)
-#undef DSA_CASE
+#define DSA_BODY(DD, GG)                                                                  \
+  return qmix ? launch_decode_one<DD, KV, GG, MODE, IsBf16<KV>::value, NWARPS>(a, s)      \
+              : launch_decode_one<DD, KV, GG, MODE, false, NWARPS>(a, s);
+  DSA_FOR_SHAPE(a.head_dim, a.hq / a.hkv, DSA_BODY);
+#undef DSA_BODY
   return cudaErrorInvalidValue;
 }
 
+// Warps per CTA built for (KV, mode): the fused call with bf16 KV also has a
+// DSA_DECODE_WARPS_BIG build.
 template <typename KV>
-cudaError_t launch_decode_t(const DecodeLaunch& a, int mode, cudaStream_t s) {
-  switch (mode) {
-    case kRowsDense: return launch_decode_dispatch<KV, kRowsDense>(a, s);
-    case kRowsList: return launch_decode_dispatch<KV, kRowsList>(a, s);
-    case kRowsMask: return launch_decode_dispatch<KV, kRowsMask>(a, s);
-  }
-  return cudaErrorInvalidValue;
+constexpr bool has_big_warps(int mode) {
+  return IsBf16<KV>::value && mode == kRowsMask && DSA_DECODE_WARPS_BIG != DSA_DECODE_WARPS;
 }
 
-template <typename KV>
-int decode_cluster_limit_t(int head_dim, int group) {
-#define DSA_CASE(DD, GG)                                                                   \
-  if (head_dim == DD && group == GG)                                                       \
-    return IsBf16<KV>::value && GG >= 2 ? DecodeTiling<DD, KV, GG, true>::kMaxClusterHere  \
-                                        : DecodeTiling<DD, KV, GG, false>::kMaxClusterHere;
-  DSA_CASE(64, 1)
-  DSA_CASE(64, 2)
-  DSA_CASE(64, 4)
-  DSA_CASE(64, 8)
-  DSA_CASE(128, 1)
-  DSA_CASE(128, 2)
-  DSA_CASE(128, 4)
-  DSA_CASE(128, 8)
-#undef DSA_CASE
-  return 1;
-}
-
-template <typename KV>
-int decode_rows_per_pass_t(int head_dim, int group) {
-#define DSA_CASE(DD, GG) \
-  if (head_dim == DD && group == GG) return DecodeTiling<DD, KV, GG>::NW * DecodeTiling<DD, KV, GG>::T;
-  DSA_CASE(64, 1)
-  DSA_CASE(64, 2)
-  DSA_CASE(64, 4)
-  DSA_CASE(64, 8)
-  DSA_CASE(128, 1)
-  DSA_CASE(128, 2)
-  DSA_CASE(128, 4)
-  DSA_CASE(128, 8)
-#undef DSA_CASE
-  return 0;
-}
-
-// Occupancy of the decode kernel as launched with `mode`.
+// One row mode: the default build, or for the fused call with bf16 KV the
+// DSA_DECODE_WARPS_BIG build when the plan asks for it.
 template <typename KV, int MODE>
-int decode_ctas_per_sm_m(int head_dim, int group) {
-  int n = 0;
-#define DSA_CASE(DD, GG)                                                                   \
-  if (head_dim == DD && group == GG) {                                                     \
-    using Tl = DecodeTiling<DD, KV, GG, IsBf16<KV>::value && (GG >= 2)>;                   \
-    auto kern = decode_kernel<DD, KV, GG, MODE, IsBf16<KV>::value>;                        \
-    const int smem = Tl::kSmem;                                                            \
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=   \
-        cudaSuccess)                                                                       \
-      return 1;                                                                            \
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, Tl::NW * 32, smem) !=      \
-        cudaSuccess)                                                                       \
-      return 1;                                                                            \
-    return n < 1 ? 1 : n;                                                                  \
-  }
-  DSA_CASE(64, 1)
-  DSA_CASE(64, 2)
-  DSA_CASE(64, 4)
-  DSA_CASE(64, 8)
-  DSA_CASE(128, 1)
-  DSA_CASE(128, 2)
-  DSA_CASE(128, 4)
-  DSA_CASE(128, 8)
-#undef DSA_CASE
-  return 1;
+cudaError_t launch_decode_mode(const DecodeLaunch& a, cudaStream_t s) {
+  if constexpr (has_big_warps<KV>(MODE))
+    if (a.warps == DSA_DECODE_WARPS_BIG)
+      return launch_decode_dispatch<KV, MODE, DSA_DECODE_WARPS_BIG>(a, s);
+  return launch_decode_dispatch<KV, MODE, DSA_DECODE_WARPS>(a, s);
 }
 
-template <typename KV>
-int decode_ctas_per_sm_t(int head_dim, int group, int mode) {
-  switch (mode) {
-    case kRowsDense: return decode_ctas_per_sm_m<KV, kRowsDense>(head_dim, group);
-    case kRowsList: return decode_ctas_per_sm_m<KV, kRowsList>(head_dim, group);
-    case kRowsMask: return decode_ctas_per_sm_m<KV, kRowsMask>(head_dim, group);
-  }
-  return 1;
+template <typename KV, int MODE, int NWARPS>
+DecodeShape decode_shape_m(int head_dim, int group) {
+  DecodeShape r{0, 1, 1, NWARPS};
+#define DSA_BODY(DD, GG)                                                                   \
+  using Tl = DecodeTiling<DD, KV, GG, IsBf16<KV>::value && (GG >= 2), NWARPS>;             \
+  auto kern = decode_kernel<DD, KV, GG, MODE, IsBf16<KV>::value, NWARPS>;                  \
+  r.rows_per_pass = Tl::NW * Tl::T;                                                        \
+  r.cluster_limit = Tl::kMaxClusterHere;                                                   \
+  int n = 0;                                                                               \
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Tl::kSmem) == \
+          cudaSuccess &&                                                                   \
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, Tl::NW * 32, Tl::kSmem) ==   \
+          cudaSuccess &&                                                                   \
+      n > 1)                                                                               \
+    r.ctas_per_sm = n;                                                                     \
+  return r;
+  DSA_FOR_SHAPE(head_dim, group, DSA_BODY);
+#undef DSA_BODY
+  return r;
+}
+
+template <typename KV, int MODE>
+DecodeShape decode_shape_mode(int head_dim, int group, int warps) {
+  if constexpr (has_big_warps<KV>(MODE))
+    if (warps == DSA_DECODE_WARPS_BIG)
+      return decode_shape_m<KV, MODE, DSA_DECODE_WARPS_BIG>(head_dim, group);
+  return decode_shape_m<KV, MODE, DSA_DECODE_WARPS>(head_dim, group);
 }
 
 }  // namespace dsa

@@ -1,22 +1,29 @@
-// decode_bf16.cu -- bf16 KV instantiations of the decode kernels.
+// decode_bf16.cu -- bf16 KV instantiations of the decode kernel for dense rows
+// and kept lists, and the bf16 entry points (the fused mode's builds live in
+// decode_bf16_mask.cu so that the two compile in parallel).
 #include "decode.cuh"
 
 namespace dsa {
 
+cudaError_t launch_decode_bf16_mask(const DecodeLaunch& a, cudaStream_t s);
+DecodeShape decode_shape_bf16_mask(int head_dim, int group, int warps);
+
 cudaError_t launch_decode_bf16(const DecodeLaunch& a, int mode, cudaStream_t s) {
-  return launch_decode_t<bf16_t>(a, mode, s);
+  switch (mode) {
+    case kRowsDense: return launch_decode_mode<bf16_t, kRowsDense>(a, s);
+    case kRowsList: return launch_decode_mode<bf16_t, kRowsList>(a, s);
+    case kRowsMask: return launch_decode_bf16_mask(a, s);
+  }
+  return cudaErrorInvalidValue;
 }
 
-int decode_cluster_limit_bf16(int head_dim, int group) {
-  return decode_cluster_limit_t<bf16_t>(head_dim, group);
-}
-
-int decode_rows_per_pass_bf16(int head_dim, int group) {
-  return decode_rows_per_pass_t<bf16_t>(head_dim, group);
-}
-
-int decode_ctas_per_sm_bf16(int head_dim, int group, int mode) {
-  return decode_ctas_per_sm_t<bf16_t>(head_dim, group, mode);
+DecodeShape decode_shape_bf16(int head_dim, int group, int mode, int warps) {
+  switch (mode) {
+    case kRowsDense: return decode_shape_mode<bf16_t, kRowsDense>(head_dim, group, warps);
+    case kRowsList: return decode_shape_mode<bf16_t, kRowsList>(head_dim, group, warps);
+    case kRowsMask: return decode_shape_bf16_mask(head_dim, group, warps);
+  }
+  return DecodeShape{0, 1, 1, DSA_DECODE_WARPS};
 }
 
 }  // namespace dsa

@@ -5,7 +5,12 @@
 namespace dsa {
 
 cudaError_t launch_decode_f32(const DecodeLaunch& a, int mode, cudaStream_t s) {
-  return launch_decode_t<float>(a, mode, s);
+  switch (mode) {
+    case kRowsDense: return launch_decode_mode<float, kRowsDense>(a, s);
+    case kRowsList: return launch_decode_mode<float, kRowsList>(a, s);
+    case kRowsMask: return launch_decode_mode<float, kRowsMask>(a, s);
+  }
+  return cudaErrorInvalidValue;
 }
 
 template <int D>
@@ -24,16 +29,13 @@ cudaError_t launch_merge(const DecodeLaunch& a, int mode, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-int decode_cluster_limit_f32(int head_dim, int group) {
-  return decode_cluster_limit_t<float>(head_dim, group);
-}
-
-int decode_rows_per_pass_f32(int head_dim, int group) {
-  return decode_rows_per_pass_t<float>(head_dim, group);
-}
-
-int decode_ctas_per_sm_f32(int head_dim, int group, int mode) {
-  return decode_ctas_per_sm_t<float>(head_dim, group, mode);
+DecodeShape decode_shape_f32(int head_dim, int group, int mode, int warps) {
+  switch (mode) {
+    case kRowsDense: return decode_shape_mode<float, kRowsDense>(head_dim, group, warps);
+    case kRowsList: return decode_shape_mode<float, kRowsList>(head_dim, group, warps);
+    case kRowsMask: return decode_shape_mode<float, kRowsMask>(head_dim, group, warps);
+  }
+  return DecodeShape{0, 1, 1, DSA_DECODE_WARPS};
 }
 
 }  // namespace dsa

@@ -140,7 +140,7 @@ int32_t* unit_rows(const dsa_dims* d, void* ws) {
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 struct Plan {
-  int chunk, num_chunks, quantum, per_sm, cluster;
+  int chunk, num_chunks, quantum, per_sm, cluster, warps;
 };
 
 // Automatic cluster size: a CTA's fixed latency (first copies, end-of-CTA
@@ -154,22 +154,31 @@ int sparse_cluster_auto(int64_t units, int64_t slots) {
   return best;
 }
 
-Plan decode_plan(const dsa_dims* d, int mode) {
-  const bool kv_bf16 = d->kv_dtype == DSA_BF16;
+DecodeShape decode_shape(const dsa_dims* d, int mode, int warps) {
   const int g = d->hq / d->hkv;
+  return d->kv_dtype == DSA_BF16 ? decode_shape_bf16(d->head_dim, g, mode, warps)
+                                 : decode_shape_f32(d->head_dim, g, mode, warps);
+}
+
+Plan decode_plan(const dsa_dims* d, int mode) {
   const int64_t n_max = mode == kModeDense ? dense_rows(d) : d->max_kept;
-  Plan p{};
-  p.quantum = kv_bf16 ? decode_rows_per_pass_bf16(d->head_dim, g)
-                      : decode_rows_per_pass_f32(d->head_dim, g);
-  p.per_sm = kv_bf16 ? decode_ctas_per_sm_bf16(d->head_dim, g, mode)
-                     : decode_ctas_per_sm_f32(d->head_dim, g, mode);
-  p.cluster = 1;
   const int64_t units = static_cast<int64_t>(d->batch) * d->hkv;
+  DecodeShape sh = decode_shape(d, mode, 0);
+  // The fused call on a batch of more than two waves of units runs the build
+  // with fewer warps per CTA (when there is one): more, smaller CTAs per SM
+  // overlap one CTA's start-up with the others' streaming.
+  if (mode == kModeMask && units > 2 * static_cast<int64_t>(sm_count()) * sh.ctas_per_sm) {
+    const DecodeShape big = decode_shape(d, mode, kDecodeWarpsBig);
+    if (big.warps == kDecodeWarpsBig) sh = big;
+  }
+  Plan p{};
+  p.quantum = sh.rows_per_pass;
+  p.per_sm = sh.ctas_per_sm;
+  p.warps = sh.warps;
+  p.cluster = 1;
   int ncl = g_sparse_cluster.load(std::memory_order_relaxed);
   if (ncl == 0) ncl = sparse_cluster_auto(units, sm_count() * p.per_sm);
-  const int limit = kv_bf16 ? decode_cluster_limit_bf16(d->head_dim, g)
-                            : decode_cluster_limit_f32(d->head_dim, g);
-  while (ncl > limit) ncl /= 2;
+  while (ncl > sh.cluster_limit) ncl /= 2;
   if (mode != kModeDense && ncl > 1 && n_max > p.quantum) {
     // the rows of a unit split evenly over a cluster of ncl CTAs
     p.cluster = ncl;
@@ -177,7 +186,7 @@ Plan decode_plan(const dsa_dims* d, int mode) {
     p.chunk = static_cast<int>(ceil_div(n_max, ncl));
     return p;
   }
-  choose_chunks(n_max, static_cast<int64_t>(d->batch) * d->hkv, sm_count() * p.per_sm, p.quantum,
+  choose_chunks(n_max, units, sm_count() * p.per_sm, p.quantum,
                 mode == kModeDense ? DSA_DENSE_WAVES : DSA_SPARSE_WAVES, &p.chunk,
                 &p.num_chunks);
   return p;
@@ -237,6 +246,7 @@ dsa_status decode_common(const dsa_dims* d, int mode, const void* q, const void*
   a.chunk = plan.chunk;
   a.num_chunks = plan.num_chunks;
   a.cluster = plan.cluster;
+  a.warps = plan.warps;
   a.scale_log2 = scale * kLog2e;
   a.out = out;
   a.lse = lse;
@@ -387,7 +397,7 @@ dsa_status dsa_attention_mass(const dsa_dims* dims, const void* q, const void* k
 }
 
 dsa_status dsa_decode_plan(const dsa_dims* dims, int32_t mode, int32_t* chunk,
-                           int32_t* num_chunks, int32_t* launches) {
+                           int32_t* num_chunks, int32_t* launches, int32_t* warps) {
   const dsa_status st = check_dims(dims);
   if (st != DSA_OK) return st;
   if (mode < kModeDense || mode > kModeMask) return DSA_ERR_INVALID_ARG;
@@ -397,6 +407,7 @@ dsa_status dsa_decode_plan(const dsa_dims* dims, int32_t mode, int32_t* chunk,
   if (num_chunks) *num_chunks = p.num_chunks;
   if (launches)
     *launches = dims->batch == 0 ? 0 : (p.num_chunks > 1 && p.cluster <= 1 ? 2 : 1);
+  if (warps) *warps = p.warps;
   return DSA_OK;
 }
 

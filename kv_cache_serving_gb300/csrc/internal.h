@@ -33,6 +33,7 @@ struct DecodeLaunch {
   int32_t max_window, mask_words;  // kRowsMask only
   int32_t chunk, num_chunks;
   int32_t cluster;   // > 1: the num_chunks (== cluster) CTAs of a unit merge in a cluster
+  int32_t warps;     // warps per CTA of the build to launch (see DecodeShape)
   float scale_log2;  // softmax scale * log2(e)
   float* out;
   float* lse;
@@ -90,15 +91,20 @@ int mass_rows_per_pass(int head_dim, int group, bool kv_bf16, bool q_bf16);
 int mass_ctas_per_sm(int head_dim, int group, bool kv_bf16, bool q_bf16);
 cudaError_t launch_compact(const CompactLaunch& a, cudaStream_t s);
 
-// Largest cluster of decode CTAs whose merge buffer fits the CTA's rings.
-int decode_cluster_limit_bf16(int head_dim, int group);
-int decode_cluster_limit_f32(int head_dim, int group);
-// Rows one pass of all warps of a decode CTA covers (warps x tile rows), for
-// the host's chunk choice.
-int decode_rows_per_pass_bf16(int head_dim, int group);
-int decode_rows_per_pass_f32(int head_dim, int group);
-// Resident CTAs per SM of the decode kernel for this instantiation (>= 1).
-int decode_ctas_per_sm_bf16(int head_dim, int group, int mode);
-int decode_ctas_per_sm_f32(int head_dim, int group, int mode);
+// Warps per CTA of the second build of the fused call (bf16 KV), chosen for
+// batches of many units; must match DSA_DECODE_WARPS_BIG in decode.cuh.
+constexpr int kDecodeWarpsBig = 3;
+
+// Host-side facts about one build of the decode kernel, for the chunk choice.
+struct DecodeShape {
+  int rows_per_pass;  // warps x tile rows
+  int ctas_per_sm;    // resident CTAs per SM (>= 1)
+  int cluster_limit;  // largest cluster whose merge buffer fits the rings
+  int warps;          // warps per CTA of this build
+};
+// The build of (head_dim, group, mode) with `warps` warps per CTA when there is
+// one (the fused call with bf16 KV has 3 and 4), else the default build.
+DecodeShape decode_shape_bf16(int head_dim, int group, int mode, int warps);
+DecodeShape decode_shape_f32(int head_dim, int group, int mode, int warps);
 
 }  // namespace dsa

@@ -92,6 +92,7 @@ def test_null_pointers_rejected_before_launch():
     assert lib.dsa_decode_sparse_masked(ctypes.byref(big), fake, fake, fake, fake, fake, fake,
                                         fake, fake, None, 0.1, fake, None, fake, None) == \
         dsa.DSA_ERR_UNSUPPORTED
-    assert lib.dsa_decode_plan(ctypes.byref(d), 3, None, None, None) == dsa.DSA_ERR_INVALID_ARG
+    assert lib.dsa_decode_plan(ctypes.byref(d), 3, None, None, None, None) == \
+        dsa.DSA_ERR_INVALID_ARG
     code = ctypes.c_int32(0)
     assert lib.dsa_get_device_error(None, None, ctypes.byref(code)) == dsa.DSA_ERR_INVALID_ARG

@@ -51,7 +51,7 @@ def test_noalloc_matches_workspace_entry_point(name, batch):
     ref_out, ref_lse = ref_out.clone(), ref_lse.clone()
     torch.cuda.synchronize()
     assert bt.device_error() == 0
-    _, chunks, _ = dsa.dsa_decode_plan(bt.dims, True)
+    chunks = dsa.dsa_decode_plan(bt.dims, dsa.PLAN_SPARSE)[1]
     assert 256 + w["batch"] * w["hq"] * chunks * (w["head_dim"] + 2) * 4 <= \
         dsa.NOALLOC_SCRATCH_BYTES
 
