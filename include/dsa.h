@@ -111,7 +111,8 @@ int32_t dsa_version(void);
 const char* dsa_status_string(dsa_status status);
 
 /* Bytes of device workspace every call on `dims` needs (0 if dims is invalid).
- * Depends on dims only. */
+ * Depends on dims only.  Zero-fill it before the first call: its error word
+ * must start at zero (dsa_clear_device_error resets it after an error). */
 size_t dsa_workspace_size(const dsa_dims* dims);
 
 /*

@@ -311,7 +311,8 @@ __global__ void __launch_bounds__(NWARPS * 32) decode_kernel(const DecodeLaunch 
 
   WarpAttn<D, KV, G, QMIX, T> wa;
   static_assert(WarpAttn<D, KV, G, QMIX, T>::kRowStride == Tl::kRowStride, "row stride");
-  wa.load_q(a.q, a.q_bf16 != 0, static_cast<size_t>(b) * a.hq + hk * G, lane);
+  typename WarpAttn<D, KV, G, QMIX, T>::Q wq_;
+  wq_.load(a.q, a.q_bf16 != 0, static_cast<size_t>(b) * a.hq + hk * G, lane);
   wa.reset();
 
   // prologue: kept indices of tiles 0..S+1, page ids of tiles 0..S, copies of
@@ -343,7 +344,7 @@ __global__ void __launch_bounds__(NWARPS * 32) decode_kernel(const DecodeLaunch 
     const unsigned char* kt = kst + static_cast<size_t>(stage) * T * kRowStride;
     unsigned char* vt = vst + static_cast<size_t>(stage) * T * kRowStride;
 
-    wa.tile(kt, vt, nrows, a.scale_log2, ps, lane);
+    wa.tile(wq_, kt, vt, nrows, a.scale_log2, ps, lane);
     __syncwarp();
     fence_proxy_async_smem();
     if (t + S < my_tiles) issue(t + S, stage, j0, pg0);

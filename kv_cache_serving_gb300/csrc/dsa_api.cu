@@ -137,6 +137,10 @@ int32_t* unit_rows(const dsa_dims* d, void* ws) {
                                     partials_region(d));
 }
 
+size_t unit_ints_region(const dsa_dims* d) {
+  return round_up(static_cast<size_t>(d->batch) * d->hkv * sizeof(int32_t), 256);
+}
+
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 struct Plan {
@@ -283,8 +287,7 @@ const char* dsa_status_string(dsa_status status) {
 
 size_t dsa_workspace_size(const dsa_dims* dims) {
   if (check_dims(dims) != DSA_OK) return 0;
-  const size_t counts = static_cast<size_t>(dims->batch) * dims->hkv * sizeof(int32_t);
-  return kWsHeader + partials_region(dims) + round_up(counts, 256);
+  return kWsHeader + partials_region(dims) + unit_ints_region(dims);
 }
 
 dsa_status dsa_build_index(const dsa_dims* dims, const int32_t* seq_len,

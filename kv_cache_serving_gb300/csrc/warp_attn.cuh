@@ -61,40 +61,28 @@ __device__ __forceinline__ void vec_to_f32<float>(const uint4& v, float* o) {
   o[3] = __uint_as_float(v.w);
 }
 
-// QMIX: q and K are bf16 (mixed-precision FMA, or tensor cores when G >= 2).
-// T: rows per tile.  Shared-memory rows are kRowStride bytes apart.
-template <int D, typename KV, int G, bool QMIX, int T>
-struct WarpAttn {
+// The G query vectors of one kv head in the registers of a warp.  CUDA cores:
+// this lane's elements (packed bf16 pairs with QMIX, else fp32).  Tensor cores:
+// mma B fragments (thread t holds head t/4, dims 16k + 2(t%4) + {0,1,8,9}).
+template <int D, typename KV, int G, bool QMIX>
+struct WarpQ {
   static constexpr bool kMMA = QMIX && G >= 2;
   static constexpr int kElt = static_cast<int>(sizeof(KV));
-  static constexpr int kRowBytes = D * kElt;
-  static constexpr int kVE = 16 / kElt;     // elements per 16-byte vector
-  static constexpr int kEPL = D / 8;        // elements of a row per lane
-  static constexpr int kNV = kEPL / kVE;    // 16-byte vectors of a row per lane
-  static constexpr int kRPL = T / 4;        // rows of a tile per lane
-  static constexpr int kRowStride = kRowBytes + (kMMA ? 16 : 0);
+  static constexpr int kVE = 16 / kElt;
+  static constexpr int kEPL = D / 8;
+  static constexpr int kNV = kEPL / kVE;
   static constexpr int kQW = QMIX ? kEPL / 2 : kEPL;
   static constexpr int GC = kMMA ? 1 : G;
   static constexpr int NK = D / 16;
-  static_assert((T & (T - 1)) == 0 && T <= 32, "tile rows: a power of two <= 32");
-  static_assert(!kMMA || T % 16 == 0, "tile rows: whole 16-row mma blocks");
+  uint32_t qv[GC][kMMA ? 1 : kQW];
+  uint32_t qf[kMMA ? NK : 1][2];
 
-  // Element of a row held in slot w of vector u by lane j of a row group.
   __device__ __forceinline__ static int elem(int u, int j, int w) {
     return u * (128 / kElt) + j * kVE + w;
   }
 
-  // CUDA cores: this lane's elements of the G query vectors (packed bf16 pairs
-  // with QMIX, else fp32) and per-head state over the lane's rows.  Tensor
-  // cores: q as mma B fragments (thread t holds head t/4, dims 16k + 2(t%4) +
-  // {0,1,8,9}) and the state of heads 2(t%4), 2(t%4)+1.
-  uint32_t qv[GC][kMMA ? 1 : kQW];
-  uint32_t qf[kMMA ? NK : 1][2];
-  float m_run[GC], l_run[GC], acc[GC][kMMA ? 1 : kEPL];
-  float m2[2], l2[2], oacc[kMMA ? NK : 1][4];
-
   // q rows qhead0 .. qhead0+G-1 of [*][D] (bf16 when q_bf16, else fp32).
-  __device__ __forceinline__ void load_q(const void* q, bool q_bf16, size_t qhead0, int lane) {
+  __device__ __forceinline__ void load(const void* q, bool q_bf16, size_t qhead0, int lane) {
     if constexpr (kMMA) {
       const int g4 = lane >> 2, tig = lane & 3;
       const uint32_t* q32 =
@@ -134,6 +122,35 @@ struct WarpAttn {
       }
     }
   }
+};
+
+// QMIX: q and K are bf16 (mixed-precision FMA, or tensor cores when G >= 2).
+// T: rows per tile.  Shared-memory rows are kRowStride bytes apart.
+template <int D, typename KV, int G, bool QMIX, int T>
+struct WarpAttn {
+  static constexpr bool kMMA = QMIX && G >= 2;
+  static constexpr int kElt = static_cast<int>(sizeof(KV));
+  static constexpr int kRowBytes = D * kElt;
+  static constexpr int kVE = 16 / kElt;     // elements per 16-byte vector
+  static constexpr int kEPL = D / 8;        // elements of a row per lane
+  static constexpr int kNV = kEPL / kVE;    // 16-byte vectors of a row per lane
+  static constexpr int kRPL = T / 4;        // rows of a tile per lane
+  static constexpr int kRowStride = kRowBytes + (kMMA ? 16 : 0);
+  static constexpr int GC = kMMA ? 1 : G;
+  static constexpr int NK = D / 16;
+  static_assert((T & (T - 1)) == 0 && T <= 32, "tile rows: a power of two <= 32");
+  static_assert(!kMMA || T % 16 == 0, "tile rows: whole 16-row mma blocks");
+
+  // Element of a row held in slot w of vector u by lane j of a row group.
+  __device__ __forceinline__ static int elem(int u, int j, int w) {
+    return u * (128 / kElt) + j * kVE + w;
+  }
+
+  using Q = WarpQ<D, KV, G, QMIX>;
+  // CUDA cores: per-head state over the lane's rows.  Tensor cores: the state
+  // of heads 2(t%4), 2(t%4)+1 for thread t.
+  float m_run[GC], l_run[GC], acc[GC][kMMA ? 1 : kEPL];
+  float m2[2], l2[2], oacc[kMMA ? NK : 1][4];
 
   __device__ __forceinline__ void reset() {
     if constexpr (kMMA) {
@@ -160,8 +177,8 @@ struct WarpAttn {
   // One tile: rows 0..nrows-1 of kt / vt (kRowStride apart; rows past nrows may
   // hold stale data).  ps: this warp's [hi, lo][8 heads][T] bf16 scratch (tensor
   // cores only).  The tensor-core engine zeroes V rows past nrows in place.
-  __device__ __forceinline__ void tile(const unsigned char* kt, unsigned char* vt, int nrows,
-                                       float scale_log2, uint16_t* ps, int lane) {
+  __device__ __forceinline__ void tile(const Q& q, const unsigned char* kt, unsigned char* vt,
+                                       int nrows, float scale_log2, uint16_t* ps, int lane) {
     if constexpr (kMMA) {
       const int g4 = lane >> 2, tig = lane & 3;
       constexpr int RB = T / 16;
@@ -180,9 +197,9 @@ struct WarpAttn {
           uint32_t af[4];
           ldsm_x4(af, arow + 32 * kk);
           if (kk & 1)
-            mma_bf16(s2, af, qf[kk][0], qf[kk][1]);
+            mma_bf16(s2, af, q.qf[kk][0], q.qf[kk][1]);
           else
-            mma_bf16(sm[rb], af, qf[kk][0], qf[kk][1]);
+            mma_bf16(sm[rb], af, q.qf[kk][0], q.qf[kk][1]);
         }
 #pragma unroll
         for (int e = 0; e < 4; ++e) sm[rb][e] += s2[e];
@@ -274,10 +291,10 @@ struct WarpAttn {
           if (QMIX) {
 #pragma unroll
             for (int u = 0; u < kNV; ++u) {
-              d0 = fma2_bf16(kv[u].x, qv[h][4 * u], d0);
-              d1 = fma2_bf16(kv[u].y, qv[h][4 * u + 1], d1);
-              d0 = fma2_bf16(kv[u].z, qv[h][4 * u + 2], d0);
-              d1 = fma2_bf16(kv[u].w, qv[h][4 * u + 3], d1);
+              d0 = fma2_bf16(kv[u].x, q.qv[h][4 * u], d0);
+              d1 = fma2_bf16(kv[u].y, q.qv[h][4 * u + 1], d1);
+              d0 = fma2_bf16(kv[u].z, q.qv[h][4 * u + 2], d0);
+              d1 = fma2_bf16(kv[u].w, q.qv[h][4 * u + 3], d1);
             }
           } else {
 #pragma unroll
@@ -286,8 +303,8 @@ struct WarpAttn {
               vec_to_f32<KV>(kv[u], kf);
 #pragma unroll
               for (int w = 0; w < kVE; w += 2) {
-                d0 = fmaf(__uint_as_float(qv[h][u * kVE + w]), kf[w], d0);
-                d1 = fmaf(__uint_as_float(qv[h][u * kVE + w + 1]), kf[w + 1], d1);
+                d0 = fmaf(__uint_as_float(q.qv[h][u * kVE + w]), kf[w], d0);
+                d1 = fmaf(__uint_as_float(q.qv[h][u * kVE + w + 1]), kf[w + 1], d1);
               }
             }
           }

@@ -242,6 +242,7 @@ def dsa_get_sparse_cluster() -> int:
     return int(_load().dsa_get_sparse_cluster())
 
 
+
 def dsa_get_device_error(ws, stream=None) -> int:
     """Synchronising read of the workspace error word; returns the DSA_DEV_* code."""
     code = ctypes.c_int32(0)

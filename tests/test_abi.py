@@ -40,6 +40,21 @@ def test_library_exports_every_declared_symbol():
     assert all(not n.startswith("_Z") for n in exported)
 
 
+def test_tuning_setters():
+    for setter, getter, good, bad in (
+            (dsa.dsa_set_sparse_cluster, dsa.dsa_get_sparse_cluster, (0, 1, 2, 8), (-1, 9)),):
+        saved = getter()
+        try:
+            for v in good:
+                setter(v)
+                assert getter() == v
+            for v in bad:
+                with pytest.raises(dsa.DSAError):
+                    setter(v)
+        finally:
+            setter(saved)
+
+
 def test_host_only_calls():
     assert dsa.dsa_version() >= 1
     assert dsa.dsa_status_string(0) == "DSA_OK"
