@@ -59,7 +59,8 @@ struct DecodeTiling {
   static constexpr int kElt = static_cast<int>(sizeof(KV));
   static constexpr int kRowBytes = D * kElt;
   static constexpr int kT0 = DSA_DECODE_STAGE_BYTES / (2 * kRowBytes);  // K+V of one stage
-  static constexpr int T = kT0 > 32 ? 32 : (kT0 < 8 ? 8 : kT0);
+  static constexpr int kTmin = MMA ? 16 : 8;  // whole 16-row mma blocks
+  static constexpr int T = kT0 > 32 ? 32 : (kT0 < kTmin ? kTmin : kT0);
   static constexpr int S = DSA_DECODE_STAGES;  // stages per warp
   static constexpr int NW = NWARPS;            // warps per CTA
   static constexpr int kVE = 16 / kElt;        // elements per 16-byte vector
