@@ -15,7 +15,8 @@
 // Build-time tuning knobs: waves of resident CTAs the chunking aims for.  Kept
 // lists are short, so sparse decode wants one chunk per (request, kv head)
 // where possible (no merge launch); dense rows vary with seq_len, so dense
-// decode and attention mass want more, shorter chunks for balance.
+// decode and attention mass want more, shorter chunks for balance (the mass
+// kernel's two score engines measured best at different counts).
 #ifndef DSA_SPARSE_WAVES
 #define DSA_SPARSE_WAVES 1
 #endif
@@ -23,7 +24,10 @@
 #define DSA_DENSE_WAVES 8
 #endif
 #ifndef DSA_MASS_WAVES
-#define DSA_MASS_WAVES 16
+#define DSA_MASS_WAVES 4
+#endif
+#ifndef DSA_MASS_WAVES_MMA
+#define DSA_MASS_WAVES_MMA 8
 #endif
 // CTAs that share one (request, kv head) of sparse decode as a thread-block
 // cluster, merging through distributed shared memory (1: no cluster, 0: chosen
@@ -389,8 +393,9 @@ dsa_status dsa_attention_mass(const dsa_dims* dims, const void* q, const void* k
   const int g = dims->hq / dims->hkv;
   choose_chunks(n_max, static_cast<int64_t>(dims->batch) * dims->hkv,
                 sm_count() * mass_ctas_per_sm(dims->head_dim, g, kv_bf16, q_bf16),
-                mass_rows_per_pass(dims->head_dim, g, kv_bf16, q_bf16), DSA_MASS_WAVES, &a.chunk,
-                &a.num_chunks);
+                mass_rows_per_pass(dims->head_dim, g, kv_bf16, q_bf16),
+                mass_uses_tensor_cores(kv_bf16, q_bf16, g) ? DSA_MASS_WAVES_MMA : DSA_MASS_WAVES,
+                &a.chunk, &a.num_chunks);
   a.scale_log2 = scale * kLog2e;
   a.mass = mass;
   a.offset_mass = offset_mass;

@@ -88,6 +88,8 @@ cudaError_t launch_mass(const MassLaunch& a, bool kv_bf16, cudaStream_t s);
 // Rows one pass of all warps of an attention-mass CTA covers, and its resident
 // CTAs per SM (>= 1), for the host's chunk choice.
 int mass_rows_per_pass(int head_dim, int group, bool kv_bf16, bool q_bf16);
+// The attention-mass build for these dtypes scores on the tensor cores.
+bool mass_uses_tensor_cores(bool kv_bf16, bool q_bf16, int group);
 int mass_ctas_per_sm(int head_dim, int group, bool kv_bf16, bool q_bf16);
 cudaError_t launch_compact(const CompactLaunch& a, cudaStream_t s);
 

@@ -103,14 +103,19 @@ __global__ void __launch_bounds__(MassTiling<D, KV, G>::NW * 32) mass_kernel(con
 
   const KV* kg = reinterpret_cast<const KV*>(a.k);
   const int32_t* pt = a.page_table + static_cast<size_t>(b) * a.max_pages;
-  auto issue = [&](int t, int stage) {
+  const int my_tiles = warp < ntiles ? (ntiles - warp + NW - 1) / NW : 0;
+  // page id of this lane's row of tile t, loaded a tile before its copy
+  auto load_pg = [&](int t) -> int {
+    const int j = row0 + (warp + t * NW) * T + lane;
+    return (t < my_tiles && lane < T && j < row1) ? __ldg(pt + (j >> 4)) : 0;
+  };
+  auto issue = [&](int t, int stage, int pg) {
     const int tr0 = row0 + (warp + t * NW) * T;
     const int nrows = min(T, row1 - tr0);
     if (lane == 0) mbar_arrive_expect_tx(&bars[stage], static_cast<uint32_t>(nrows * kRowBytes));
     __syncwarp();
     if (lane < nrows) {
       const int j = tr0 + lane;
-      int pg = pt[j >> 4];
       if (static_cast<unsigned>(pg) >= static_cast<unsigned>(a.num_pages)) {
         set_error(a.err, DSA_DEV_BAD_PAGE);
         pg = 0;
@@ -136,8 +141,15 @@ __global__ void __launch_bounds__(MassTiling<D, KV, G>::NW * 32) mass_kernel(con
     for (int k = 0; k < 4; ++k) bins[h][k] = 0.f;
   }
 
-  const int my_tiles = warp < ntiles ? (ntiles - warp + NW - 1) / NW : 0;
-  for (int t = 0; t < S && t < my_tiles; ++t) issue(t, t);
+  {
+    int pg0[S];
+#pragma unroll
+    for (int t = 0; t < S; ++t) pg0[t] = load_pg(t);
+#pragma unroll
+    for (int t = 0; t < S; ++t)
+      if (t < my_tiles) issue(t, t, pg0[t]);
+  }
+  int pg_next = load_pg(S);  // next tile to issue: S
   const int myrow = RowMap<T>::row(lane);
   const bool own = RowMap<T>::owner(lane);
   const size_t om_stride = static_cast<size_t>(a.max_window) + 1;
@@ -185,7 +197,8 @@ __global__ void __launch_bounds__(MassTiling<D, KV, G>::NW * 32) mass_kernel(con
     }
     __syncwarp();
     fence_proxy_async_smem();
-    if (t + S < my_tiles) issue(t + S, stage);
+    if (t + S < my_tiles) issue(t + S, stage, pg_next);
+    pg_next = load_pg(t + S + 1);
   }
   if (failed_at >= 0) {
     if (lane == 0) set_error(a.err, DSA_DEV_TIMEOUT);
@@ -507,7 +520,7 @@ __global__ void __launch_bounds__(128) mass_merge_kernel(const MassLaunch a) {
 }
 
 // Tensor cores for bf16 q and K with grouped-query heads.
-inline bool mass_uses_mma(bool kv_bf16, bool q_bf16, int group) {
+bool mass_uses_tensor_cores(bool kv_bf16, bool q_bf16, int group) {
   return kv_bf16 && q_bf16 && group >= 2;
 }
 
@@ -539,7 +552,7 @@ R with_mass_kernel(int head_dim, int group, bool kv_bf16, bool q_bf16, F f, R fa
     using Tl = MassTiling<DD, KV, GG>;                                                  \
     return f(mass_kernel<DD, KV, GG>, Tl::kSmem, Tl::NW * 32, Tl::NW * Tl::T);          \
   }
-  if (mass_uses_mma(kv_bf16, q_bf16, group)) {
+  if (mass_uses_tensor_cores(kv_bf16, q_bf16, group)) {
     DSA_MMA_CASE(64, 2)
     DSA_MMA_CASE(64, 4)
     DSA_MMA_CASE(64, 8)
