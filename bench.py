@@ -106,6 +106,9 @@ def parse_args():
     p.add_argument("--sparse-cluster", type=int, default=-1,
                    help="CTAs per thread-block cluster of sparse decode (0: chosen per call, "
                         "default: the library's setting)")
+    p.add_argument("--sweep-sparsity", action="store_true",
+                   help="no headline line: time the fused sparse step against dense decode "
+                        "over a range of windows and mask densities (one JSON line each)")
     p.add_argument("--batch", type=int, default=0,
                    help="with --profile: override the workload's batch size")
     return p.parse_args()
@@ -640,9 +643,78 @@ def run_profile(args):
                       "launches": args.warmup + args.steps}), flush=True)
 
 
+def run_sparsity_sweep(args):
+    """Speedup of the sparse step over dense decode as the kept fraction varies.
+
+    The Janus-Pro-7B-like batch (64 requests, 32 heads, head_dim 128, prompt 256,
+    L = P + U[64, 1024]) with per-(request, head) random masks: the band 1..8
+    always kept, every other window offset kept with probability p; the window
+    W and p are swept.  Each point: the fused step and the dense decode of the
+    same batch, CUDA-graph timed over KV copies larger than 4x L2."""
+    device = torch.device("cuda", 0)
+    base = wl.WORKLOADS["janus-pro-7b"]
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    stream = torch.cuda.Stream(device)
+    torch.cuda.set_stream(stream)
+    K = max(10, min(args.steps, 100))
+    for W in (32, 96, 256, 512, 1024):
+        for p in (0.0, 0.25, 1.0):
+            cfg = wl.scaled(base, window_rows=None, window=W, random_frac=(p, p),
+                            seed=base.seed + 17)
+            w = wl.generate(cfg, device=str(device))
+            bt = DecodeBatch.from_workload(w, device=device)
+            bt.build_index()
+            torch.cuda.synchronize()
+            kept = bt.kept_cnt.cpu().numpy()
+            by = step_bytes(w, bt.kept_idx.cpu().numpy(), kept)
+            dense_bytes = by["dense"]
+            pool = bt.k_pages.numel() * bt.k_pages.element_size() * 2
+            free, _ = torch.cuda.mem_get_info(device)
+            R = int(max(1, min(math.ceil(4 * l2 / max(by["kv"], 1)), 32, (0.5 * free) // pool)))
+            pools = [(bt.k_pages, bt.v_pages)] + [(bt.k_pages.clone(), bt.v_pages.clone())
+                                                  for _ in range(R - 1)]
+            d = bt.dims
+            out_d = torch.empty_like(bt.out)
+            lse_d = torch.empty_like(bt.lse)
+
+            def fused(k):
+                kp, vp = pools[k % R]
+                dsa.dsa_decode_sparse_masked(d, bt.q, kp, vp, bt.page_table, bt.seq_len,
+                                             bt.prompt_len, bt.window, bt.keep_mask, bt.scale,
+                                             bt.out, bt.lse, bt.ws, stream)
+
+            def dense(k):
+                kp, vp = pools[k % R]
+                dsa.dsa_decode_dense(d, bt.q, kp, vp, bt.page_table, bt.seq_len, bt.scale,
+                                     out_d, lse_d, bt.ws, stream)
+
+            for k in range(3):
+                fused(k)
+                dense(k)
+            torch.cuda.synchronize()
+            bt.check("sweep warm-up")
+            gf, gd = graph_of(fused, K, stream), graph_of(dense, K, stream)
+            gf.replay()
+            gd.replay()
+            tf = time_graph(gf, stream) / K
+            td = time_graph(gd, stream) / K
+            bt.check("sweep")
+            frac = by["rows"] / by["dense_rows"]
+            print(json.dumps({
+                "sweep": "sparsity", "workload": cfg.name, "window": W, "keep_p": p,
+                "kept_fraction": frac, "fused_us": 1e6 * tf, "dense_us": 1e6 * td,
+                "speedup": td / tf, "ideal_speedup": 1.0 / frac,
+                "fused_gbs": by["masked"] / tf / 1e9, "dense_gbs": dense_bytes / td / 1e9,
+            }), flush=True)
+            del pools, bt, w, gf, gd
+            torch.cuda.empty_cache()
+
+
 def main():
     args = parse_args()
-    if args.profile:
+    if args.sweep_sparsity:
+        run_sparsity_sweep(args)
+    elif args.profile:
         run_profile(args)
     elif args.impl == "reference":
         run_reference(args)

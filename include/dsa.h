@@ -175,6 +175,14 @@ dsa_status dsa_decode_sparse(const dsa_dims* dims, const void* q, const void* k_
  *                     outside 0..batch-1 sets DSA_DEV_BAD_ORDER and is
  *                     skipped; a request missing from a non-permutation is
  *                     left unspecified.
+ *   k_new, v_new      [batch][hkv][head_dim] (kv_dtype, device, 16-byte
+ *                     aligned), or both NULL: the K and V rows of the query
+ *                     token L_b - 1, appended by this call -- attention reads
+ *                     row L_b - 1 from here, and the call stores it into
+ *                     k_pages / v_pages at page_table[b][(L_b-1)/16], slot
+ *                     (L_b-1)%16, for later steps (the page must be mapped;
+ *                     else DSA_DEV_BAD_PAGE).  With NULL the cache must
+ *                     already hold row L_b - 1 and is only read.
  * max_window must be <= 1024 (each warp holds the window's mask bits, one
  * 32-bit word per lane), else DSA_ERR_UNSUPPORTED: use the two calls then.  Invalid per-request data
  * (the DSA_DEV_BAD_SEQ_LEN / _PROMPT / _WINDOW / _COUNT cases of
@@ -182,12 +190,13 @@ dsa_status dsa_decode_sparse(const dsa_dims* dims, const void* q, const void* k_
  * and lse rows of the affected kv head.  The workspace also holds the kept
  * count of every (request, kv head) for the LSE merge of split work.
  */
-dsa_status dsa_decode_sparse_masked(const dsa_dims* dims, const void* q, const void* k_pages,
-                                    const void* v_pages, const int32_t* page_table,
+dsa_status dsa_decode_sparse_masked(const dsa_dims* dims, const void* q, void* k_pages,
+                                    void* v_pages, const int32_t* page_table,
                                     const int32_t* seq_len, const int32_t* prompt_len,
                                     const int32_t* window, const uint32_t* keep_mask,
-                                    const int32_t* request_order, float scale, float* out,
-                                    float* lse, void* ws, void* stream);
+                                    const int32_t* request_order, const void* k_new,
+                                    const void* v_new, float scale, float* out, float* lse,
+                                    void* ws, void* stream);
 
 /*
  * dsa_decode_dense -- the dense causal baseline: the same as dsa_decode_sparse

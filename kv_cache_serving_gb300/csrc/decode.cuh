@@ -207,6 +207,30 @@ __global__ void __launch_bounds__(NWARPS * 32) decode_kernel(const DecodeLaunch 
     }
     return;
   }
+  // Append: row L-1 (the query token) comes from k_new / v_new; the first CTA
+  // of the unit also stores it into its page slot for later steps.  No CTA of
+  // this launch reads that slot, so the store needs no ordering with the copies.
+  const KV* knew = a.k_new != nullptr
+                       ? reinterpret_cast<const KV*>(a.k_new) + (static_cast<size_t>(b) * a.hkv + hk) * D
+                       : nullptr;
+  const KV* vnew = a.v_new != nullptr
+                       ? reinterpret_cast<const KV*>(a.v_new) + (static_cast<size_t>(b) * a.hkv + hk) * D
+                       : nullptr;
+  if (knew != nullptr && c == 0 && warp == 0) {
+    int pg = __ldg(a.page_table + static_cast<size_t>(b) * a.max_pages + ((L - 1) >> 4));
+    if (static_cast<unsigned>(pg) >= static_cast<unsigned>(a.num_pages)) {
+      if (lane == 0) set_error(a.err, DSA_DEV_BAD_PAGE);
+    } else {
+      const size_t off = ((static_cast<size_t>(pg) * kPage + ((L - 1) & (kPage - 1))) * a.hkv + hk) * D;
+      constexpr int kVec = Tl::kRowBytes / 16;  // 16-byte vectors per row
+      uint4* kd = reinterpret_cast<uint4*>(const_cast<void*>(a.k)) + off * sizeof(KV) / 16;
+      uint4* vd = reinterpret_cast<uint4*>(const_cast<void*>(a.v)) + off * sizeof(KV) / 16;
+      for (int v = lane; v < 2 * kVec; v += 32) {
+        if (v < kVec) kd[v] = __ldg(reinterpret_cast<const uint4*>(knew) + v);
+        else vd[v - kVec] = __ldg(reinterpret_cast<const uint4*>(vnew) + v - kVec);
+      }
+    }
+  }
   // Rows of this CTA.  Cluster mode: the a.cluster CTAs of a cluster split the
   // unit's rows evenly (tile-aligned) and every one of them reaches the cluster
   // merge, rows or not.  Otherwise: fixed chunks, partials merged by merge_kernel.
@@ -305,8 +329,11 @@ __global__ void __launch_bounds__(NWARPS * 32) decode_kernel(const DecodeLaunch 
       }
       const size_t off = ((static_cast<size_t>(pg) * kPage + (j & (kPage - 1))) * a.hkv + hk) * D;
       const size_t dst = (static_cast<size_t>(stage) * T + my_r) * kRowStride;
-      if (T == 32 || lane < T) bulk_copy_g2s(kst + dst, kg + off, kRowBytes, &bars[stage]);
-      if (T == 32 || lane >= T) bulk_copy_g2s(vst + dst, vg + off, kRowBytes, &bars[stage]);
+      const bool fresh = knew != nullptr && j == L - 1;  // the appended row
+      if (T == 32 || lane < T)
+        bulk_copy_g2s(kst + dst, fresh ? knew : kg + off, kRowBytes, &bars[stage]);
+      if (T == 32 || lane >= T)
+        bulk_copy_g2s(vst + dst, fresh ? vnew : vg + off, kRowBytes, &bars[stage]);
     }
   };
 

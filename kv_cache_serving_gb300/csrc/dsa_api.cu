@@ -209,6 +209,8 @@ struct RowSource {
   const int32_t* window = nullptr;
   const uint32_t* keep_mask = nullptr;
   const int32_t* order = nullptr;
+  const void* k_new = nullptr;
+  const void* v_new = nullptr;
 };
 
 dsa_status decode_common(const dsa_dims* d, int mode, const void* q, const void* k,
@@ -222,6 +224,9 @@ dsa_status decode_common(const dsa_dims* d, int mode, const void* q, const void*
   if (mode == kModeMask && (!rs.prompt_len || !rs.window || !rs.keep_mask))
     return DSA_ERR_INVALID_ARG;
   if (mode == kModeMask && d->max_window > kMaskModeMaxWindow) return DSA_ERR_UNSUPPORTED;
+  if ((rs.k_new == nullptr) != (rs.v_new == nullptr)) return DSA_ERR_INVALID_ARG;
+  if (rs.k_new != nullptr && (!aligned(rs.k_new, 16) || !aligned(rs.v_new, 16)))
+    return DSA_ERR_INVALID_ARG;
   if (!(scale == scale) || !aligned(ws, 256) || !aligned(k, 16) || !aligned(v, 16) ||
       !aligned(q, 16))
     return DSA_ERR_INVALID_ARG;
@@ -242,6 +247,8 @@ dsa_status decode_common(const dsa_dims* d, int mode, const void* q, const void*
   a.keep_mask = rs.keep_mask;
   a.unit_rows = mode == kModeMask ? unit_rows(d, ws) : nullptr;
   a.order = rs.order;
+  a.k_new = rs.k_new;
+  a.v_new = rs.v_new;
   a.max_window = d->max_window;
   a.mask_words = d->mask_words;
   a.batch = d->batch;
@@ -332,17 +339,20 @@ dsa_status dsa_decode_sparse(const dsa_dims* dims, const void* q, const void* k_
                        lse, ws, stream);
 }
 
-dsa_status dsa_decode_sparse_masked(const dsa_dims* dims, const void* q, const void* k_pages,
-                                    const void* v_pages, const int32_t* page_table,
+dsa_status dsa_decode_sparse_masked(const dsa_dims* dims, const void* q, void* k_pages,
+                                    void* v_pages, const int32_t* page_table,
                                     const int32_t* seq_len, const int32_t* prompt_len,
                                     const int32_t* window, const uint32_t* keep_mask,
-                                    const int32_t* request_order, float scale, float* out,
-                                    float* lse, void* ws, void* stream) {
+                                    const int32_t* request_order, const void* k_new,
+                                    const void* v_new, float scale, float* out, float* lse,
+                                    void* ws, void* stream) {
   RowSource rs;
   rs.prompt_len = prompt_len;
   rs.window = window;
   rs.keep_mask = keep_mask;
   rs.order = request_order;
+  rs.k_new = k_new;
+  rs.v_new = v_new;
   return decode_common(dims, kModeMask, q, k_pages, v_pages, page_table, seq_len, rs, scale, out,
                        lse, ws, stream);
 }

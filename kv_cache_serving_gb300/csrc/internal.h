@@ -29,6 +29,8 @@ struct DecodeLaunch {
   const uint32_t* keep_mask;  // kRowsMask only: [batch][hkv][mask_words]
   int32_t* unit_rows;         // kRowsMask only: [batch][hkv] kept count or -error
   const int32_t* order;       // [batch] request scheduled at each grid z, or null (z itself)
+  const void* k_new;          // [batch][hkv][head_dim] K/V of row seq_len-1, or null (the
+  const void* v_new;          //   cache already holds it); written into its page slot
   int32_t batch, hq, hkv, head_dim, max_pages, num_pages, max_kept;
   int32_t max_window, mask_words;  // kRowsMask only
   int32_t chunk, num_chunks;

@@ -65,7 +65,7 @@ def _load():
         "dsa_workspace_size": ([D], SZ),
         "dsa_build_index": ([D, P, P, P, P, P, P, P, P], I32),
         "dsa_decode_sparse": ([D, P, P, P, P, P, P, P, F32, P, P, P, P], I32),
-        "dsa_decode_sparse_masked": ([D, P, P, P, P, P, P, P, P, P, F32, P, P, P, P], I32),
+        "dsa_decode_sparse_masked": ([D, P, P, P, P, P, P, P, P, P, P, P, F32, P, P, P, P], I32),
         "dsa_decode_dense": ([D, P, P, P, P, P, F32, P, P, P, P], I32),
         "dsa_attention_mass": ([D, P, P, P, P, P, P, P, I32, I32, F32, P, P, P, P], I32),
         "dsa_decode_plan": ([D, I32, ctypes.POINTER(I32), ctypes.POINTER(I32),
@@ -170,16 +170,20 @@ def dsa_decode_sparse(dims, q, k_pages, v_pages, page_table, seq_len, kept_idx, 
 
 
 def dsa_decode_sparse_masked(dims, q, k_pages, v_pages, page_table, seq_len, prompt_len, window,
-                             keep_mask, scale, out, lse, ws, stream=None, request_order=None):
+                             keep_mask, scale, out, lse, ws, stream=None, request_order=None,
+                             k_new=None, v_new=None):
     """dsa_build_index + dsa_decode_sparse in one call: the kernels read each
     (request, kv head)'s kept set from the mask themselves.  request_order
-    (int32 [batch] CUDA tensor or None) is the order requests are scheduled in."""
+    (int32 [batch] CUDA tensor or None) is the order requests are scheduled in;
+    k_new / v_new ([batch, hkv, head_dim] CUDA tensors or None) append the query
+    token's K/V row to the cache in the same call."""
     _check(_load().dsa_decode_sparse_masked(
         ctypes.byref(dims), _ptr(q, _QKV, "q"), _ptr(k_pages, _QKV, "k_pages"),
         _ptr(v_pages, _QKV, "v_pages"), _ptr(page_table, _I32, "page_table"),
         _ptr(seq_len, _I32, "seq_len"), _ptr(prompt_len, _I32, "prompt_len"),
         _ptr(window, _I32, "window"), _ptr(keep_mask, _MASK, "keep_mask"),
-        _ptr(request_order, _I32, "request_order"), float(scale),
+        _ptr(request_order, _I32, "request_order"), _ptr(k_new, _QKV, "k_new"),
+        _ptr(v_new, _QKV, "v_new"), float(scale),
         _ptr(out, torch.float32, "out"), _ptr(lse, torch.float32, "lse"), _ptr(ws),
         _stream(stream)), "dsa_decode_sparse_masked")
 

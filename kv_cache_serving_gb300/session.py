@@ -136,13 +136,14 @@ class DecodeBatch:
                               self.ws, stream)
         return out, lse
 
-    def decode_sparse_masked(self, out=None, lse=None, stream=None, request_order=None):
+    def decode_sparse_masked(self, out=None, lse=None, stream=None, request_order=None,
+                             k_new=None, v_new=None):
         out = self.out if out is None else out
         lse = self.lse if lse is None else lse
         dsa.dsa_decode_sparse_masked(self.dims, self.q, self.k_pages, self.v_pages,
                                      self.page_table, self.seq_len, self.prompt_len, self.window,
                                      self.keep_mask, self.scale, out, lse, self.ws, stream,
-                                     request_order)
+                                     request_order, k_new, v_new)
         return out, lse
 
     def longest_first_order(self):

@@ -102,10 +102,16 @@ def test_null_pointers_rejected_before_launch():
                                 ctypes.c_void_p((1 << 20) + 8), None) == dsa.DSA_ERR_INVALID_ARG
     # masked decode: a missing keep mask, then a window too long for the in-kernel list
     assert lib.dsa_decode_sparse_masked(D, fake, fake, fake, fake, fake, fake, fake, None, None,
-                                        0.1, fake, None, fake, None) == dsa.DSA_ERR_INVALID_ARG
+                                        None, None, 0.1, fake, None, fake,
+                                        None) == dsa.DSA_ERR_INVALID_ARG
+    # an appended K row without its V row
+    assert lib.dsa_decode_sparse_masked(D, fake, fake, fake, fake, fake, fake, fake, fake, None,
+                                        fake, None, 0.1, fake, None, fake,
+                                        None) == dsa.DSA_ERR_INVALID_ARG
     big = dsa.make_dims(2, 8, 4, 128, 10, 4, 1025, 33, 50, "bf16", "bf16")
     assert lib.dsa_decode_sparse_masked(ctypes.byref(big), fake, fake, fake, fake, fake, fake,
-                                        fake, fake, None, 0.1, fake, None, fake, None) == \
+                                        fake, fake, None, None, None, 0.1, fake, None, fake,
+                                        None) == \
         dsa.DSA_ERR_UNSUPPORTED
     assert lib.dsa_decode_plan(ctypes.byref(d), 3, None, None, None, None) == \
         dsa.DSA_ERR_INVALID_ARG

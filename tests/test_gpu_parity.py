@@ -291,6 +291,39 @@ def test_large_window_many_mask_words():
     run_both(w)
 
 
+@pytest.mark.parametrize("name,batch", [("llamagen-xl", 6), ("mixed-serving", 8),
+                                        ("janus-pro-7b", 4)])
+def test_fused_append_of_the_query_row(name, batch):
+    """k_new / v_new: the call attends with the new row and stores it in the
+    cache.  Reference: the same batch whose cache already holds the row (the
+    oracle's input) -- same outputs bit for bit, and the cache afterwards
+    equals that reference cache."""
+    w = wl.generate(wl.scaled(wl.WORKLOADS[name], batch=batch))
+    if w["keep_mask"] is None:
+        w["keep_mask"] = top_mass_masks_from_oracle(w)
+    ref_bt = DecodeBatch.from_workload(w)
+    ref_out, ref_lse = [t.clone() for t in ref_bt.decode_sparse_masked()]
+    # the new rows, then a cache whose rows L-1 hold garbage
+    B, Hkv, D = w["batch"], w["hkv"], w["head_dim"]
+    k_new = torch.empty((B, Hkv, D), dtype=ref_bt.k_pages.dtype, device="cuda")
+    v_new = torch.empty_like(k_new)
+    bt = DecodeBatch.from_workload(w)
+    for b in range(B):
+        j = int(w["seq_len"][b]) - 1
+        pg, slot = int(w["page_table"][b, j // 16]), j % 16
+        k_new[b] = bt.k_pages[pg, slot]
+        v_new[b] = bt.v_pages[pg, slot]
+        bt.k_pages[pg, slot] = float("nan")
+        bt.v_pages[pg, slot] = 1e30
+    out, lse = bt.decode_sparse_masked(k_new=k_new, v_new=v_new)
+    torch.cuda.synchronize()
+    assert bt.device_error() == 0
+    assert torch.equal(out, ref_out) and torch.equal(lse, ref_lse)
+    assert torch.equal(bt.k_pages, ref_bt.k_pages) and torch.equal(bt.v_pages, ref_bt.v_pages)
+    ref_o, ref_l = oracle.decode(w, sparse=True)
+    assert_outputs(out.cpu().numpy(), ref_o, fp32=False)
+
+
 # ---------------------------------------------------------------------------
 # attention mass
 # ---------------------------------------------------------------------------
