@@ -71,6 +71,8 @@ def _load():
         i32, p, d = ctypes.c_int32, ctypes.c_void_p, ctypes.c_double
         lib.oracle_kept_set.argtypes = [i32, i32, i32, p, p]
         lib.oracle_kept_set.restype = i32
+        lib.oracle_evictable_pages.argtypes = [i32, i32, i32, p]
+        lib.oracle_evictable_pages.restype = i32
         lib.oracle_mask_matrix.argtypes = [i32, i32, i32, i32, p]
         lib.oracle_mask_matrix.restype = None
         lib.oracle_sparsity.argtypes = [i32, p]
@@ -105,6 +107,16 @@ def kept_set(L: int, P: int, W: int, mask_words) -> np.ndarray:
     if n < 0:
         raise ValueError(f"oracle_kept_set rejected L={L} P={P} W={W}")
     return out[:n].copy()
+
+
+def evictable_pages(L: int, P: int, W: int) -> np.ndarray:
+    """bool[ceil(L/16)]: pages of a request that no later decode step reads."""
+    lib = _load()
+    flags = np.zeros(max((L + 15) // 16, 1), dtype=np.uint8)
+    n = lib.oracle_evictable_pages(L, P, W, _ptr(flags))
+    if n < 0:
+        raise ValueError(f"oracle_evictable_pages rejected L={L} P={P} W={W}")
+    return flags[:(L + 15) // 16].astype(bool)
 
 
 def mask_matrix(N: int, W: int, B: int, causal: bool = False) -> np.ndarray:

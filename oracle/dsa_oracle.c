@@ -96,6 +96,28 @@ int32_t oracle_kept_set(int32_t L, int32_t P, int32_t W, const uint32_t* mask,
 }
 
 /* ---------------------------------------------------------------------------
+ * Pages that no later decode step can read [DAS-formula], [DAS-abstract]:
+ * the kept set of any query i' >= i = L-1 holds prompt rows and rows of its
+ * window i'-W .. i', so a row j with P <= j < i - W lies below every later
+ * window and outside the prompt: it is never read again (reading: P and W of
+ * a request stay fixed while it decodes).  Page p holds rows 16p .. 16p+15;
+ * flags[p] = 1 when every one of them is such a row, for the ceil(L/16) pages
+ * a request of length L maps.  Returns the count, or OR_BAD_REQUEST.
+ * ------------------------------------------------------------------------- */
+int32_t oracle_evictable_pages(int32_t L, int32_t P, int32_t W, uint8_t* flags) {
+  if (L < 1 || P < 0 || W < 0) return OR_BAD_REQUEST;
+  int32_t i = L - 1, pages = (L + OR_PAGE - 1) / OR_PAGE, count = 0;
+  for (int32_t p = 0; p < pages; ++p) {
+    int never = 1;
+    for (int32_t j = p * OR_PAGE; j < (p + 1) * OR_PAGE; ++j)
+      if (!(j >= P && j < i - W)) never = 0;
+    flags[p] = (uint8_t)never;
+    count += never;
+  }
+  return count;
+}
+
+/* ---------------------------------------------------------------------------
  * The summary's literal N x N mask [DAS-formula]: M_ij = 1 iff |i-j| <= B and
  * j >= i-W.  With causal != 0 the entries j > i are also cleared (decode).
  * ------------------------------------------------------------------------- */

@@ -361,3 +361,34 @@ def test_mass_vs_torch_softmax():
             for o in range(inp["max_window"] + 1):
                 want = a[i - o] if (o <= W and o <= i) else 0.0
                 assert abs(om[t, o] - want) < 1e-12
+
+
+# ---------------------------------------------------------------------------
+# evictable pages: rows no later decode step can read
+# ---------------------------------------------------------------------------
+
+def test_evictable_pages_against_future_kept_sets():
+    """A page is evictable exactly when no kept set of the current or any later
+    query (i' = L-1, L, ..., with every window bit set: the largest kept set)
+    contains one of its rows -- checked by brute force over later queries."""
+    rng = np.random.default_rng(41)
+    for _ in range(150):
+        L = int(rng.integers(1, 700))
+        P = int(rng.integers(0, 300))
+        W = int(rng.integers(0, 200))
+        ones = np.full((W + 31) // 32 + 1, 0xFFFFFFFF, dtype=np.uint32)
+        read_again = set()
+        for Lf in range(L, L + W + 40):
+            read_again.update(oracle.kept_set(Lf, P, W, ones).tolist())
+        want = np.array([not any(j in read_again for j in range(16 * p, 16 * p + 16))
+                         for p in range((L + 15) // 16)], dtype=bool)
+        assert np.array_equal(oracle.evictable_pages(L, P, W), want), (L, P, W)
+
+
+@pytest.mark.parametrize("L,P,W", [(100, 20, 30), (8100, 64, 360), (16, 0, 0), (500, 600, 10),
+                                   (1, 0, 5), (257, 0, 0)])
+def test_evictable_page_count_closed_form(L, P, W):
+    """Pages strictly after the prompt's last page and ending before row L-1-W:
+    max(0, floor((L-1-W)/16) - ceil(P/16))."""
+    want = max(0, (L - 1 - W) // 16 - (P + 15) // 16)
+    assert int(oracle.evictable_pages(L, P, W).sum()) == want
