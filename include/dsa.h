@@ -85,7 +85,8 @@ enum {
   DSA_DEV_BAD_COUNT = 6,    /* kept count < 1 or > max_kept                */
   DSA_DEV_TIMEOUT = 7,      /* a bounded wait for an async copy gave up    */
   DSA_DEV_BAD_GRID_W = 8,   /* grid width < 1 (attention mass)             */
-  DSA_DEV_BAD_ORDER = 9     /* request_order entry outside 0..batch-1      */
+  DSA_DEV_BAD_ORDER = 9,    /* request_order entry outside 0..batch-1      */
+  DSA_DEV_FREE_LIST_FULL = 10 /* dsa_evict_pages: more pages than capacity   */
 };
 
 /* Problem sizes, shared by all calls on one KV cache. */
@@ -231,6 +232,34 @@ dsa_status dsa_attention_mass(const dsa_dims* dims, const void* q, const void* k
                               const int32_t* grid_w, int32_t r_local, int32_t r_diag,
                               float scale, float* mass, float* offset_mass, void* ws,
                               void* stream);
+
+/*
+ * dsa_evict_pages -- unmap the pages no later decode step can read, and hand
+ * them back for reuse: the memory side of the method (its kept set reads only
+ * the prompt and a window that moves forward; arXiv abstract: the other KV
+ * entries are skipped), so a long request keeps about P + W + 16 rows resident
+ * instead of L.  A page of request b holding rows 16p .. 16p+15 is evicted when
+ * every row j of it satisfies P_b <= j < (L_b - 1) - W_b (P_b and W_b taken as
+ * fixed while the request decodes); such rows are outside the kept set of the
+ * current query and of every later one, for any keep mask.
+ *   seq_len, prompt_len, window  [batch] int32 (device), as in dsa_build_index
+ *   page_table   [batch][max_pages_per_req] int32 (device, updated in place):
+ *                evicted entries become -1; entries already -1 are skipped
+ *   freed_pages  [capacity] int32 (device, out): the evicted page ids, in no
+ *                particular order, from index *freed_count (as it was) on
+ *   freed_count  one int32 (device, in/out): entries already in freed_pages;
+ *                advanced by the number of pages evicted
+ *   capacity     size of freed_pages (>= 0)
+ * A page that finds the list full stays mapped and sets DSA_DEV_FREE_LIST_FULL
+ * (freed_count may then exceed capacity: only the first `capacity` entries are
+ * written).  Invalid sizes set DSA_DEV_BAD_SEQ_LEN / _PROMPT / _WINDOW and leave
+ * that request's pages alone.  The decode calls never read evicted rows, so a
+ * batch decodes the same after eviction.
+ */
+dsa_status dsa_evict_pages(const dsa_dims* dims, const int32_t* seq_len,
+                           const int32_t* prompt_len, const int32_t* window, int32_t* page_table,
+                           int32_t* freed_pages, int32_t* freed_count, int32_t capacity, void* ws,
+                           void* stream);
 
 /*
  * dsa_decode_plan -- how a decode call will split its work on the CURRENT

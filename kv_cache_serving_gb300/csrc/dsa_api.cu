@@ -327,6 +327,31 @@ dsa_status dsa_build_index(const dsa_dims* dims, const int32_t* seq_len,
   return from_cuda(launch_compact(a, static_cast<cudaStream_t>(stream)));
 }
 
+dsa_status dsa_evict_pages(const dsa_dims* dims, const int32_t* seq_len,
+                           const int32_t* prompt_len, const int32_t* window, int32_t* page_table,
+                           int32_t* freed_pages, int32_t* freed_count, int32_t capacity, void* ws,
+                           void* stream) {
+  const dsa_status st = check_dims(dims);
+  if (st != DSA_OK) return st;
+  if (!seq_len || !prompt_len || !window || !page_table || !freed_count || !ws || capacity < 0 ||
+      (capacity > 0 && !freed_pages))
+    return DSA_ERR_INVALID_ARG;
+  if (!aligned(ws, 256)) return DSA_ERR_INVALID_ARG;
+  EvictLaunch a{};
+  a.seq_len = seq_len;
+  a.prompt_len = prompt_len;
+  a.window = window;
+  a.page_table = page_table;
+  a.freed = freed_pages;
+  a.freed_count = freed_count;
+  a.batch = dims->batch;
+  a.max_pages = dims->max_pages_per_req;
+  a.max_window = dims->max_window;
+  a.capacity = capacity;
+  a.err = err_word(ws);
+  return from_cuda(launch_evict(a, static_cast<cudaStream_t>(stream)));
+}
+
 dsa_status dsa_decode_sparse(const dsa_dims* dims, const void* q, const void* k_pages,
                              const void* v_pages, const int32_t* page_table,
                              const int32_t* seq_len, const int32_t* kept_idx,

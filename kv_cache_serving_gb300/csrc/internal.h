@@ -73,6 +73,17 @@ struct CompactLaunch {
   int32_t* err;
 };
 
+struct EvictLaunch {
+  const int32_t* seq_len;
+  const int32_t* prompt_len;
+  const int32_t* window;
+  int32_t* page_table;   // [batch][max_pages], evicted entries set to -1
+  int32_t* freed;        // [capacity] freed page ids
+  int32_t* freed_count;  // appended to atomically
+  int32_t batch, max_pages, max_window, capacity;
+  int32_t* err;
+};
+
 // Row sources of a decode launch (`mode` below).
 constexpr int kModeDense = 0;  // rows 0..L-1
 constexpr int kModeList = 1;   // kept_idx / kept_cnt from dsa_build_index
@@ -94,6 +105,7 @@ int mass_rows_per_pass(int head_dim, int group, bool kv_bf16, bool q_bf16);
 bool mass_uses_tensor_cores(bool kv_bf16, bool q_bf16, int group);
 int mass_ctas_per_sm(int head_dim, int group, bool kv_bf16, bool q_bf16);
 cudaError_t launch_compact(const CompactLaunch& a, cudaStream_t s);
+cudaError_t launch_evict(const EvictLaunch& a, cudaStream_t s);
 
 // Warps per CTA of the second build of the fused call (bf16 KV), chosen for
 // batches of many units; must match DSA_DECODE_WARPS_BIG in decode.cuh.

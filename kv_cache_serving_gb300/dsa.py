@@ -65,6 +65,7 @@ def _load():
         "dsa_workspace_size": ([D], SZ),
         "dsa_build_index": ([D, P, P, P, P, P, P, P, P], I32),
         "dsa_decode_sparse": ([D, P, P, P, P, P, P, P, F32, P, P, P, P], I32),
+        "dsa_evict_pages": ([D, P, P, P, P, P, P, I32, P, P], I32),
         "dsa_decode_sparse_masked": ([D, P, P, P, P, P, P, P, P, P, P, P, F32, P, P, P, P], I32),
         "dsa_decode_dense": ([D, P, P, P, P, P, F32, P, P, P, P], I32),
         "dsa_attention_mass": ([D, P, P, P, P, P, P, P, I32, I32, F32, P, P, P, P], I32),
@@ -157,6 +158,19 @@ def dsa_build_index(dims, seq_len, prompt_len, window, keep_mask, kept_idx, kept
         _ptr(window, _I32, "window"), _ptr(keep_mask, _MASK, "keep_mask"),
         _ptr(kept_idx, _I32, "kept_idx"), _ptr(kept_cnt, _I32, "kept_cnt"), _ptr(ws), _stream(stream)),
         "dsa_build_index")
+
+
+def dsa_evict_pages(dims, seq_len, prompt_len, window, page_table, freed_pages, freed_count, ws,
+                    stream=None):
+    """Unmap (set to -1) the page-table entries no later decode step reads and
+    append their page ids to freed_pages (int32 CUDA tensor) from freed_count
+    (one-element int32 CUDA tensor) on."""
+    cap = 0 if freed_pages is None else int(freed_pages.numel())
+    _check(_load().dsa_evict_pages(
+        ctypes.byref(dims), _ptr(seq_len, _I32, "seq_len"), _ptr(prompt_len, _I32, "prompt_len"),
+        _ptr(window, _I32, "window"), _ptr(page_table, _I32, "page_table"),
+        _ptr(freed_pages, _I32, "freed_pages"), _ptr(freed_count, _I32, "freed_count"), cap,
+        _ptr(ws), _stream(stream)), "dsa_evict_pages")
 
 
 def dsa_decode_sparse(dims, q, k_pages, v_pages, page_table, seq_len, kept_idx, kept_cnt, scale,

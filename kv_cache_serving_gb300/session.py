@@ -128,6 +128,16 @@ class DecodeBatch:
         dsa.dsa_build_index(self.dims, self.seq_len, self.prompt_len, self.window, self.keep_mask,
                             self.kept_idx, self.kept_cnt, self.ws, stream)
 
+    def evict_pages(self, capacity=None, stream=None):
+        """Unmap the pages no later step reads; returns (freed page ids tensor,
+        count tensor) -- the ids are valid up to min(count, capacity)."""
+        cap = self.page_table.numel() if capacity is None else capacity
+        freed = torch.full((max(cap, 1),), -1, dtype=torch.int32, device=self.device)
+        count = torch.zeros(1, dtype=torch.int32, device=self.device)
+        dsa.dsa_evict_pages(self.dims, self.seq_len, self.prompt_len, self.window, self.page_table,
+                            freed[:cap] if cap > 0 else None, count, self.ws, stream)
+        return freed, count
+
     def decode_sparse(self, out=None, lse=None, stream=None):
         out = self.out if out is None else out
         lse = self.lse if lse is None else lse

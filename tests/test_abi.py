@@ -115,5 +115,10 @@ def test_null_pointers_rejected_before_launch():
         dsa.DSA_ERR_UNSUPPORTED
     assert lib.dsa_decode_plan(ctypes.byref(d), 3, None, None, None, None) == \
         dsa.DSA_ERR_INVALID_ARG
+    # eviction: a missing free-list counter, a negative capacity
+    assert lib.dsa_evict_pages(D, fake, fake, fake, fake, fake, None, 4, fake,
+                               None) == dsa.DSA_ERR_INVALID_ARG
+    assert lib.dsa_evict_pages(D, fake, fake, fake, fake, fake, fake, -1, fake,
+                               None) == dsa.DSA_ERR_INVALID_ARG
     code = ctypes.c_int32(0)
     assert lib.dsa_get_device_error(None, None, ctypes.byref(code)) == dsa.DSA_ERR_INVALID_ARG

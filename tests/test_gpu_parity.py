@@ -324,6 +324,65 @@ def test_fused_append_of_the_query_row(name, batch):
     assert_outputs(out.cpu().numpy(), ref_o, fp32=False)
 
 
+@pytest.mark.parametrize("name,batch", [("emu3-8b", 8), ("mixed-serving", 24),
+                                        ("llamagen-xl", 8)])
+def test_evict_pages_then_decode_unchanged(name, batch):
+    """dsa_evict_pages unmaps exactly the pages the oracle marks, hands back
+    exactly their ids, frees nothing more when repeated, and the sparse decode
+    calls give the same bits on the evicted cache (they never read those rows)."""
+    w = wl.generate(wl.scaled(wl.WORKLOADS[name], batch=batch))
+    if w["keep_mask"] is None:
+        w["keep_mask"] = top_mass_masks_from_oracle(w)
+    bt = DecodeBatch.from_workload(w)
+    bt.build_index()
+    before = [t.clone() for t in bt.decode_sparse()] + \
+             [t.clone() for t in bt.decode_sparse_masked(out=torch.empty_like(bt.out),
+                                                         lse=torch.empty_like(bt.lse))]
+    table0 = bt.page_table.cpu().numpy().copy()
+    freed, count = bt.evict_pages()
+    torch.cuda.synchronize()
+    assert bt.device_error() == 0
+    table1 = bt.page_table.cpu().numpy()
+    want_ids = []
+    for b in range(batch):
+        flags = oracle.evictable_pages(int(w["seq_len"][b]), int(w["prompt_len"][b]),
+                                       int(w["window"][b]))
+        npg = len(flags)
+        assert np.array_equal(table1[b, :npg] == -1, flags), b
+        assert np.array_equal(table1[b, npg:], table0[b, npg:])
+        want_ids += table0[b, :npg][flags].tolist()
+    n = int(count.item())
+    assert n == len(want_ids)
+    assert sorted(freed[:n].cpu().tolist()) == sorted(want_ids)
+    # again: nothing left to free
+    freed2, count2 = bt.evict_pages()
+    torch.cuda.synchronize()
+    assert int(count2.item()) == 0 and bt.device_error() == 0
+    # decode on the evicted cache: same bits
+    bt.build_index()
+    after = [t.clone() for t in bt.decode_sparse()] + \
+            [t.clone() for t in bt.decode_sparse_masked(out=torch.empty_like(bt.out),
+                                                        lse=torch.empty_like(bt.lse))]
+    torch.cuda.synchronize()
+    assert bt.device_error() == 0
+    for x, y in zip(before, after):
+        assert torch.equal(x, y)
+
+
+def test_evict_pages_free_list_full():
+    w = wl.generate(wl.scaled(wl.WORKLOADS["emu3-8b"], batch=4))
+    bt = DecodeBatch.from_workload(w)
+    total = sum(int(oracle.evictable_pages(int(w["seq_len"][b]), int(w["prompt_len"][b]),
+                                           int(w["window"][b])).sum()) for b in range(4))
+    cap = total // 2
+    freed, count = bt.evict_pages(capacity=cap)
+    torch.cuda.synchronize()
+    assert bt.device_error() == 10
+    assert int(count.item()) == total                  # every candidate took a ticket
+    assert int((bt.page_table == -1).sum()) - int((torch.as_tensor(w["page_table"]) == -1).sum()) == cap
+    assert (freed[:cap] >= 0).all()
+
+
 # ---------------------------------------------------------------------------
 # attention mass
 # ---------------------------------------------------------------------------
