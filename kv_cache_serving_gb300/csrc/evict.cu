@@ -14,7 +14,7 @@
 //
 // One thread per (request, page slot of the page table): the test is a range
 // check on the page's first and last row.  Freed page ids are appended to the
-// caller's list with an atomic counter (order unspecified).
+// caller's list through one atomic per warp (order unspecified).
 #include "common.cuh"
 #include "internal.h"
 
@@ -22,31 +22,37 @@ namespace dsa {
 
 __global__ void __launch_bounds__(256) evict_kernel(const EvictLaunch a) {
   const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (idx >= static_cast<int64_t>(a.batch) * a.max_pages) return;
-  const int b = static_cast<int>(idx / a.max_pages);
-  const int p = static_cast<int>(idx % a.max_pages);
-  const int L = a.seq_len[b], P = a.prompt_len[b], W = a.window[b];
-  int code = 0;
-  if (L < 1 || L > a.max_pages * kPage) code = DSA_DEV_BAD_SEQ_LEN;
-  else if (P < 0) code = DSA_DEV_BAD_PROMPT;
-  else if (W < 0 || W > a.max_window) code = DSA_DEV_BAD_WINDOW;
-  if (code != 0) {
-    if (p == 0) set_error(a.err, code);
-    return;
+  const int lane = threadIdx.x & 31;
+  int pg = -1;  // page this thread unmaps, or -1
+  if (idx < static_cast<int64_t>(a.batch) * a.max_pages) {
+    const int b = static_cast<int>(idx / a.max_pages);
+    const int p = static_cast<int>(idx % a.max_pages);
+    const int L = a.seq_len[b], P = a.prompt_len[b], W = a.window[b];
+    int code = 0;
+    if (L < 1 || L > a.max_pages * kPage) code = DSA_DEV_BAD_SEQ_LEN;
+    else if (P < 0) code = DSA_DEV_BAD_PROMPT;
+    else if (W < 0 || W > a.max_window) code = DSA_DEV_BAD_WINDOW;
+    if (code != 0) {
+      if (p == 0) set_error(a.err, code);
+    } else if (p < (L + kPage - 1) / kPage) {  // a page of the request's rows
+      const int first = p * kPage, last = first + kPage - 1, i = L - 1;
+      if (first >= P && last < i - W) pg = a.page_table[idx];  // -1: already unmapped
+    }
   }
-  if (p >= (L + kPage - 1) / kPage) return;  // beyond the request's rows
-  const int first = p * kPage, last = first + kPage - 1, i = L - 1;
-  if (!(first >= P && last < i - W)) return;  // some row may still be read
-  int32_t* entry = a.page_table + idx;
-  const int pg = *entry;
-  if (pg < 0) return;  // already unmapped
-  const int slot = atomicAdd(a.freed_count, 1);
+  // one atomic per warp: the lanes with a page take consecutive list slots
+  const unsigned want = __ballot_sync(0xffffffffu, pg >= 0);
+  if (want == 0) return;
+  int base = 0;
+  if (lane == __ffs(want) - 1) base = atomicAdd(a.freed_count, __popc(want));
+  base = __shfl_sync(0xffffffffu, base, __ffs(want) - 1);
+  if (pg < 0) return;
+  const int slot = base + __popc(want & ((1u << lane) - 1u));
   if (slot >= a.capacity) {  // no room: the page stays mapped
     set_error(a.err, DSA_DEV_FREE_LIST_FULL);
     return;
   }
   a.freed[slot] = pg;
-  *entry = -1;
+  a.page_table[idx] = -1;
 }
 
 cudaError_t launch_evict(const EvictLaunch& a, cudaStream_t s) {
