@@ -37,11 +37,15 @@
 
 namespace dsa {
 
-// Build-time tuning knobs: stages per warp, warps per CTA (DSA_DECODE_WARPS_BIG:
-// the fused call on batches of more than two waves of units), bytes of K+V per
-// stage.
+// Build-time tuning knobs: stages per warp, warps per CTA and bytes of K+V per
+// stage; the _BIG pair is the build of the fused call for batches of more than
+// two waves of units (more, smaller CTAs and tiles: more warps per SM overlap
+// the latency of the gathers; tensor-core tiles keep at least 16 rows).
 #ifndef DSA_DECODE_WARPS_BIG
 #define DSA_DECODE_WARPS_BIG 3
+#endif
+#ifndef DSA_DECODE_STAGE_BYTES_BIG
+#define DSA_DECODE_STAGE_BYTES_BIG 4096
 #endif
 static_assert(DSA_DECODE_WARPS_BIG == dsa::kDecodeWarpsBig, "host and device agree on the big build");
 #ifndef DSA_DECODE_STAGE_BYTES
@@ -54,11 +58,12 @@ static_assert(DSA_DECODE_WARPS_BIG == dsa::kDecodeWarpsBig, "host and device agr
 #define DSA_DECODE_WARPS 4
 #endif
 
-template <int D, typename KV, int G, bool MMA = false, int NWARPS = DSA_DECODE_WARPS>
+template <int D, typename KV, int G, bool MMA = false, int NWARPS = DSA_DECODE_WARPS,
+          int STAGE_BYTES = DSA_DECODE_STAGE_BYTES>
 struct DecodeTiling {
   static constexpr int kElt = static_cast<int>(sizeof(KV));
   static constexpr int kRowBytes = D * kElt;
-  static constexpr int kT0 = DSA_DECODE_STAGE_BYTES / (2 * kRowBytes);  // K+V of one stage
+  static constexpr int kT0 = STAGE_BYTES / (2 * kRowBytes);  // K+V of one stage
   static constexpr int kTmin = MMA ? 16 : 8;  // whole 16-row mma blocks
   static constexpr int T = kT0 > 32 ? 32 : (kT0 < kTmin ? kTmin : kT0);
   static constexpr int S = DSA_DECODE_STAGES;  // stages per warp
@@ -129,9 +134,10 @@ __device__ __forceinline__ int request_rows(const DecodeLaunch& a, int b, int hk
 }
 
 // QMIX: q and K are bf16 and the dot products use the mixed-precision FMA.
-template <int D, typename KV, int G, int MODE, bool QMIX, int NWARPS = DSA_DECODE_WARPS>
+template <int D, typename KV, int G, int MODE, bool QMIX, int NWARPS = DSA_DECODE_WARPS,
+          int STAGE_BYTES = DSA_DECODE_STAGE_BYTES>
 __global__ void __launch_bounds__(NWARPS * 32) decode_kernel(const DecodeLaunch a) {
-  using Tl = DecodeTiling<D, KV, G, QMIX && G >= 2, NWARPS>;
+  using Tl = DecodeTiling<D, KV, G, QMIX && G >= 2, NWARPS, STAGE_BYTES>;
   constexpr int T = Tl::T, S = Tl::S, NW = Tl::NW;
   constexpr int kRowBytes = Tl::kRowBytes;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -523,10 +529,10 @@ struct IsBf16<bf16_t> {
   static constexpr bool value = true;
 };
 
-template <int D, typename KV, int G, int MODE, bool QMIX, int NWARPS>
+template <int D, typename KV, int G, int MODE, bool QMIX, int NWARPS, int SB>
 cudaError_t launch_decode_one(const DecodeLaunch& a, cudaStream_t s) {
-  using Tl = DecodeTiling<D, KV, G, QMIX && G >= 2, NWARPS>;
-  auto kern = decode_kernel<D, KV, G, MODE, QMIX, NWARPS>;
+  using Tl = DecodeTiling<D, KV, G, QMIX && G >= 2, NWARPS, SB>;
+  auto kern = decode_kernel<D, KV, G, MODE, QMIX, NWARPS, SB>;
   const int smem = Tl::kSmem;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -567,12 +573,12 @@ cudaError_t launch_decode_one(const DecodeLaunch& a, cudaStream_t s) {
     if (hd_ == 128 && g_ == 8) { BODY(128, 8) }   \
   } while (0)
 
-template <typename KV, int MODE, int NWARPS>
+template <typename KV, int MODE, int NWARPS, int SB>
 cudaError_t launch_decode_dispatch(const DecodeLaunch& a, cudaStream_t s) {
   const bool qmix = IsBf16<KV>::value && a.q_bf16 != 0;
 #define DSA_BODY(DD, GG)                                                                  \
-  return qmix ? launch_decode_one<DD, KV, GG, MODE, IsBf16<KV>::value, NWARPS>(a, s)      \
-              : launch_decode_one<DD, KV, GG, MODE, false, NWARPS>(a, s);
+  return qmix ? launch_decode_one<DD, KV, GG, MODE, IsBf16<KV>::value, NWARPS, SB>(a, s)  \
+              : launch_decode_one<DD, KV, GG, MODE, false, NWARPS, SB>(a, s);
   DSA_FOR_SHAPE(a.head_dim, a.hq / a.hkv, DSA_BODY);
 #undef DSA_BODY
   return cudaErrorInvalidValue;
@@ -582,7 +588,9 @@ cudaError_t launch_decode_dispatch(const DecodeLaunch& a, cudaStream_t s) {
 // DSA_DECODE_WARPS_BIG build.
 template <typename KV>
 constexpr bool has_big_warps(int mode) {
-  return IsBf16<KV>::value && mode == kRowsMask && DSA_DECODE_WARPS_BIG != DSA_DECODE_WARPS;
+  return IsBf16<KV>::value && mode == kRowsMask &&
+         (DSA_DECODE_WARPS_BIG != DSA_DECODE_WARPS ||
+          DSA_DECODE_STAGE_BYTES_BIG != DSA_DECODE_STAGE_BYTES);
 }
 
 // One row mode: the default build, or for the fused call with bf16 KV the
@@ -591,16 +599,17 @@ template <typename KV, int MODE>
 cudaError_t launch_decode_mode(const DecodeLaunch& a, cudaStream_t s) {
   if constexpr (has_big_warps<KV>(MODE))
     if (a.warps == DSA_DECODE_WARPS_BIG)
-      return launch_decode_dispatch<KV, MODE, DSA_DECODE_WARPS_BIG>(a, s);
-  return launch_decode_dispatch<KV, MODE, DSA_DECODE_WARPS>(a, s);
+      return launch_decode_dispatch<KV, MODE, DSA_DECODE_WARPS_BIG, DSA_DECODE_STAGE_BYTES_BIG>(
+          a, s);
+  return launch_decode_dispatch<KV, MODE, DSA_DECODE_WARPS, DSA_DECODE_STAGE_BYTES>(a, s);
 }
 
-template <typename KV, int MODE, int NWARPS>
+template <typename KV, int MODE, int NWARPS, int SB>
 DecodeShape decode_shape_m(int head_dim, int group) {
   DecodeShape r{0, 1, 1, NWARPS};
 #define DSA_BODY(DD, GG)                                                                   \
-  using Tl = DecodeTiling<DD, KV, GG, IsBf16<KV>::value && (GG >= 2), NWARPS>;             \
-  auto kern = decode_kernel<DD, KV, GG, MODE, IsBf16<KV>::value, NWARPS>;                  \
+  using Tl = DecodeTiling<DD, KV, GG, IsBf16<KV>::value && (GG >= 2), NWARPS, SB>;         \
+  auto kern = decode_kernel<DD, KV, GG, MODE, IsBf16<KV>::value, NWARPS, SB>;              \
   r.rows_per_pass = Tl::NW * Tl::T;                                                        \
   r.cluster_limit = Tl::kMaxClusterHere;                                                   \
   int n = 0;                                                                               \
@@ -620,8 +629,9 @@ template <typename KV, int MODE>
 DecodeShape decode_shape_mode(int head_dim, int group, int warps) {
   if constexpr (has_big_warps<KV>(MODE))
     if (warps == DSA_DECODE_WARPS_BIG)
-      return decode_shape_m<KV, MODE, DSA_DECODE_WARPS_BIG>(head_dim, group);
-  return decode_shape_m<KV, MODE, DSA_DECODE_WARPS>(head_dim, group);
+      return decode_shape_m<KV, MODE, DSA_DECODE_WARPS_BIG, DSA_DECODE_STAGE_BYTES_BIG>(head_dim,
+                                                                                     group);
+  return decode_shape_m<KV, MODE, DSA_DECODE_WARPS, DSA_DECODE_STAGE_BYTES>(head_dim, group);
 }
 
 }  // namespace dsa

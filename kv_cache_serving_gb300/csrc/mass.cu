@@ -243,12 +243,23 @@ __global__ void __launch_bounds__(MassTiling<D, KV, G>::NW * 32) mass_kernel(con
 
 // Tensor-core tiling: K rows only, T rows per tile, rows padded by 16 bytes so
 // that the ldmatrix row addresses of one 8x8 tile fall in distinct banks.
+#ifndef DSA_MASS_STAGES
+#define DSA_MASS_STAGES 2
+#endif
+#ifndef DSA_MASS_WARPS
+#define DSA_MASS_WARPS 4
+#endif
+#ifndef DSA_MASS_STAGE_BYTES
+#define DSA_MASS_STAGE_BYTES 4096
+#endif
 template <int D>
 struct MassMmaTiling {
   static constexpr int kRowBytes = D * 2;
-  static constexpr int T = 8192 / kRowBytes > 64 ? 64 : 8192 / kRowBytes;
-  static constexpr int S = 2;
-  static constexpr int NW = 4;
+  static constexpr int kT0 = DSA_MASS_STAGE_BYTES / kRowBytes;
+  static constexpr int T = kT0 > 64 ? 64 : (kT0 < 16 ? 16 : kT0);
+  static_assert(T == 16 || T == 32 || T == 64, "tile rows: whole mma blocks, <= 2 per lane");
+  static constexpr int S = DSA_MASS_STAGES;
+  static constexpr int NW = DSA_MASS_WARPS;
   static constexpr int kRowStride = kRowBytes + 16;
   static constexpr int kStageBytes = T * kRowStride;
   static constexpr int kWarpBytes = S * kStageBytes;
@@ -265,7 +276,8 @@ template <int D, int G>
 __global__ void __launch_bounds__(MassMmaTiling<D>::NW * 32)
     mass_mma_kernel(const MassLaunch a) {
   using Tl = MassMmaTiling<D>;
-  constexpr int T = Tl::T, S = Tl::S, NW = Tl::NW, RB = T / 16, NK = D / 16, RPL = T / 32;
+  constexpr int T = Tl::T, S = Tl::S, NW = Tl::NW, RB = T / 16, NK = D / 16;
+  constexpr int RPL = (T + 31) / 32;  // rows of a tile per lane (lane + 32 u < T)
   constexpr int kRowBytes = Tl::kRowBytes, kRowStride = Tl::kRowStride;
   extern __shared__ __align__(128) unsigned char smem[];
 
@@ -302,7 +314,7 @@ __global__ void __launch_bounds__(MassMmaTiling<D>::NW * 32)
 #pragma unroll
     for (int u = 0; u < RPL; ++u) {
       const int j = tile_r0(t) + lane + 32 * u;
-      pg[u] = (t < my_tiles && j < row1) ? __ldg(pt + (j >> 4)) : 0;
+      pg[u] = (t < my_tiles && lane + 32 * u < T && j < row1) ? __ldg(pt + (j >> 4)) : 0;
     }
   };
   auto issue = [&](int t, int stage, const int (&pg)[RPL]) {
