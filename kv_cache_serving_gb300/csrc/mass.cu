@@ -26,15 +26,24 @@
 
 namespace dsa {
 
+#ifndef DSA_MASS_CC_STAGES
+#define DSA_MASS_CC_STAGES 2
+#endif
+#ifndef DSA_MASS_CC_STAGE_BYTES
+#define DSA_MASS_CC_STAGE_BYTES 4096
+#endif
+#ifndef DSA_MASS_CC_WARPS
+#define DSA_MASS_CC_WARPS 4
+#endif
 template <int D, typename KV, int G>
 struct MassTiling {
   static constexpr int kRowBytes = D * static_cast<int>(sizeof(KV));
-  static constexpr int kTByBytes = 8192 / kRowBytes;
+  static constexpr int kTByBytes = DSA_MASS_CC_STAGE_BYTES / kRowBytes;
   static constexpr int kTByRegs = 64 / G;
   static constexpr int kT0 = kTByBytes < kTByRegs ? kTByBytes : kTByRegs;
   static constexpr int T = kT0 > 32 ? 32 : (kT0 < 8 ? 8 : kT0);
-  static constexpr int S = 3;
-  static constexpr int NW = 4;
+  static constexpr int S = DSA_MASS_CC_STAGES;
+  static constexpr int NW = DSA_MASS_CC_WARPS;
   static constexpr int kDPL = D / 32;
   static constexpr int kStageBytes = T * kRowBytes;
   static constexpr int kWarpBytes = S * kStageBytes;
