@@ -47,6 +47,9 @@ namespace dsa {
 #ifndef DSA_DECODE_STAGE_BYTES_BIG
 #define DSA_DECODE_STAGE_BYTES_BIG 4096
 #endif
+#ifndef DSA_DECODE_STAGE_BYTES_DENSE
+#define DSA_DECODE_STAGE_BYTES_DENSE 4096  // dense rows: long, split into many chunks
+#endif
 static_assert(DSA_DECODE_WARPS_BIG == dsa::kDecodeWarpsBig, "host and device agree on the big build");
 #ifndef DSA_DECODE_STAGE_BYTES
 #define DSA_DECODE_STAGE_BYTES 8192
@@ -586,11 +589,16 @@ cudaError_t launch_decode_dispatch(const DecodeLaunch& a, cudaStream_t s) {
 
 // Warps per CTA built for (KV, mode): the fused call with bf16 KV also has a
 // DSA_DECODE_WARPS_BIG build.
+// Stage bytes of the default build of a row mode.
+constexpr int default_stage_bytes(int mode) {
+  return mode == kRowsDense ? DSA_DECODE_STAGE_BYTES_DENSE : DSA_DECODE_STAGE_BYTES;
+}
+
 template <typename KV>
 constexpr bool has_big_warps(int mode) {
   return IsBf16<KV>::value && mode == kRowsMask &&
          (DSA_DECODE_WARPS_BIG != DSA_DECODE_WARPS ||
-          DSA_DECODE_STAGE_BYTES_BIG != DSA_DECODE_STAGE_BYTES);
+          DSA_DECODE_STAGE_BYTES_BIG != default_stage_bytes(mode));
 }
 
 // One row mode: the default build, or for the fused call with bf16 KV the
@@ -601,7 +609,7 @@ cudaError_t launch_decode_mode(const DecodeLaunch& a, cudaStream_t s) {
     if (a.warps == DSA_DECODE_WARPS_BIG)
       return launch_decode_dispatch<KV, MODE, DSA_DECODE_WARPS_BIG, DSA_DECODE_STAGE_BYTES_BIG>(
           a, s);
-  return launch_decode_dispatch<KV, MODE, DSA_DECODE_WARPS, DSA_DECODE_STAGE_BYTES>(a, s);
+  return launch_decode_dispatch<KV, MODE, DSA_DECODE_WARPS, default_stage_bytes(MODE)>(a, s);
 }
 
 template <typename KV, int MODE, int NWARPS, int SB>
@@ -631,7 +639,7 @@ DecodeShape decode_shape_mode(int head_dim, int group, int warps) {
     if (warps == DSA_DECODE_WARPS_BIG)
       return decode_shape_m<KV, MODE, DSA_DECODE_WARPS_BIG, DSA_DECODE_STAGE_BYTES_BIG>(head_dim,
                                                                                      group);
-  return decode_shape_m<KV, MODE, DSA_DECODE_WARPS, DSA_DECODE_STAGE_BYTES>(head_dim, group);
+  return decode_shape_m<KV, MODE, DSA_DECODE_WARPS, default_stage_bytes(MODE)>(head_dim, group);
 }
 
 }  // namespace dsa
