@@ -393,7 +393,8 @@ def run_ours(args):
     bt.check("warm-up")
     plan_m = dsa.dsa_decode_plan(d, dsa.PLAN_MASKED)
     plan_s = dsa.dsa_decode_plan(d, dsa.PLAN_SPARSE)
-    same_plan = (plan_m[0], plan_m[1], plan_m[3]) == (plan_s[0], plan_s[1], plan_s[3])
+    same_plan = ((plan_m[0], plan_m[1], plan_m[3], plan_m[4]) ==
+                 (plan_s[0], plan_s[1], plan_s[3], plan_s[4]))
     same_bits = bool(torch.equal(bt.out, out_2) and torch.equal(bt.lse, lse_2))
 
     g_step = graph_of(step, K, stream)
@@ -495,7 +496,7 @@ def run_ours(args):
     step_s = t_step / K
     tokens = world * B / step_s
     peak, peak_src = hbm_peak()
-    chunk, nch, launches, warps = dsa.dsa_decode_plan(d, dsa.PLAN_MASKED)
+    chunk, nch, launches, warps, tile_rows = dsa.dsa_decode_plan(d, dsa.PLAN_MASKED)
     launches_two = dsa.dsa_decode_plan(d, dsa.PLAN_SPARSE)[2]
     achieved = by["masked"] / step_s / 1e9
     kernel = "decode_kernel, kept set read from the keep mask (dsa_decode_sparse_masked)"
@@ -529,7 +530,7 @@ def run_ours(args):
             "request_order": "longest first" if order is not None else "batch order",
             "decode_chunk_rows": chunk, "decode_chunks_max": nch,
             "sparse_cluster": nch if launches == 1 else 1,
-            "warps_per_cta": warps,
+            "warps_per_cta": warps, "tile_rows": tile_rows,
         },
         "effective_kv_gbs": by["masked"] / step_s / 1e9,
         "pct_of_hbm_peak": 100.0 * by["masked"] / step_s / 1e9 / peak,

@@ -264,14 +264,15 @@ dsa_status dsa_evict_pages(const dsa_dims* dims, const int32_t* seq_len,
 /*
  * dsa_decode_plan -- how a decode call will split its work on the CURRENT
  * device: rows per CTA (*chunk), CTAs per (request, kv head) at most
- * (*num_chunks), kernel launches per call (*launches) and warps per CTA
- * (*warps).  mode selects the call: 0 dsa_decode_dense, 1 dsa_decode_sparse,
+ * (*num_chunks), kernel launches per call (*launches), warps per CTA (*warps)
+ * and rows per tile (*tile_rows).  mode selects the call: 0 dsa_decode_dense, 1 dsa_decode_sparse,
  * 2 dsa_decode_sparse_masked (other values: DSA_ERR_INVALID_ARG).  Two calls
  * with the same plan sum in the same order.  Host-only; any output pointer may
  * be NULL.
  */
 dsa_status dsa_decode_plan(const dsa_dims* dims, int32_t mode, int32_t* chunk,
-                           int32_t* num_chunks, int32_t* launches, int32_t* warps);
+                           int32_t* num_chunks, int32_t* launches, int32_t* warps,
+                           int32_t* tile_rows);
 
 /*
  * dsa_decode_sparse_noalloc -- dsa_decode_sparse for callers that cannot

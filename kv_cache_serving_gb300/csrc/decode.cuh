@@ -41,16 +41,12 @@ namespace dsa {
 // stage; the _BIG pair is the build of the fused call for batches of more than
 // two waves of units (more, smaller CTAs and tiles: more warps per SM overlap
 // the latency of the gathers; tensor-core tiles keep at least 16 rows).
-#ifndef DSA_DECODE_WARPS_BIG
-#define DSA_DECODE_WARPS_BIG 3
-#endif
 #ifndef DSA_DECODE_STAGE_BYTES_BIG
 #define DSA_DECODE_STAGE_BYTES_BIG 4096
 #endif
 #ifndef DSA_DECODE_STAGE_BYTES_DENSE
 #define DSA_DECODE_STAGE_BYTES_DENSE 4096  // dense rows: long, split into many chunks
 #endif
-static_assert(DSA_DECODE_WARPS_BIG == dsa::kDecodeWarpsBig, "host and device agree on the big build");
 #ifndef DSA_DECODE_STAGE_BYTES
 #define DSA_DECODE_STAGE_BYTES 8192
 #endif
@@ -80,9 +76,14 @@ struct DecodeTiling {
   // loads (8 lanes over 128 contiguous bytes) need no padding.
   static constexpr int kRowStride = kRowBytes + (MMA ? 16 : 0);
   static constexpr int kStageBytes = 2 * T * kRowStride;
-  static constexpr int kWarpBytes = S * kStageBytes;
+  // A 16-row tensor-core tile whose K and V do not fit STAGE_BYTES is staged
+  // as one K buffer and one V buffer per warp (each refilled as soon as its
+  // half of the tile is computed) instead of S stages of K and V.
+  static constexpr bool kSplit = MMA && (2 * 16 * kRowBytes > STAGE_BYTES);
+  static constexpr int kBars = kSplit ? 2 : S;  // mbarriers per warp
+  static constexpr int kWarpBytes = kSplit ? kStageBytes : S * kStageBytes;
   static constexpr int kBarOff = NW * kWarpBytes;
-  static constexpr int kPsOff = kBarOff + NW * S * 8;  // [NW][hi, lo][8 heads][T] bf16
+  static constexpr int kPsOff = kBarOff + NW * kBars * 8;  // [NW][hi, lo][8 heads][T] bf16
   static constexpr int kSmem = kPsOff + (MMA ? NW * 2 * 8 * T * 2 : 0);
   // a warp's end-of-CTA state [G][D+2] floats reuses the start of its own ring
   static_assert(G * (D + 2) * 4 <= kWarpBytes, "merge slot fits the ring");
@@ -137,9 +138,23 @@ __device__ __forceinline__ int request_rows(const DecodeLaunch& a, int b, int hk
 }
 
 // QMIX: q and K are bf16 and the dot products use the mixed-precision FMA.
+#ifndef DSA_DECODE_SPLIT_MIN_CTAS
+#define DSA_DECODE_SPLIT_MIN_CTAS 5
+#endif
+// Resident CTAs per SM the compiler must allow for (register budget): the
+// split-staged builds are small enough in shared memory for several.
+template <int D, typename KV, int G, bool QMIX, int NWARPS, int STAGE_BYTES>
+constexpr int decode_min_ctas() {
+  return DecodeTiling<D, KV, G, QMIX && G >= 2, NWARPS, STAGE_BYTES>::kSplit
+             ? DSA_DECODE_SPLIT_MIN_CTAS
+             : 1;
+}
+
 template <int D, typename KV, int G, int MODE, bool QMIX, int NWARPS = DSA_DECODE_WARPS,
           int STAGE_BYTES = DSA_DECODE_STAGE_BYTES>
-__global__ void __launch_bounds__(NWARPS * 32) decode_kernel(const DecodeLaunch a) {
+__global__ void __launch_bounds__(NWARPS * 32,
+                                  (decode_min_ctas<D, KV, G, QMIX, NWARPS, STAGE_BYTES>()))
+    decode_kernel(const DecodeLaunch a) {
   using Tl = DecodeTiling<D, KV, G, QMIX && G >= 2, NWARPS, STAGE_BYTES>;
   constexpr int T = Tl::T, S = Tl::S, NW = Tl::NW;
   constexpr int kRowBytes = Tl::kRowBytes;
@@ -259,16 +274,17 @@ __global__ void __launch_bounds__(NWARPS * 32) decode_kernel(const DecodeLaunch 
   const int ntiles = (row1 - row0 + T - 1) / T;
 
   constexpr int kRowStride = Tl::kRowStride;
+  constexpr bool kSplit = Tl::kSplit;
   unsigned char* kst = smem + warp * Tl::kWarpBytes;  // [S][T] K rows, kRowStride apart
-  unsigned char* vst = kst + S * T * kRowStride;      // [S][T] V rows
+  unsigned char* vst = kst + (kSplit ? 1 : S) * T * kRowStride;  // [S][T] V rows
   uint16_t* ps = reinterpret_cast<uint16_t*>(smem + Tl::kPsOff) + warp * 2 * 8 * T;  // [2][8][T]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Tl::kBarOff) + warp * S;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Tl::kBarOff) + warp * Tl::kBars;
   // end-of-CTA state of warp w: [G][D+2] floats at the start of w's ring
   auto mslot = [&](int w) { return reinterpret_cast<float*>(smem + w * Tl::kWarpBytes); };
 
   if (lane == 0) {
 #pragma unroll
-    for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
+    for (int s = 0; s < Tl::kBars; ++s) mbar_init(&bars[s], 1);
     fence_mbar_init();
   }
   __syncwarp();
@@ -346,6 +362,25 @@ __global__ void __launch_bounds__(NWARPS * 32) decode_kernel(const DecodeLaunch 
     }
   };
 
+  // Split staging: the K (half 0) or V (half 1) rows of local tile t into
+  // their buffer, completing on bars[half]; lanes [0,T) copy one row each.
+  auto issue_half = [&](int t, int half, int j, int pg) {
+    const int nrows = tile_rows(t);
+    if (lane == 0) mbar_arrive_expect_tx(&bars[half], static_cast<uint32_t>(nrows * kRowBytes));
+    __syncwarp();
+    if (my_r < nrows && lane < T) {
+      if (static_cast<unsigned>(pg) >= static_cast<unsigned>(a.num_pages)) {
+        set_error(a.err, DSA_DEV_BAD_PAGE);
+        pg = 0;
+      }
+      const size_t off = ((static_cast<size_t>(pg) * kPage + (j & (kPage - 1))) * a.hkv + hk) * D;
+      const bool fresh = knew != nullptr && j == L - 1;  // the appended row
+      const KV* src = half == 0 ? (fresh ? knew : kg + off) : (fresh ? vnew : vg + off);
+      bulk_copy_g2s((half == 0 ? kst : vst) + static_cast<size_t>(my_r) * kRowStride, src,
+                    kRowBytes, &bars[half]);
+    }
+  };
+
   WarpAttn<D, KV, G, QMIX, T> wa;
   static_assert(WarpAttn<D, KV, G, QMIX, T>::kRowStride == Tl::kRowStride, "row stride");
   typename WarpAttn<D, KV, G, QMIX, T>::Q wq_;
@@ -365,12 +400,54 @@ __global__ void __launch_bounds__(NWARPS * 32) decode_kernel(const DecodeLaunch 
     else
       pr[t] = load_pg(t, jr[t]);
   }
+  int failed_at = -1;
+  if constexpr (kSplit) {
+    // K and V of tile 0 in flight; then per tile: QK^T + softmax on K(t),
+    // refill the K buffer with tile t+1, PV on V(t), refill the V buffer
+    if (my_tiles > 0) {
+      issue_half(0, 0, jr[0], pr[0]);
+      issue_half(0, 1, jr[0], pr[0]);
+    }
+    int ja = jr[1], pa = pr[1], jb = jr[2];  // addresses of tiles 1 and 2
+    bool failed_on_v = false;
+    for (int t = 0; t < my_tiles; ++t) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars[0], static_cast<uint32_t>(t) & 1u))) {
+        failed_at = t;
+        break;
+      }
+      const int nrows = min(T, row1 - (row0 + (warp + t * NW) * T));
+      wa.qk_softmax(wq_, kst, nrows, a.scale_log2, ps, lane);
+      __syncwarp();
+      fence_proxy_async_smem();
+      if (t + 1 < my_tiles) issue_half(t + 1, 0, ja, pa);
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars[1], static_cast<uint32_t>(t) & 1u))) {
+        failed_at = t;
+        failed_on_v = true;
+        break;
+      }
+      wa.pv(vst, nrows, ps, lane);
+      __syncwarp();
+      fence_proxy_async_smem();
+      if (t + 1 < my_tiles) issue_half(t + 1, 1, ja, pa);
+      ja = jb;
+      pa = load_pg(t + 2, ja);
+      jb = load_j(t + 3);
+    }
+    if (failed_at >= 0) {
+      // Give the copies still in flight a bounded chance to land before exiting.
+      if (lane == 0) set_error(a.err, DSA_DEV_TIMEOUT);
+      // in flight: V of the failed tile, and K of it (failed on K) or of the next
+      mbar_wait(&bars[1], static_cast<uint32_t>(failed_at) & 1u);
+      if (!failed_on_v) mbar_wait(&bars[0], static_cast<uint32_t>(failed_at) & 1u);
+      else if (failed_at + 1 < my_tiles)
+        mbar_wait(&bars[0], static_cast<uint32_t>(failed_at + 1) & 1u);
+    }
+  } else {
 #pragma unroll
   for (int t = 0; t < S; ++t)
     if (t < my_tiles) issue(t, t, jr[t], pr[t]);
   int j0 = jr[S], pg0 = pr[S], j1 = jr[S + 1];  // next tile to issue: S
 
-  int failed_at = -1;
   for (int t = 0; t < my_tiles; ++t) {
     const int stage = t % S;
     if (!__all_sync(0xffffffffu, mbar_wait(&bars[stage], static_cast<uint32_t>(t / S) & 1u))) {
@@ -396,6 +473,7 @@ __global__ void __launch_bounds__(NWARPS * 32) decode_kernel(const DecodeLaunch 
     for (int t = failed_at; t < my_tiles && t < failed_at + S; ++t)
       mbar_wait(&bars[t % S], static_cast<uint32_t>(t / S) & 1u);
   }
+  }  // S-stage staging
 
   // sum the warp's partial states, then merge the warps of this CTA (each
   // warp's ring is idle now: its copies have all landed)
@@ -587,8 +665,8 @@ cudaError_t launch_decode_dispatch(const DecodeLaunch& a, cudaStream_t s) {
   return cudaErrorInvalidValue;
 }
 
-// Warps per CTA built for (KV, mode): the fused call with bf16 KV also has a
-// DSA_DECODE_WARPS_BIG build.
+// The fused call with bf16 KV also has a big-batch build (its own warps per
+// CTA and stage size).
 // Stage bytes of the default build of a row mode.
 constexpr int default_stage_bytes(int mode) {
   return mode == kRowsDense ? DSA_DECODE_STAGE_BYTES_DENSE : DSA_DECODE_STAGE_BYTES;
@@ -606,19 +684,20 @@ constexpr bool has_big_warps(int mode) {
 template <typename KV, int MODE>
 cudaError_t launch_decode_mode(const DecodeLaunch& a, cudaStream_t s) {
   if constexpr (has_big_warps<KV>(MODE))
-    if (a.warps == DSA_DECODE_WARPS_BIG)
+    if (a.big != 0)
       return launch_decode_dispatch<KV, MODE, DSA_DECODE_WARPS_BIG, DSA_DECODE_STAGE_BYTES_BIG>(
           a, s);
   return launch_decode_dispatch<KV, MODE, DSA_DECODE_WARPS, default_stage_bytes(MODE)>(a, s);
 }
 
 template <typename KV, int MODE, int NWARPS, int SB>
-DecodeShape decode_shape_m(int head_dim, int group) {
-  DecodeShape r{0, 1, 1, NWARPS};
+DecodeShape decode_shape_m(int head_dim, int group, bool big) {
+  DecodeShape r{0, 1, 1, NWARPS, 0, big};
 #define DSA_BODY(DD, GG)                                                                   \
   using Tl = DecodeTiling<DD, KV, GG, IsBf16<KV>::value && (GG >= 2), NWARPS, SB>;         \
   auto kern = decode_kernel<DD, KV, GG, MODE, IsBf16<KV>::value, NWARPS, SB>;              \
   r.rows_per_pass = Tl::NW * Tl::T;                                                        \
+  r.tile_rows = Tl::T;                                                                     \
   r.cluster_limit = Tl::kMaxClusterHere;                                                   \
   int n = 0;                                                                               \
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Tl::kSmem) == \
@@ -634,12 +713,13 @@ DecodeShape decode_shape_m(int head_dim, int group) {
 }
 
 template <typename KV, int MODE>
-DecodeShape decode_shape_mode(int head_dim, int group, int warps) {
+DecodeShape decode_shape_mode(int head_dim, int group, bool big) {
   if constexpr (has_big_warps<KV>(MODE))
-    if (warps == DSA_DECODE_WARPS_BIG)
-      return decode_shape_m<KV, MODE, DSA_DECODE_WARPS_BIG, DSA_DECODE_STAGE_BYTES_BIG>(head_dim,
-                                                                                     group);
-  return decode_shape_m<KV, MODE, DSA_DECODE_WARPS, default_stage_bytes(MODE)>(head_dim, group);
+    if (big)
+      return decode_shape_m<KV, MODE, DSA_DECODE_WARPS_BIG, DSA_DECODE_STAGE_BYTES_BIG>(
+          head_dim, group, true);
+  return decode_shape_m<KV, MODE, DSA_DECODE_WARPS, default_stage_bytes(MODE)>(head_dim, group,
+                                                                             false);
 }
 
 }  // namespace dsa

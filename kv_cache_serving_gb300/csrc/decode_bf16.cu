@@ -6,7 +6,7 @@
 namespace dsa {
 
 cudaError_t launch_decode_bf16_mask(const DecodeLaunch& a, cudaStream_t s);
-DecodeShape decode_shape_bf16_mask(int head_dim, int group, int warps);
+DecodeShape decode_shape_bf16_mask(int head_dim, int group, bool big);
 
 cudaError_t launch_decode_bf16(const DecodeLaunch& a, int mode, cudaStream_t s) {
   switch (mode) {
@@ -17,13 +17,13 @@ cudaError_t launch_decode_bf16(const DecodeLaunch& a, int mode, cudaStream_t s) 
   return cudaErrorInvalidValue;
 }
 
-DecodeShape decode_shape_bf16(int head_dim, int group, int mode, int warps) {
+DecodeShape decode_shape_bf16(int head_dim, int group, int mode, bool big) {
   switch (mode) {
-    case kRowsDense: return decode_shape_mode<bf16_t, kRowsDense>(head_dim, group, warps);
-    case kRowsList: return decode_shape_mode<bf16_t, kRowsList>(head_dim, group, warps);
-    case kRowsMask: return decode_shape_bf16_mask(head_dim, group, warps);
+    case kRowsDense: return decode_shape_mode<bf16_t, kRowsDense>(head_dim, group, big);
+    case kRowsList: return decode_shape_mode<bf16_t, kRowsList>(head_dim, group, big);
+    case kRowsMask: return decode_shape_bf16_mask(head_dim, group, big);
   }
-  return DecodeShape{0, 1, 1, DSA_DECODE_WARPS};
+  return DecodeShape{0, 1, 1, DSA_DECODE_WARPS, 0, false};
 }
 
 }  // namespace dsa

@@ -148,7 +148,8 @@ size_t unit_ints_region(const dsa_dims* d) {
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 struct Plan {
-  int chunk, num_chunks, quantum, per_sm, cluster, warps;
+  int chunk, num_chunks, quantum, per_sm, cluster, warps, tile_rows;
+  bool big;
 };
 
 // Automatic cluster size: a CTA's fixed latency (first copies, end-of-CTA
@@ -162,27 +163,29 @@ int sparse_cluster_auto(int64_t units, int64_t slots) {
   return best;
 }
 
-DecodeShape decode_shape(const dsa_dims* d, int mode, int warps) {
+DecodeShape decode_shape(const dsa_dims* d, int mode, bool big) {
   const int g = d->hq / d->hkv;
-  return d->kv_dtype == DSA_BF16 ? decode_shape_bf16(d->head_dim, g, mode, warps)
-                                 : decode_shape_f32(d->head_dim, g, mode, warps);
+  return d->kv_dtype == DSA_BF16 ? decode_shape_bf16(d->head_dim, g, mode, big)
+                                 : decode_shape_f32(d->head_dim, g, mode, big);
 }
 
 Plan decode_plan(const dsa_dims* d, int mode) {
   const int64_t n_max = mode == kModeDense ? dense_rows(d) : d->max_kept;
   const int64_t units = static_cast<int64_t>(d->batch) * d->hkv;
-  DecodeShape sh = decode_shape(d, mode, 0);
+  DecodeShape sh = decode_shape(d, mode, false);
   // The fused call on a batch of more than two waves of units runs the build
   // with fewer warps per CTA (when there is one): more, smaller CTAs per SM
   // overlap one CTA's start-up with the others' streaming.
   if (mode == kModeMask && units > 2 * static_cast<int64_t>(sm_count()) * sh.ctas_per_sm) {
-    const DecodeShape big = decode_shape(d, mode, kDecodeWarpsBig);
-    if (big.warps == kDecodeWarpsBig) sh = big;
+    const DecodeShape big = decode_shape(d, mode, true);
+    if (big.big) sh = big;
   }
   Plan p{};
   p.quantum = sh.rows_per_pass;
   p.per_sm = sh.ctas_per_sm;
   p.warps = sh.warps;
+  p.tile_rows = sh.tile_rows;
+  p.big = sh.big;
   p.cluster = 1;
   int ncl = g_sparse_cluster.load(std::memory_order_relaxed);
   if (ncl == 0) ncl = sparse_cluster_auto(units, sm_count() * p.per_sm);
@@ -262,6 +265,7 @@ dsa_status decode_common(const dsa_dims* d, int mode, const void* q, const void*
   a.num_chunks = plan.num_chunks;
   a.cluster = plan.cluster;
   a.warps = plan.warps;
+  a.big = plan.big ? 1 : 0;
   a.scale_log2 = scale * kLog2e;
   a.out = out;
   a.lse = lse;
@@ -440,7 +444,8 @@ dsa_status dsa_attention_mass(const dsa_dims* dims, const void* q, const void* k
 }
 
 dsa_status dsa_decode_plan(const dsa_dims* dims, int32_t mode, int32_t* chunk,
-                           int32_t* num_chunks, int32_t* launches, int32_t* warps) {
+                           int32_t* num_chunks, int32_t* launches, int32_t* warps,
+                           int32_t* tile_rows) {
   const dsa_status st = check_dims(dims);
   if (st != DSA_OK) return st;
   if (mode < kModeDense || mode > kModeMask) return DSA_ERR_INVALID_ARG;
@@ -451,6 +456,7 @@ dsa_status dsa_decode_plan(const dsa_dims* dims, int32_t mode, int32_t* chunk,
   if (launches)
     *launches = dims->batch == 0 ? 0 : (p.num_chunks > 1 && p.cluster <= 1 ? 2 : 1);
   if (warps) *warps = p.warps;
+  if (tile_rows) *tile_rows = p.tile_rows;
   return DSA_OK;
 }
 

@@ -36,6 +36,7 @@ struct DecodeLaunch {
   int32_t chunk, num_chunks;
   int32_t cluster;   // > 1: the num_chunks (== cluster) CTAs of a unit merge in a cluster
   int32_t warps;     // warps per CTA of the build to launch (see DecodeShape)
+  int32_t big;       // 1: the big-batch build of the fused call (see DecodeShape)
   float scale_log2;  // softmax scale * log2(e)
   float* out;
   float* lse;
@@ -108,8 +109,11 @@ cudaError_t launch_compact(const CompactLaunch& a, cudaStream_t s);
 cudaError_t launch_evict(const EvictLaunch& a, cudaStream_t s);
 
 // Warps per CTA of the second build of the fused call (bf16 KV), chosen for
-// batches of many units; must match DSA_DECODE_WARPS_BIG in decode.cuh.
-constexpr int kDecodeWarpsBig = 3;
+// batches of many units (build-time knob shared by host and device code).
+#ifndef DSA_DECODE_WARPS_BIG
+#define DSA_DECODE_WARPS_BIG 4
+#endif
+constexpr int kDecodeWarpsBig = DSA_DECODE_WARPS_BIG;
 
 // Host-side facts about one build of the decode kernel, for the chunk choice.
 struct DecodeShape {
@@ -117,10 +121,12 @@ struct DecodeShape {
   int ctas_per_sm;    // resident CTAs per SM (>= 1)
   int cluster_limit;  // largest cluster whose merge buffer fits the rings
   int warps;          // warps per CTA of this build
+  int tile_rows;      // rows per tile of this build
+  bool big;           // this is the big-batch build
 };
-// The build of (head_dim, group, mode) with `warps` warps per CTA when there is
-// one (the fused call with bf16 KV has 3 and 4), else the default build.
-DecodeShape decode_shape_bf16(int head_dim, int group, int mode, int warps);
-DecodeShape decode_shape_f32(int head_dim, int group, int mode, int warps);
+// The big-batch build of (head_dim, group, mode) when `big` and there is one
+// (the fused call with bf16 KV), else the default build.
+DecodeShape decode_shape_bf16(int head_dim, int group, int mode, bool big);
+DecodeShape decode_shape_f32(int head_dim, int group, int mode, bool big);
 
 }  // namespace dsa

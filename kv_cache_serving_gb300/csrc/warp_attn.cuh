@@ -174,106 +174,123 @@ struct WarpAttn {
     }
   }
 
+  // Tensor cores, first half of a tile: S = K q^T, the online-softmax update,
+  // and P (bf16 hi + lo) into ps.  Reads kt only.
+  __device__ __forceinline__ void qk_softmax(const Q& q, const unsigned char* kt, int nrows,
+                                             float scale_log2, uint16_t* ps, int lane) {
+    static_assert(kMMA, "tensor-core engine");
+    const int g4 = lane >> 2, tig = lane & 3;
+    constexpr int RB = T / 16;
+    float sm[RB][4];
+#pragma unroll
+    for (int rb = 0; rb < RB; ++rb) {
+      // two accumulator chains (even / odd 16-dim slices) halve the
+      // dependent mma latency; summed once at the end
+      float s2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sm[rb][e] = 0.f;
+      const unsigned char* arow =
+          kt + (rb * 16 + (lane & 7) + 8 * ((lane >> 3) & 1)) * kRowStride + 16 * (lane >> 4);
+#pragma unroll
+      for (int kk = 0; kk < NK; ++kk) {
+        uint32_t af[4];
+        ldsm_x4(af, arow + 32 * kk);
+        if (kk & 1)
+          mma_bf16(s2, af, q.qf[kk][0], q.qf[kk][1]);
+        else
+          mma_bf16(sm[rb], af, q.qf[kk][0], q.qf[kk][1]);
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sm[rb][e] += s2[e];
+    }
+    // scale, mask rows past nrows (stale data), online softmax for the
+    // thread's two heads (rows spread over the 8 lanes of a column pair)
+    float alpha[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      float tmax = -INFINITY;
+#pragma unroll
+      for (int rb = 0; rb < RB; ++rb)
+#pragma unroll
+        for (int hi = 0; hi < 2; ++hi) {
+          const int r = rb * 16 + g4 + 8 * hi;
+          float& x = sm[rb][2 * hi + j];
+          x = (r < nrows) ? x * scale_log2 : -INFINITY;
+          tmax = fmaxf(tmax, x);
+        }
+      tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 4));
+      tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 8));
+      tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
+      const float mnew = fmaxf(m2[j], tmax);
+      alpha[j] = exp2f(m2[j] - mnew);
+      m2[j] = mnew;
+      float psum = 0.f;
+#pragma unroll
+      for (int rb = 0; rb < RB; ++rb)
+#pragma unroll
+        for (int hi = 0; hi < 2; ++hi) {
+          float& x = sm[rb][2 * hi + j];
+          x = exp2f(x - mnew);
+          psum += x;
+        }
+      l2[j] = l2[j] * alpha[j] + psum;
+    }
+#pragma unroll
+    for (int mt = 0; mt < NK; ++mt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) oacc[mt][e] *= alpha[e & 1];
+    // P as bf16 hi + lo into the warp's [head][row] buffers (mma B operand)
+#pragma unroll
+    for (int rb = 0; rb < RB; ++rb)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int h = 2 * tig + (e & 1), r = rb * 16 + g4 + 8 * (e >> 1);
+        const float x = sm[rb][e];
+        const uint16_t xh = f32_to_bf16_rn(x);
+        ps[h * T + r] = xh;
+        ps[8 * T + h * T + r] = f32_to_bf16_rn(x - bf16_lo(xh));
+      }
+  }
+
+  // Tensor cores, second half: O^T += V^T P from ps.  Zeroes V rows past nrows
+  // in place (stale shared memory times p = 0 must stay 0).
+  __device__ __forceinline__ void pv(unsigned char* vt, int nrows, const uint16_t* ps, int lane) {
+    static_assert(kMMA, "tensor-core engine");
+    const int g4 = lane >> 2, tig = lane & 3;
+    constexpr int RB = T / 16;
+    // rows past nrows may hold stale shared memory: zero them so 0 * V stays 0
+    if (nrows < T) {
+      for (int r = nrows; r < T; ++r)
+        for (int x = lane * 16; x < kRowBytes; x += 32 * 16)
+          *reinterpret_cast<uint4*>(vt + r * kRowStride + x) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    __syncwarp();
+#pragma unroll
+    for (int kb = 0; kb < RB; ++kb) {
+      const uint32_t* ph = reinterpret_cast<const uint32_t*>(ps + g4 * T + kb * 16 + 2 * tig);
+      const uint32_t* pl =
+          reinterpret_cast<const uint32_t*>(ps + 8 * T + g4 * T + kb * 16 + 2 * tig);
+      const uint32_t bh0 = ph[0], bh1 = ph[4], bl0 = pl[0], bl1 = pl[4];
+      const unsigned char* vrow =
+          vt + (kb * 16 + (lane & 7) + 8 * (lane >> 4)) * kRowStride + 16 * ((lane >> 3) & 1);
+#pragma unroll
+      for (int mt = 0; mt < NK; ++mt) {
+        uint32_t af[4];
+        ldsm_x4_trans(af, vrow + 32 * mt);
+        mma_bf16(oacc[mt], af, bh0, bh1);
+        mma_bf16(oacc[mt], af, bl0, bl1);
+      }
+    }
+  }
+
   // One tile: rows 0..nrows-1 of kt / vt (kRowStride apart; rows past nrows may
   // hold stale data).  ps: this warp's [hi, lo][8 heads][T] bf16 scratch (tensor
   // cores only).  The tensor-core engine zeroes V rows past nrows in place.
   __device__ __forceinline__ void tile(const Q& q, const unsigned char* kt, unsigned char* vt,
                                        int nrows, float scale_log2, uint16_t* ps, int lane) {
     if constexpr (kMMA) {
-      const int g4 = lane >> 2, tig = lane & 3;
-      constexpr int RB = T / 16;
-      float sm[RB][4];
-#pragma unroll
-      for (int rb = 0; rb < RB; ++rb) {
-        // two accumulator chains (even / odd 16-dim slices) halve the
-        // dependent mma latency; summed once at the end
-        float s2[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) sm[rb][e] = 0.f;
-        const unsigned char* arow =
-            kt + (rb * 16 + (lane & 7) + 8 * ((lane >> 3) & 1)) * kRowStride + 16 * (lane >> 4);
-#pragma unroll
-        for (int kk = 0; kk < NK; ++kk) {
-          uint32_t af[4];
-          ldsm_x4(af, arow + 32 * kk);
-          if (kk & 1)
-            mma_bf16(s2, af, q.qf[kk][0], q.qf[kk][1]);
-          else
-            mma_bf16(sm[rb], af, q.qf[kk][0], q.qf[kk][1]);
-        }
-#pragma unroll
-        for (int e = 0; e < 4; ++e) sm[rb][e] += s2[e];
-      }
-      // scale, mask rows past nrows (stale data), online softmax for the
-      // thread's two heads (rows spread over the 8 lanes of a column pair)
-      float alpha[2];
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        float tmax = -INFINITY;
-#pragma unroll
-        for (int rb = 0; rb < RB; ++rb)
-#pragma unroll
-          for (int hi = 0; hi < 2; ++hi) {
-            const int r = rb * 16 + g4 + 8 * hi;
-            float& x = sm[rb][2 * hi + j];
-            x = (r < nrows) ? x * scale_log2 : -INFINITY;
-            tmax = fmaxf(tmax, x);
-          }
-        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 4));
-        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 8));
-        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
-        const float mnew = fmaxf(m2[j], tmax);
-        alpha[j] = exp2f(m2[j] - mnew);
-        m2[j] = mnew;
-        float psum = 0.f;
-#pragma unroll
-        for (int rb = 0; rb < RB; ++rb)
-#pragma unroll
-          for (int hi = 0; hi < 2; ++hi) {
-            float& x = sm[rb][2 * hi + j];
-            x = exp2f(x - mnew);
-            psum += x;
-          }
-        l2[j] = l2[j] * alpha[j] + psum;
-      }
-#pragma unroll
-      for (int mt = 0; mt < NK; ++mt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) oacc[mt][e] *= alpha[e & 1];
-      // P as bf16 hi + lo into the warp's [head][row] buffers (mma B operand)
-#pragma unroll
-      for (int rb = 0; rb < RB; ++rb)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int h = 2 * tig + (e & 1), r = rb * 16 + g4 + 8 * (e >> 1);
-          const float x = sm[rb][e];
-          const uint16_t xh = f32_to_bf16_rn(x);
-          ps[h * T + r] = xh;
-          ps[8 * T + h * T + r] = f32_to_bf16_rn(x - bf16_lo(xh));
-        }
-      // rows past nrows may hold stale shared memory: zero them so 0 * V stays 0
-      if (nrows < T) {
-        for (int r = nrows; r < T; ++r)
-          for (int x = lane * 16; x < kRowBytes; x += 32 * 16)
-            *reinterpret_cast<uint4*>(vt + r * kRowStride + x) = make_uint4(0u, 0u, 0u, 0u);
-      }
-      __syncwarp();
-#pragma unroll
-      for (int kb = 0; kb < RB; ++kb) {
-        const uint32_t* ph = reinterpret_cast<const uint32_t*>(ps + g4 * T + kb * 16 + 2 * tig);
-        const uint32_t* pl =
-            reinterpret_cast<const uint32_t*>(ps + 8 * T + g4 * T + kb * 16 + 2 * tig);
-        const uint32_t bh0 = ph[0], bh1 = ph[4], bl0 = pl[0], bl1 = pl[4];
-        const unsigned char* vrow =
-            vt + (kb * 16 + (lane & 7) + 8 * (lane >> 4)) * kRowStride + 16 * ((lane >> 3) & 1);
-#pragma unroll
-        for (int mt = 0; mt < NK; ++mt) {
-          uint32_t af[4];
-          ldsm_x4_trans(af, vrow + 32 * mt);
-          mma_bf16(oacc[mt], af, bh0, bh1);
-          mma_bf16(oacc[mt], af, bl0, bl1);
-        }
-      }
+      qk_softmax(q, kt, nrows, scale_log2, ps, lane);
+      pv(vt, nrows, ps, lane);
     } else {
       const int grp = lane >> 3, jl = lane & 7;  // row group, lane in group
       // scores of this lane's rows (rows past nrows hold stale data: masked)

@@ -70,7 +70,8 @@ def _load():
         "dsa_decode_dense": ([D, P, P, P, P, P, F32, P, P, P, P], I32),
         "dsa_attention_mass": ([D, P, P, P, P, P, P, P, I32, I32, F32, P, P, P, P], I32),
         "dsa_decode_plan": ([D, I32, ctypes.POINTER(I32), ctypes.POINTER(I32),
-                             ctypes.POINTER(I32), ctypes.POINTER(I32)], I32),
+                             ctypes.POINTER(I32), ctypes.POINTER(I32), ctypes.POINTER(I32)],
+                            I32),
         "dsa_decode_sparse_noalloc": ([D, P, P, P, P, P, P, P, F32, P, P, P, P], I32),
         "dsa_set_sparse_cluster": ([I32], I32),
         "dsa_get_sparse_cluster": ([], I32),
@@ -241,13 +242,13 @@ PLAN_DENSE, PLAN_SPARSE, PLAN_MASKED = 0, 1, 2
 
 def dsa_decode_plan(dims, mode: int):
     """(rows per CTA, max CTAs per (request, kv head), kernel launches per call,
-    warps per CTA) on the current device for dsa_decode_dense (mode 0),
-    dsa_decode_sparse (1) or dsa_decode_sparse_masked (2)."""
-    c, n, l, wp = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
-    _check(_load().dsa_decode_plan(ctypes.byref(dims), int(mode), ctypes.byref(c),
-                                   ctypes.byref(n), ctypes.byref(l), ctypes.byref(wp)),
-           "dsa_decode_plan")
-    return c.value, n.value, l.value, wp.value
+    warps per CTA, rows per tile) on the current device for dsa_decode_dense
+    (mode 0), dsa_decode_sparse (1) or dsa_decode_sparse_masked (2); calls with
+    the same plan sum in the same order."""
+    v = [ctypes.c_int32() for _ in range(5)]
+    _check(_load().dsa_decode_plan(ctypes.byref(dims), int(mode),
+                                   *[ctypes.byref(x) for x in v]), "dsa_decode_plan")
+    return tuple(x.value for x in v)
 
 
 def dsa_set_sparse_cluster(ctas: int) -> None:

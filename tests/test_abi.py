@@ -113,7 +113,7 @@ def test_null_pointers_rejected_before_launch():
                                         fake, fake, None, None, None, 0.1, fake, None, fake,
                                         None) == \
         dsa.DSA_ERR_UNSUPPORTED
-    assert lib.dsa_decode_plan(ctypes.byref(d), 3, None, None, None, None) == \
+    assert lib.dsa_decode_plan(ctypes.byref(d), 3, None, None, None, None, None) == \
         dsa.DSA_ERR_INVALID_ARG
     # eviction: a missing free-list counter, a negative capacity
     assert lib.dsa_evict_pages(D, fake, fake, fake, fake, fake, None, 4, fake,

@@ -77,7 +77,7 @@ def same_plan(bt):
     same warps, so that they sum in the same order."""
     ps = dsa.dsa_decode_plan(bt.dims, dsa.PLAN_SPARSE)
     pm = dsa.dsa_decode_plan(bt.dims, dsa.PLAN_MASKED)
-    return (ps[0], ps[1], ps[3]) == (pm[0], pm[1], pm[3])
+    return (ps[0], ps[1], ps[3], ps[4]) == (pm[0], pm[1], pm[3], pm[4])
 
 
 def run_both(w, mask=None, bh=None):
