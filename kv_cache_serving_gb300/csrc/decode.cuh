@@ -41,6 +41,12 @@ namespace dsa {
 // stage; the _BIG pair is the build of the fused call for batches of more than
 // two waves of units (more, smaller CTAs and tiles: more warps per SM overlap
 // the latency of the gathers; tensor-core tiles keep at least 16 rows).
+#ifndef DSA_DECODE_WARPS_BIG
+#define DSA_DECODE_WARPS_BIG 3
+#endif
+#ifndef DSA_DECODE_WARPS_BIG_MMA
+#define DSA_DECODE_WARPS_BIG_MMA 4
+#endif
 #ifndef DSA_DECODE_STAGE_BYTES_BIG
 #define DSA_DECODE_STAGE_BYTES_BIG 4096
 #endif
@@ -142,12 +148,13 @@ __device__ __forceinline__ int request_rows(const DecodeLaunch& a, int b, int hk
 #define DSA_DECODE_SPLIT_MIN_CTAS 5
 #endif
 // Resident CTAs per SM the compiler must allow for (register budget): the
-// split-staged builds are small enough in shared memory for several.
+// split-staged builds are small enough in shared memory for several; 0 leaves
+// the other builds to the compiler's own register choice.
 template <int D, typename KV, int G, bool QMIX, int NWARPS, int STAGE_BYTES>
 constexpr int decode_min_ctas() {
   return DecodeTiling<D, KV, G, QMIX && G >= 2, NWARPS, STAGE_BYTES>::kSplit
              ? DSA_DECODE_SPLIT_MIN_CTAS
-             : 1;
+             : 0;
 }
 
 template <int D, typename KV, int G, int MODE, bool QMIX, int NWARPS = DSA_DECODE_WARPS,
@@ -654,48 +661,60 @@ cudaError_t launch_decode_one(const DecodeLaunch& a, cudaStream_t s) {
     if (hd_ == 128 && g_ == 8) { BODY(128, 8) }   \
   } while (0)
 
-template <typename KV, int MODE, int NWARPS, int SB>
-cudaError_t launch_decode_dispatch(const DecodeLaunch& a, cudaStream_t s) {
-  const bool qmix = IsBf16<KV>::value && a.q_bf16 != 0;
-#define DSA_BODY(DD, GG)                                                                  \
-  return qmix ? launch_decode_one<DD, KV, GG, MODE, IsBf16<KV>::value, NWARPS, SB>(a, s)  \
-              : launch_decode_one<DD, KV, GG, MODE, false, NWARPS, SB>(a, s);
-  DSA_FOR_SHAPE(a.head_dim, a.hq / a.hkv, DSA_BODY);
-#undef DSA_BODY
-  return cudaErrorInvalidValue;
-}
-
-// The fused call with bf16 KV also has a big-batch build (its own warps per
-// CTA and stage size).
 // Stage bytes of the default build of a row mode.
 constexpr int default_stage_bytes(int mode) {
   return mode == kRowsDense ? DSA_DECODE_STAGE_BYTES_DENSE : DSA_DECODE_STAGE_BYTES;
 }
 
+// The fused call with bf16 KV also has a big-batch build: 4 KB stages and its
+// own warps per CTA (measured best: 3 on the CUDA-core engine, 4 with a
+// 5-CTA register budget on the split-staged tensor-core engine).
 template <typename KV>
-constexpr bool has_big_warps(int mode) {
-  return IsBf16<KV>::value && mode == kRowsMask &&
-         (DSA_DECODE_WARPS_BIG != DSA_DECODE_WARPS ||
-          DSA_DECODE_STAGE_BYTES_BIG != default_stage_bytes(mode));
+constexpr bool has_big_build(int mode) {
+  return IsBf16<KV>::value && mode == kRowsMask;
+}
+template <int G, bool QMIX, bool BIG>
+constexpr int build_warps() {
+  return !BIG ? DSA_DECODE_WARPS
+              : ((QMIX && G >= 2) ? DSA_DECODE_WARPS_BIG_MMA : DSA_DECODE_WARPS_BIG);
+}
+template <int MODE, bool BIG>
+constexpr int build_stage_bytes() {
+  return BIG ? DSA_DECODE_STAGE_BYTES_BIG : default_stage_bytes(MODE);
 }
 
-// One row mode: the default build, or for the fused call with bf16 KV the
-// DSA_DECODE_WARPS_BIG build when the plan asks for it.
+template <typename KV, int MODE, bool BIG>
+cudaError_t launch_decode_dispatch(const DecodeLaunch& a, cudaStream_t s) {
+  const bool qmix = IsBf16<KV>::value && a.q_bf16 != 0;
+  constexpr bool kQ = IsBf16<KV>::value;
+#define DSA_BODY(DD, GG)                                                                      \
+  return qmix ? launch_decode_one<DD, KV, GG, MODE, kQ, build_warps<GG, kQ, BIG>(),           \
+                                  build_stage_bytes<MODE, BIG>()>(a, s)                       \
+              : launch_decode_one<DD, KV, GG, MODE, false, build_warps<GG, false, BIG>(),     \
+                                  build_stage_bytes<MODE, BIG>()>(a, s);
+  DSA_FOR_SHAPE(a.head_dim, a.hq / a.hkv, DSA_BODY);
+#undef DSA_BODY
+  return cudaErrorInvalidValue;
+}
+
+// One row mode: the default build, or the big-batch build when the plan asks
+// for it (a.big) and there is one.
 template <typename KV, int MODE>
 cudaError_t launch_decode_mode(const DecodeLaunch& a, cudaStream_t s) {
-  if constexpr (has_big_warps<KV>(MODE))
-    if (a.big != 0)
-      return launch_decode_dispatch<KV, MODE, DSA_DECODE_WARPS_BIG, DSA_DECODE_STAGE_BYTES_BIG>(
-          a, s);
-  return launch_decode_dispatch<KV, MODE, DSA_DECODE_WARPS, default_stage_bytes(MODE)>(a, s);
+  if constexpr (has_big_build<KV>(MODE))
+    if (a.big != 0) return launch_decode_dispatch<KV, MODE, true>(a, s);
+  return launch_decode_dispatch<KV, MODE, false>(a, s);
 }
 
-template <typename KV, int MODE, int NWARPS, int SB>
-DecodeShape decode_shape_m(int head_dim, int group, bool big) {
-  DecodeShape r{0, 1, 1, NWARPS, 0, big};
+template <typename KV, int MODE, bool BIG>
+DecodeShape decode_shape_m(int head_dim, int group) {
+  DecodeShape r{0, 1, 1, DSA_DECODE_WARPS, 0, BIG};
+  constexpr bool kQ = IsBf16<KV>::value;
 #define DSA_BODY(DD, GG)                                                                   \
-  using Tl = DecodeTiling<DD, KV, GG, IsBf16<KV>::value && (GG >= 2), NWARPS, SB>;         \
-  auto kern = decode_kernel<DD, KV, GG, MODE, IsBf16<KV>::value, NWARPS, SB>;              \
+  constexpr int kNW = build_warps<GG, kQ, BIG>(), kSB = build_stage_bytes<MODE, BIG>();    \
+  using Tl = DecodeTiling<DD, KV, GG, kQ && (GG >= 2), kNW, kSB>;                          \
+  auto kern = decode_kernel<DD, KV, GG, MODE, kQ, kNW, kSB>;                               \
+  r.warps = kNW;                                                                           \
   r.rows_per_pass = Tl::NW * Tl::T;                                                        \
   r.tile_rows = Tl::T;                                                                     \
   r.cluster_limit = Tl::kMaxClusterHere;                                                   \
@@ -714,12 +733,9 @@ DecodeShape decode_shape_m(int head_dim, int group, bool big) {
 
 template <typename KV, int MODE>
 DecodeShape decode_shape_mode(int head_dim, int group, bool big) {
-  if constexpr (has_big_warps<KV>(MODE))
-    if (big)
-      return decode_shape_m<KV, MODE, DSA_DECODE_WARPS_BIG, DSA_DECODE_STAGE_BYTES_BIG>(
-          head_dim, group, true);
-  return decode_shape_m<KV, MODE, DSA_DECODE_WARPS, default_stage_bytes(MODE)>(head_dim, group,
-                                                                             false);
+  if constexpr (has_big_build<KV>(MODE))
+    if (big) return decode_shape_m<KV, MODE, true>(head_dim, group);
+  return decode_shape_m<KV, MODE, false>(head_dim, group);
 }
 
 }  // namespace dsa

@@ -108,13 +108,6 @@ int mass_ctas_per_sm(int head_dim, int group, bool kv_bf16, bool q_bf16);
 cudaError_t launch_compact(const CompactLaunch& a, cudaStream_t s);
 cudaError_t launch_evict(const EvictLaunch& a, cudaStream_t s);
 
-// Warps per CTA of the second build of the fused call (bf16 KV), chosen for
-// batches of many units (build-time knob shared by host and device code).
-#ifndef DSA_DECODE_WARPS_BIG
-#define DSA_DECODE_WARPS_BIG 4
-#endif
-constexpr int kDecodeWarpsBig = DSA_DECODE_WARPS_BIG;
-
 // Host-side facts about one build of the decode kernel, for the chunk choice.
 struct DecodeShape {
   int rows_per_pass;  // warps x tile rows
