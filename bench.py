@@ -59,12 +59,12 @@ FALLBACK_HBM_GBS = 6800.0
 # on the same batch; the summaries are under profiles/).  They describe the
 # kernel sources whose digest is `digest` and are reported as null otherwise.
 NCU_TRAFFIC = {
-    "digest": "d03d1dec811cf07f",
+    "digest": "bde1485b50de915d",
     "bytes": {
-        "llamagen-xl-like-24x24": 21432832,
-        "janus-pro-7b-like-32x32": 316642304,
-        "emu3-8b-like-90x90-gqa4": 3281920,
-        "mixed-serving-gqa4": 168031744,
+        "llamagen-xl-like-24x24": 21435136,
+        "janus-pro-7b-like-32x32": 316938752,
+        "emu3-8b-like-90x90-gqa4": 3282176,
+        "mixed-serving-gqa4": 168145152,
     },
 }
 
