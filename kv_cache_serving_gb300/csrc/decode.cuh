@@ -666,12 +666,12 @@ constexpr int default_stage_bytes(int mode) {
   return mode == kRowsDense ? DSA_DECODE_STAGE_BYTES_DENSE : DSA_DECODE_STAGE_BYTES;
 }
 
-// The fused call with bf16 KV also has a big-batch build: 4 KB stages and its
-// own warps per CTA (measured best: 3 on the CUDA-core engine, 4 with a
+// The sparse calls with bf16 KV also have a big-batch build: 4 KB stages and
+// their own warps per CTA (measured best: 3 on the CUDA-core engine, 4 with a
 // 5-CTA register budget on the split-staged tensor-core engine).
 template <typename KV>
 constexpr bool has_big_build(int mode) {
-  return IsBf16<KV>::value && mode == kRowsMask;
+  return IsBf16<KV>::value && mode != kRowsDense;
 }
 template <int G, bool QMIX, bool BIG>
 constexpr int build_warps() {

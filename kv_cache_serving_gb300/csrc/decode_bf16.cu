@@ -1,17 +1,19 @@
-// decode_bf16.cu -- bf16 KV instantiations of the decode kernel for dense rows
-// and kept lists, and the bf16 entry points (the fused mode's builds live in
-// decode_bf16_mask.cu so that the two compile in parallel).
+// decode_bf16.cu -- bf16 KV instantiations of the decode kernel for dense rows,
+// and the bf16 entry points (the kept-list and fused modes' builds live in
+// decode_bf16_list.cu and decode_bf16_mask.cu so that they compile in parallel).
 #include "decode.cuh"
 
 namespace dsa {
 
+cudaError_t launch_decode_bf16_list(const DecodeLaunch& a, cudaStream_t s);
+DecodeShape decode_shape_bf16_list(int head_dim, int group, bool big);
 cudaError_t launch_decode_bf16_mask(const DecodeLaunch& a, cudaStream_t s);
 DecodeShape decode_shape_bf16_mask(int head_dim, int group, bool big);
 
 cudaError_t launch_decode_bf16(const DecodeLaunch& a, int mode, cudaStream_t s) {
   switch (mode) {
     case kRowsDense: return launch_decode_mode<bf16_t, kRowsDense>(a, s);
-    case kRowsList: return launch_decode_mode<bf16_t, kRowsList>(a, s);
+    case kRowsList: return launch_decode_bf16_list(a, s);
     case kRowsMask: return launch_decode_bf16_mask(a, s);
   }
   return cudaErrorInvalidValue;
@@ -20,7 +22,7 @@ cudaError_t launch_decode_bf16(const DecodeLaunch& a, int mode, cudaStream_t s) 
 DecodeShape decode_shape_bf16(int head_dim, int group, int mode, bool big) {
   switch (mode) {
     case kRowsDense: return decode_shape_mode<bf16_t, kRowsDense>(head_dim, group, big);
-    case kRowsList: return decode_shape_mode<bf16_t, kRowsList>(head_dim, group, big);
+    case kRowsList: return decode_shape_bf16_list(head_dim, group, big);
     case kRowsMask: return decode_shape_bf16_mask(head_dim, group, big);
   }
   return DecodeShape{0, 1, 1, DSA_DECODE_WARPS, 0, false};

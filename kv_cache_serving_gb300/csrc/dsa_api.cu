@@ -173,10 +173,10 @@ Plan decode_plan(const dsa_dims* d, int mode) {
   const int64_t n_max = mode == kModeDense ? dense_rows(d) : d->max_kept;
   const int64_t units = static_cast<int64_t>(d->batch) * d->hkv;
   DecodeShape sh = decode_shape(d, mode, false);
-  // The fused call on a batch of more than two waves of units runs the build
-  // with fewer warps per CTA (when there is one): more, smaller CTAs per SM
-  // overlap one CTA's start-up with the others' streaming.
-  if (mode == kModeMask && units > 2 * static_cast<int64_t>(sm_count()) * sh.ctas_per_sm) {
+  // A sparse call on a batch of more than two waves of units runs the
+  // big-batch build (when there is one): smaller stages, more warps per SM to
+  // overlap the latency of the gathers.
+  if (mode != kModeDense && units > 2 * static_cast<int64_t>(sm_count()) * sh.ctas_per_sm) {
     const DecodeShape big = decode_shape(d, mode, true);
     if (big.big) sh = big;
   }
