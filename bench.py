@@ -59,12 +59,12 @@ FALLBACK_HBM_GBS = 6800.0
 # on the same batch; the summaries are under profiles/).  They describe the
 # kernel sources whose digest is `digest` and are reported as null otherwise.
 NCU_TRAFFIC = {
-    "digest": "bde1485b50de915d",
+    "digest": "6315e33b234cf141",
     "bytes": {
-        "llamagen-xl-like-24x24": 21435136,
-        "janus-pro-7b-like-32x32": 316938752,
-        "emu3-8b-like-90x90-gqa4": 3282176,
-        "mixed-serving-gqa4": 168145152,
+        "llamagen-xl-like-24x24": 21432832,
+        "janus-pro-7b-like-32x32": 316569088,
+        "emu3-8b-like-90x90-gqa4": 3282432,
+        "mixed-serving-gqa4": 168176896,
     },
 }
 
@@ -492,6 +492,14 @@ def run_ours(args):
                 "resident_kv_bytes_after": (mapped - evicted) * page_bytes,
                 "evict_us": 1e3 * e0.elapsed_time(e1)}
 
+    # attention mass: every K row of every request (no V), q, the bins and the
+    # per-offset weights (written as raw scores, then normalised by the merge)
+    elt = 2 if w["dtype"] == "bf16" else 4
+    om_bytes = w["batch"] * w["hq"] * (w["max_window"] + 1) * 4
+    mass_bytes = (int(w["seq_len"].astype(np.int64).sum()) * w["hkv"] * w["head_dim"] * elt
+                  + w["batch"] * w["hq"] * w["head_dim"] * elt + w["batch"] * w["hq"] * 16
+                  + 3 * om_bytes)
+
     B = w["batch"]
     step_s = t_step / K
     tokens = world * B / step_s
@@ -566,6 +574,9 @@ def run_ours(args):
             "dense_gbs": by["dense"] / (t_dense / K) / 1e9,
         },
         "attention_mass_ms": mass_ms,
+        "attention_mass_roofline": None if mass_ms is None else {
+            "bound": "hbm", "bytes": mass_bytes, "achieved": mass_bytes / (mass_ms * 1e-3) / 1e9,
+            "peak": peak, "unit": "GB/s", "frac": mass_bytes / (mass_ms * 1e-3) / 1e9 / peak},
         "eviction": eviction,
         "e2e": {"value": world * B / (t_e2e / K), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
