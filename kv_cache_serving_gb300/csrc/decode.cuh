@@ -50,6 +50,9 @@ namespace dsa {
 #ifndef DSA_DECODE_STAGE_BYTES_BIG
 #define DSA_DECODE_STAGE_BYTES_BIG 4096
 #endif
+#ifndef DSA_DECODE_WARPS_SMALL
+#define DSA_DECODE_WARPS_SMALL 5
+#endif
 #ifndef DSA_DECODE_STAGE_BYTES_DENSE
 #define DSA_DECODE_STAGE_BYTES_DENSE 4096  // dense rows: long, split into many chunks
 #endif
@@ -64,14 +67,14 @@ namespace dsa {
 #endif
 
 template <int D, typename KV, int G, bool MMA = false, int NWARPS = DSA_DECODE_WARPS,
-          int STAGE_BYTES = DSA_DECODE_STAGE_BYTES>
+          int STAGE_BYTES = DSA_DECODE_STAGE_BYTES, int STAGES = DSA_DECODE_STAGES>
 struct DecodeTiling {
   static constexpr int kElt = static_cast<int>(sizeof(KV));
   static constexpr int kRowBytes = D * kElt;
   static constexpr int kT0 = STAGE_BYTES / (2 * kRowBytes);  // K+V of one stage
   static constexpr int kTmin = MMA ? 16 : 8;  // whole 16-row mma blocks
   static constexpr int T = kT0 > 32 ? 32 : (kT0 < kTmin ? kTmin : kT0);
-  static constexpr int S = DSA_DECODE_STAGES;  // stages per warp
+  static constexpr int S = STAGES;             // stages per warp
   static constexpr int NW = NWARPS;            // warps per CTA
   static constexpr int kVE = 16 / kElt;        // elements per 16-byte vector
   static constexpr int kEPL = D / 8;           // elements of a row per lane
@@ -90,9 +93,13 @@ struct DecodeTiling {
   static constexpr int kWarpBytes = kSplit ? kStageBytes : S * kStageBytes;
   static constexpr int kBarOff = NW * kWarpBytes;
   static constexpr int kPsOff = kBarOff + NW * kBars * 8;  // [NW][hi, lo][8 heads][T] bf16
-  static constexpr int kSmem = kPsOff + (MMA ? NW * 2 * 8 * T * 2 : 0);
+  // End-of-CTA state of each warp, G x [acc(D), m, l] floats: at the start of
+  // the warp's own ring (idle by then) when it fits, else in a region of its own.
+  static constexpr int kSlotBytes = G * (D + 2) * 4;
+  static constexpr bool kSlotInRing = kSlotBytes <= kWarpBytes;
+  static constexpr int kSlotOff = kPsOff + (MMA ? NW * 2 * 8 * T * 2 : 0);
+  static constexpr int kSmem = kSlotOff + (kSlotInRing ? 0 : NW * kSlotBytes);
   // a warp's end-of-CTA state [G][D+2] floats reuses the start of its own ring
-  static_assert(G * (D + 2) * 4 <= kWarpBytes, "merge slot fits the ring");
   // Largest cluster whose merge buffer [cluster][G][D+2] floats fits the rings.
   static constexpr int kClusterFit = NW * kWarpBytes / (G * (D + 2) * 4);
   static constexpr int kMaxClusterHere = kClusterFit >= 8 ? 8 : kClusterFit >= 4 ? 4
@@ -150,19 +157,19 @@ __device__ __forceinline__ int request_rows(const DecodeLaunch& a, int b, int hk
 // Resident CTAs per SM the compiler must allow for (register budget): the
 // split-staged builds are small enough in shared memory for several; 0 leaves
 // the other builds to the compiler's own register choice.
-template <int D, typename KV, int G, bool QMIX, int NWARPS, int STAGE_BYTES>
+template <int D, typename KV, int G, bool QMIX, int NWARPS, int STAGE_BYTES, int STAGES>
 constexpr int decode_min_ctas() {
-  return DecodeTiling<D, KV, G, QMIX && G >= 2, NWARPS, STAGE_BYTES>::kSplit
+  return DecodeTiling<D, KV, G, QMIX && G >= 2, NWARPS, STAGE_BYTES, STAGES>::kSplit
              ? DSA_DECODE_SPLIT_MIN_CTAS
              : 0;
 }
 
 template <int D, typename KV, int G, int MODE, bool QMIX, int NWARPS = DSA_DECODE_WARPS,
-          int STAGE_BYTES = DSA_DECODE_STAGE_BYTES>
+          int STAGE_BYTES = DSA_DECODE_STAGE_BYTES, int STAGES = DSA_DECODE_STAGES>
 __global__ void __launch_bounds__(NWARPS * 32,
-                                  (decode_min_ctas<D, KV, G, QMIX, NWARPS, STAGE_BYTES>()))
+                                  (decode_min_ctas<D, KV, G, QMIX, NWARPS, STAGE_BYTES, STAGES>()))
     decode_kernel(const DecodeLaunch a) {
-  using Tl = DecodeTiling<D, KV, G, QMIX && G >= 2, NWARPS, STAGE_BYTES>;
+  using Tl = DecodeTiling<D, KV, G, QMIX && G >= 2, NWARPS, STAGE_BYTES, STAGES>;
   constexpr int T = Tl::T, S = Tl::S, NW = Tl::NW;
   constexpr int kRowBytes = Tl::kRowBytes;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -287,7 +294,10 @@ __global__ void __launch_bounds__(NWARPS * 32,
   uint16_t* ps = reinterpret_cast<uint16_t*>(smem + Tl::kPsOff) + warp * 2 * 8 * T;  // [2][8][T]
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Tl::kBarOff) + warp * Tl::kBars;
   // end-of-CTA state of warp w: [G][D+2] floats at the start of w's ring
-  auto mslot = [&](int w) { return reinterpret_cast<float*>(smem + w * Tl::kWarpBytes); };
+  auto mslot = [&](int w) {
+    return reinterpret_cast<float*>(
+        smem + (Tl::kSlotInRing ? w * Tl::kWarpBytes : Tl::kSlotOff + w * Tl::kSlotBytes));
+  };
 
   if (lane == 0) {
 #pragma unroll
@@ -617,10 +627,10 @@ struct IsBf16<bf16_t> {
   static constexpr bool value = true;
 };
 
-template <int D, typename KV, int G, int MODE, bool QMIX, int NWARPS, int SB>
+template <int D, typename KV, int G, int MODE, bool QMIX, int NWARPS, int SB, int ST>
 cudaError_t launch_decode_one(const DecodeLaunch& a, cudaStream_t s) {
-  using Tl = DecodeTiling<D, KV, G, QMIX && G >= 2, NWARPS, SB>;
-  auto kern = decode_kernel<D, KV, G, MODE, QMIX, NWARPS, SB>;
+  using Tl = DecodeTiling<D, KV, G, QMIX && G >= 2, NWARPS, SB, ST>;
+  auto kern = decode_kernel<D, KV, G, MODE, QMIX, NWARPS, SB, ST>;
   const int smem = Tl::kSmem;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -666,54 +676,66 @@ constexpr int default_stage_bytes(int mode) {
   return mode == kRowsDense ? DSA_DECODE_STAGE_BYTES_DENSE : DSA_DECODE_STAGE_BYTES;
 }
 
-// The sparse calls with bf16 KV also have a big-batch build: 4 KB stages and
-// their own warps per CTA (measured best: 3 on the CUDA-core engine, 4 with a
-// 5-CTA register budget on the split-staged tensor-core engine).
+// The sparse calls with bf16 KV have two builds besides the default one.
+// Big-batch build: 4 KB stages and its own warps per CTA (measured best: 3 on
+// the CUDA-core engine, 4 with a 5-CTA register budget on the split-staged
+// tensor-core engine).  Small-batch build: 5 warps of one 8 KB stage, so that
+// a batch that needs two waves of the default build runs in one.
 template <typename KV>
-constexpr bool has_big_build(int mode) {
-  return IsBf16<KV>::value && mode != kRowsDense;
+constexpr bool has_build(int mode, int build) {
+  return build == kBuildDefault || (IsBf16<KV>::value && mode != kRowsDense);
 }
-template <int G, bool QMIX, bool BIG>
+template <int G, bool QMIX, int BUILD>
 constexpr int build_warps() {
-  return !BIG ? DSA_DECODE_WARPS
-              : ((QMIX && G >= 2) ? DSA_DECODE_WARPS_BIG_MMA : DSA_DECODE_WARPS_BIG);
+  return BUILD == kBuildBig
+             ? ((QMIX && G >= 2) ? DSA_DECODE_WARPS_BIG_MMA : DSA_DECODE_WARPS_BIG)
+             : (BUILD == kBuildSmall ? DSA_DECODE_WARPS_SMALL : DSA_DECODE_WARPS);
 }
-template <int MODE, bool BIG>
+template <int MODE, int BUILD>
 constexpr int build_stage_bytes() {
-  return BIG ? DSA_DECODE_STAGE_BYTES_BIG : default_stage_bytes(MODE);
+  return BUILD == kBuildBig     ? DSA_DECODE_STAGE_BYTES_BIG
+         : BUILD == kBuildSmall ? DSA_DECODE_STAGE_BYTES
+                                : default_stage_bytes(MODE);
+}
+template <int BUILD>
+constexpr int build_stages() {
+  return BUILD == kBuildSmall ? 1 : DSA_DECODE_STAGES;
 }
 
-template <typename KV, int MODE, bool BIG>
+template <typename KV, int MODE, int BUILD>
 cudaError_t launch_decode_dispatch(const DecodeLaunch& a, cudaStream_t s) {
   const bool qmix = IsBf16<KV>::value && a.q_bf16 != 0;
   constexpr bool kQ = IsBf16<KV>::value;
+  constexpr int kSB = build_stage_bytes<MODE, BUILD>(), kST = build_stages<BUILD>();
 #define DSA_BODY(DD, GG)                                                                      \
-  return qmix ? launch_decode_one<DD, KV, GG, MODE, kQ, build_warps<GG, kQ, BIG>(),           \
-                                  build_stage_bytes<MODE, BIG>()>(a, s)                       \
-              : launch_decode_one<DD, KV, GG, MODE, false, build_warps<GG, false, BIG>(),     \
-                                  build_stage_bytes<MODE, BIG>()>(a, s);
+  return qmix ? launch_decode_one<DD, KV, GG, MODE, kQ, build_warps<GG, kQ, BUILD>(), kSB,    \
+                                  kST>(a, s)                                                  \
+              : launch_decode_one<DD, KV, GG, MODE, false, build_warps<GG, false, BUILD>(),   \
+                                  kSB, kST>(a, s);
   DSA_FOR_SHAPE(a.head_dim, a.hq / a.hkv, DSA_BODY);
 #undef DSA_BODY
   return cudaErrorInvalidValue;
 }
 
-// One row mode: the default build, or the big-batch build when the plan asks
-// for it (a.big) and there is one.
+// One row mode in the build the plan asks for (a.build), if there is one.
 template <typename KV, int MODE>
 cudaError_t launch_decode_mode(const DecodeLaunch& a, cudaStream_t s) {
-  if constexpr (has_big_build<KV>(MODE))
-    if (a.big != 0) return launch_decode_dispatch<KV, MODE, true>(a, s);
-  return launch_decode_dispatch<KV, MODE, false>(a, s);
+  if constexpr (has_build<KV>(MODE, kBuildBig))
+    if (a.build == kBuildBig) return launch_decode_dispatch<KV, MODE, kBuildBig>(a, s);
+  if constexpr (has_build<KV>(MODE, kBuildSmall))
+    if (a.build == kBuildSmall) return launch_decode_dispatch<KV, MODE, kBuildSmall>(a, s);
+  return launch_decode_dispatch<KV, MODE, kBuildDefault>(a, s);
 }
 
-template <typename KV, int MODE, bool BIG>
+template <typename KV, int MODE, int BUILD>
 DecodeShape decode_shape_m(int head_dim, int group) {
-  DecodeShape r{0, 1, 1, DSA_DECODE_WARPS, 0, BIG};
+  DecodeShape r{0, 1, 1, DSA_DECODE_WARPS, 0, BUILD};
   constexpr bool kQ = IsBf16<KV>::value;
+  constexpr int kSB = build_stage_bytes<MODE, BUILD>(), kST = build_stages<BUILD>();
 #define DSA_BODY(DD, GG)                                                                   \
-  constexpr int kNW = build_warps<GG, kQ, BIG>(), kSB = build_stage_bytes<MODE, BIG>();    \
-  using Tl = DecodeTiling<DD, KV, GG, kQ && (GG >= 2), kNW, kSB>;                          \
-  auto kern = decode_kernel<DD, KV, GG, MODE, kQ, kNW, kSB>;                               \
+  constexpr int kNW = build_warps<GG, kQ, BUILD>();                                        \
+  using Tl = DecodeTiling<DD, KV, GG, kQ && (GG >= 2), kNW, kSB, kST>;                     \
+  auto kern = decode_kernel<DD, KV, GG, MODE, kQ, kNW, kSB, kST>;                          \
   r.warps = kNW;                                                                           \
   r.rows_per_pass = Tl::NW * Tl::T;                                                        \
   r.tile_rows = Tl::T;                                                                     \
@@ -732,10 +754,12 @@ DecodeShape decode_shape_m(int head_dim, int group) {
 }
 
 template <typename KV, int MODE>
-DecodeShape decode_shape_mode(int head_dim, int group, bool big) {
-  if constexpr (has_big_build<KV>(MODE))
-    if (big) return decode_shape_m<KV, MODE, true>(head_dim, group);
-  return decode_shape_m<KV, MODE, false>(head_dim, group);
+DecodeShape decode_shape_mode(int head_dim, int group, int build) {
+  if constexpr (has_build<KV>(MODE, kBuildBig))
+    if (build == kBuildBig) return decode_shape_m<KV, MODE, kBuildBig>(head_dim, group);
+  if constexpr (has_build<KV>(MODE, kBuildSmall))
+    if (build == kBuildSmall) return decode_shape_m<KV, MODE, kBuildSmall>(head_dim, group);
+  return decode_shape_m<KV, MODE, kBuildDefault>(head_dim, group);
 }
 
 }  // namespace dsa

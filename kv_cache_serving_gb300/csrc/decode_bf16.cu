@@ -6,9 +6,9 @@
 namespace dsa {
 
 cudaError_t launch_decode_bf16_list(const DecodeLaunch& a, cudaStream_t s);
-DecodeShape decode_shape_bf16_list(int head_dim, int group, bool big);
+DecodeShape decode_shape_bf16_list(int head_dim, int group, int build);
 cudaError_t launch_decode_bf16_mask(const DecodeLaunch& a, cudaStream_t s);
-DecodeShape decode_shape_bf16_mask(int head_dim, int group, bool big);
+DecodeShape decode_shape_bf16_mask(int head_dim, int group, int build);
 
 cudaError_t launch_decode_bf16(const DecodeLaunch& a, int mode, cudaStream_t s) {
   switch (mode) {
@@ -19,13 +19,13 @@ cudaError_t launch_decode_bf16(const DecodeLaunch& a, int mode, cudaStream_t s) 
   return cudaErrorInvalidValue;
 }
 
-DecodeShape decode_shape_bf16(int head_dim, int group, int mode, bool big) {
+DecodeShape decode_shape_bf16(int head_dim, int group, int mode, int build) {
   switch (mode) {
-    case kRowsDense: return decode_shape_mode<bf16_t, kRowsDense>(head_dim, group, big);
-    case kRowsList: return decode_shape_bf16_list(head_dim, group, big);
-    case kRowsMask: return decode_shape_bf16_mask(head_dim, group, big);
+    case kRowsDense: return decode_shape_mode<bf16_t, kRowsDense>(head_dim, group, build);
+    case kRowsList: return decode_shape_bf16_list(head_dim, group, build);
+    case kRowsMask: return decode_shape_bf16_mask(head_dim, group, build);
   }
-  return DecodeShape{0, 1, 1, DSA_DECODE_WARPS, 0, false};
+  return DecodeShape{0, 1, 1, DSA_DECODE_WARPS, 0, kBuildDefault};
 }
 
 }  // namespace dsa

@@ -8,8 +8,8 @@ cudaError_t launch_decode_bf16_list(const DecodeLaunch& a, cudaStream_t s) {
   return launch_decode_mode<bf16_t, kRowsList>(a, s);
 }
 
-DecodeShape decode_shape_bf16_list(int head_dim, int group, bool big) {
-  return decode_shape_mode<bf16_t, kRowsList>(head_dim, group, big);
+DecodeShape decode_shape_bf16_list(int head_dim, int group, int build) {
+  return decode_shape_mode<bf16_t, kRowsList>(head_dim, group, build);
 }
 
 }  // namespace dsa

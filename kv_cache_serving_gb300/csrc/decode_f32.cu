@@ -29,13 +29,13 @@ cudaError_t launch_merge(const DecodeLaunch& a, int mode, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-DecodeShape decode_shape_f32(int head_dim, int group, int mode, bool big) {
+DecodeShape decode_shape_f32(int head_dim, int group, int mode, int build) {
   switch (mode) {
-    case kRowsDense: return decode_shape_mode<float, kRowsDense>(head_dim, group, big);
-    case kRowsList: return decode_shape_mode<float, kRowsList>(head_dim, group, big);
-    case kRowsMask: return decode_shape_mode<float, kRowsMask>(head_dim, group, big);
+    case kRowsDense: return decode_shape_mode<float, kRowsDense>(head_dim, group, build);
+    case kRowsList: return decode_shape_mode<float, kRowsList>(head_dim, group, build);
+    case kRowsMask: return decode_shape_mode<float, kRowsMask>(head_dim, group, build);
   }
-  return DecodeShape{0, 1, 1, DSA_DECODE_WARPS, 0, false};
+  return DecodeShape{0, 1, 1, DSA_DECODE_WARPS, 0, kBuildDefault};
 }
 
 }  // namespace dsa

@@ -148,8 +148,7 @@ size_t unit_ints_region(const dsa_dims* d) {
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 struct Plan {
-  int chunk, num_chunks, quantum, per_sm, cluster, warps, tile_rows;
-  bool big;
+  int chunk, num_chunks, quantum, per_sm, cluster, warps, tile_rows, build;
 };
 
 // Automatic cluster size: a CTA's fixed latency (first copies, end-of-CTA
@@ -163,29 +162,35 @@ int sparse_cluster_auto(int64_t units, int64_t slots) {
   return best;
 }
 
-DecodeShape decode_shape(const dsa_dims* d, int mode, bool big) {
+DecodeShape decode_shape(const dsa_dims* d, int mode, int build) {
   const int g = d->hq / d->hkv;
-  return d->kv_dtype == DSA_BF16 ? decode_shape_bf16(d->head_dim, g, mode, big)
-                                 : decode_shape_f32(d->head_dim, g, mode, big);
+  return d->kv_dtype == DSA_BF16 ? decode_shape_bf16(d->head_dim, g, mode, build)
+                                 : decode_shape_f32(d->head_dim, g, mode, build);
 }
 
 Plan decode_plan(const dsa_dims* d, int mode) {
   const int64_t n_max = mode == kModeDense ? dense_rows(d) : d->max_kept;
   const int64_t units = static_cast<int64_t>(d->batch) * d->hkv;
-  DecodeShape sh = decode_shape(d, mode, false);
-  // A sparse call on a batch of more than two waves of units runs the
-  // big-batch build (when there is one): smaller stages, more warps per SM to
-  // overlap the latency of the gathers.
-  if (mode != kModeDense && units > 2 * static_cast<int64_t>(sm_count()) * sh.ctas_per_sm) {
-    const DecodeShape big = decode_shape(d, mode, true);
-    if (big.big) sh = big;
+  DecodeShape sh = decode_shape(d, mode, kBuildDefault);
+  const int64_t slots = static_cast<int64_t>(sm_count()) * sh.ctas_per_sm;
+  if (mode != kModeDense && units > 2 * slots) {
+    // more than two waves of units: the big-batch build (smaller stages, more
+    // warps per SM to overlap the latency of the gathers), when there is one
+    const DecodeShape big = decode_shape(d, mode, kBuildBig);
+    if (big.build == kBuildBig) sh = big;
+  } else if (mode != kModeDense && units > slots) {
+    // two waves of the default build: the small-batch build if it takes the
+    // whole batch in one wave
+    const DecodeShape small = decode_shape(d, mode, kBuildSmall);
+    if (small.build == kBuildSmall && units <= static_cast<int64_t>(sm_count()) * small.ctas_per_sm)
+      sh = small;
   }
   Plan p{};
   p.quantum = sh.rows_per_pass;
   p.per_sm = sh.ctas_per_sm;
   p.warps = sh.warps;
   p.tile_rows = sh.tile_rows;
-  p.big = sh.big;
+  p.build = sh.build;
   p.cluster = 1;
   int ncl = g_sparse_cluster.load(std::memory_order_relaxed);
   if (ncl == 0) ncl = sparse_cluster_auto(units, sm_count() * p.per_sm);
@@ -265,7 +270,7 @@ dsa_status decode_common(const dsa_dims* d, int mode, const void* q, const void*
   a.num_chunks = plan.num_chunks;
   a.cluster = plan.cluster;
   a.warps = plan.warps;
-  a.big = plan.big ? 1 : 0;
+  a.build = plan.build;
   a.scale_log2 = scale * kLog2e;
   a.out = out;
   a.lse = lse;

@@ -36,7 +36,7 @@ struct DecodeLaunch {
   int32_t chunk, num_chunks;
   int32_t cluster;   // > 1: the num_chunks (== cluster) CTAs of a unit merge in a cluster
   int32_t warps;     // warps per CTA of the build to launch (see DecodeShape)
-  int32_t big;       // 1: the big-batch build of the fused call (see DecodeShape)
+  int32_t build;     // kBuildDefault / kBuildBig / kBuildSmall (see DecodeShape)
   float scale_log2;  // softmax scale * log2(e)
   float* out;
   float* lse;
@@ -108,6 +108,12 @@ int mass_ctas_per_sm(int head_dim, int group, bool kv_bf16, bool q_bf16);
 cudaError_t launch_compact(const CompactLaunch& a, cudaStream_t s);
 cudaError_t launch_evict(const EvictLaunch& a, cudaStream_t s);
 
+// Builds of the decode kernel.  The sparse calls with bf16 KV have two more
+// besides the default: one for batches of more than two waves of units (more
+// warps per SM), one for batches that fit one wave only with it (5 warps of a
+// single stage, each warp about one tile of a unit).
+enum : int { kBuildDefault = 0, kBuildBig = 1, kBuildSmall = 2 };
+
 // Host-side facts about one build of the decode kernel, for the chunk choice.
 struct DecodeShape {
   int rows_per_pass;  // warps x tile rows
@@ -115,11 +121,11 @@ struct DecodeShape {
   int cluster_limit;  // largest cluster whose merge buffer fits the rings
   int warps;          // warps per CTA of this build
   int tile_rows;      // rows per tile of this build
-  bool big;           // this is the big-batch build
+  int build;          // which build this is
 };
-// The big-batch build of (head_dim, group, mode) when `big` and there is one
-// (the fused call with bf16 KV), else the default build.
-DecodeShape decode_shape_bf16(int head_dim, int group, int mode, bool big);
-DecodeShape decode_shape_f32(int head_dim, int group, int mode, bool big);
+// The requested build of (head_dim, group, mode) when there is one, else the
+// default build.
+DecodeShape decode_shape_bf16(int head_dim, int group, int mode, int build);
+DecodeShape decode_shape_f32(int head_dim, int group, int mode, int build);
 
 }  // namespace dsa
