@@ -1,5 +1,5 @@
-// decode.cuh -- split-KV flash-decode over a paged KV cache (sparse kept list or
-// dense causal range), and the log-sum-exp merge of its per-chunk partials.
+// decode.cuh -- split-KV flash-decode over a paged KV cache, and the
+// log-sum-exp merge of its per-chunk partials.
 //
 // Method: softmax(q K^T * scale) V of one decode query per (request, head) over
 // the rows of the kept set -- the masked attention of "Understanding and
@@ -7,25 +7,34 @@
 // paper-daily summary, section 核心公式 (core formula), with masked entries
 // skipped rather than zeroed (arXiv abstract: KV entries are skipped).
 //
+// Row sources (template MODE): dense rows 0..L-1; the kept list written by
+// dsa_build_index; or the kept set read straight from the keep mask (each lane
+// holds one 32-bit word of the window's mask bits and a prefix count, and finds
+// the row of a list position by a binary search over the lanes plus a
+// rank-select inside the word -- no kept list in memory).
+//
 // Work decomposition: grid (chunk, kv head, request).  A CTA owns `chunk`
 // consecutive entries of the row list of one (request, kv head) and all G query
 // heads of that kv head (grouped-query attention shares the rows).  Its NW
-// warps take tiles of T rows round-robin.  Each warp runs its own S-stage
+// warps take tiles of T rows round-robin.  Each warp runs its own
 // shared-memory ring: lanes issue one bulk async copy per K row and per V row
-// (the row's page comes from the page table), completing on the stage's
-// mbarrier; compute never waits for anything but its own copies.
+// (the row's page comes from the page table, loaded a tile ahead; the kept
+// row two tiles ahead), completing on the stage's mbarrier with the expected
+// byte count; compute never waits for anything but its own copies.  Either S
+// stages of K and V, or -- for 16-row tensor-core tiles too large for the
+// stage size -- one K buffer and one V buffer refilled as soon as their half
+// of the tile is computed.  The per-tile arithmetic (CUDA-core or tensor-core
+// engine) is WarpAttn (warp_attn.cuh).
 //
-// Per tile a warp works on 4 rows at a time: lane (g = lane/8, j = lane%8)
-// handles rows g, g+4, ... of the tile and 16-byte vectors j, j+8, ... of each
-// row (byte offsets 16 j + 128 u: conflict-free shared loads).  A row's G dot
-// products are summed over its 8 lanes by a 3-step butterfly, so every lane
-// holds the scores of its own rows; with bf16 q and K the products use the
-// mixed-precision fma.rn.f32.bf16 (bf16 x bf16 exact, fp32 accumulation).  The
-// online softmax runs in the log2 domain (scores times scale*log2 e); p_j v_j
-// accumulates into per-lane fp32 partial sums over the lane's rows, and the 4
-// row groups are summed once, at the end.  The CTA merges its warps' (m, l,
-// acc) in shared memory and either writes the final output (one chunk) or a
-// partial that merge_kernel combines.
+// End of a CTA: the warps' (m, l, acc) merge in shared memory; the CTA then
+// writes the output (one chunk), a partial for merge_kernel (several chunks),
+// or -- when the CTAs of a (request, kv head) form a thread-block cluster --
+// its state into the first CTA's shared memory for an in-cluster merge.
+//
+// Builds (warps per CTA, stage bytes, stages) are template parameters: the
+// default one, and for the sparse calls with bf16 KV a big-batch build (more
+// warps per SM) and a small-batch build (one wave of CTAs); the host plan
+// picks one per call.
 #pragma once
 
 #include <math.h>
