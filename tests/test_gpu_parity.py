@@ -225,6 +225,27 @@ def test_workload_full_size_sampled(name):
     run_both(w, mask=mask, bh=bh)
 
 
+@pytest.mark.parametrize("name,batch", [("mixed-serving", 64), ("janus-pro-7b", 20),
+                                        ("llamagen-xl", 24)])
+def test_small_batch_build(name, batch):
+    """Batches that need two waves of the default build: the small-batch build
+    (5 warps, one stage) where it fits them in one wave, kept lists and the
+    fused call, sampled pairs vs the oracle."""
+    w = wl.generate(wl.scaled(wl.WORKLOADS[name], batch=batch))
+    mask = top_mass_masks_from_oracle(w) if w["keep_mask"] is None else None
+    bt = DecodeBatch.from_workload(w, keep_mask=mask)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    plan = dsa.dsa_decode_plan(bt.dims, dsa.PLAN_MASKED)
+    if sms == 152 and w["hq"] == w["hkv"]:
+        # CUDA-core engine, 480-640 units: two waves of 3 CTAs/SM, one of the small
+        # build (on the tensor-core engine it holds no more CTAs, so the plan keeps
+        # the default build there)
+        assert plan[3] == 5, plan
+    rng = np.random.default_rng(7 + batch)
+    bh = [(int(rng.integers(w["batch"])), int(rng.integers(w["hq"]))) for _ in range(40)]
+    run_both(w, mask=mask, bh=bh)
+
+
 # ---------------------------------------------------------------------------
 # invariants and edge cases
 # ---------------------------------------------------------------------------
