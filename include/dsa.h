@@ -200,6 +200,47 @@ dsa_status dsa_decode_sparse_masked(const dsa_dims* dims, const void* q, void* k
                                     void* ws, void* stream);
 
 /*
+ * dsa_host_io -- the host side of one decode step: a contiguous block of inputs
+ * copied up before the attention and a contiguous block of results copied back
+ * after it, both issued by the call itself on its stream.
+ *   host_in   host memory, in_bytes, the source of the upload; pinned
+ *             (page-locked) for the copy to be asynchronous
+ *   dev_in    device memory, in_bytes, the destination of the upload (the
+ *             call's device inputs normally point into it)
+ *   dev_out   device memory, out_bytes, the source of the download (normally
+ *             holding the call's out and lse)
+ *   host_out  host memory, out_bytes, the destination of the download; pinned
+ * A size of 0 skips that copy (its two pointers may then be NULL).  The caller
+ * owns all four buffers; the library keeps no pointer after the call returns.
+ */
+typedef struct {
+  const void* host_in;
+  void* dev_in;
+  size_t in_bytes;
+  const void* dev_out;
+  void* host_out;
+  size_t out_bytes;
+} dsa_host_io;
+
+/*
+ * dsa_decode_sparse_masked_io -- one decode step from host memory in one call:
+ * on `stream`, the upload host_in -> dev_in, then exactly the work of
+ * dsa_decode_sparse_masked on the remaining (device) arguments, then the
+ * download dev_out -> host_out.  Everything is asynchronous; host_out holds the
+ * results once the stream has passed the call (e.g. cudaStreamSynchronize).
+ * All arguments are checked before the upload: a call that returns
+ * DSA_ERR_INVALID_ARG or DSA_ERR_UNSUPPORTED has issued nothing.  A failed copy
+ * returns DSA_ERR_CUDA.  io must not be NULL.
+ */
+dsa_status dsa_decode_sparse_masked_io(const dsa_host_io* io, const dsa_dims* dims,
+                                       const void* q, void* k_pages, void* v_pages,
+                                       const int32_t* page_table, const int32_t* seq_len,
+                                       const int32_t* prompt_len, const int32_t* window,
+                                       const uint32_t* keep_mask, const int32_t* request_order,
+                                       const void* k_new, const void* v_new, float scale,
+                                       float* out, float* lse, void* ws, void* stream);
+
+/*
  * dsa_decode_dense -- the dense causal baseline: the same as dsa_decode_sparse
  * with K(b,hk) = {0 .. L_b - 1} (the T_dense of the summary's speedup
  * T_dense / T_sparse, section 核心公式).  Arguments as above.

@@ -101,11 +101,18 @@ int sm_count() {
 
 // Rows per CTA: enough CTAs for `waves` waves of resident CTAs, at most
 // kMaxChunks chunks per (request, kv head), a multiple of the CTA's rows per pass.
+// With `whole_split` a unit is cut into floor(target / units) equal chunks (at
+// least one): n_max is only a bound on a unit's rows, so a cut sized from it
+// would add CTAs (and a merge launch) past the wave without shortening any.
 void choose_chunks(int64_t n_max, int64_t units, int resident, int quantum, int waves,
-                   int* chunk, int* num_chunks) {
+                   bool whole_split, int* chunk, int* num_chunks) {
   if (quantum < kChunkQuantum) quantum = kChunkQuantum;
   const int64_t target = static_cast<int64_t>(waves) * resident;
   int64_t c = ceil_div(n_max * units, target > 0 ? target : 1);
+  if (whole_split) {
+    const int64_t k = units > 0 ? target / units : 1;
+    c = ceil_div(n_max, k > 1 ? k : 1);
+  }
   const int64_t lo = ceil_div(n_max, kMaxChunks);
   if (c < lo) c = lo;
   c = ceil_div(c, quantum) * quantum;
@@ -203,8 +210,8 @@ Plan decode_plan(const dsa_dims* d, int mode) {
     return p;
   }
   choose_chunks(n_max, units, sm_count() * p.per_sm, p.quantum,
-                mode == kModeDense ? DSA_DENSE_WAVES : DSA_SPARSE_WAVES, &p.chunk,
-                &p.num_chunks);
+                mode == kModeDense ? DSA_DENSE_WAVES : DSA_SPARSE_WAVES, mode != kModeDense,
+                &p.chunk, &p.num_chunks);
   return p;
 }
 
@@ -221,10 +228,17 @@ struct RowSource {
   const void* v_new = nullptr;
 };
 
+dsa_status decode_launch(const dsa_dims* d, int mode, const void* q, const void* k,
+                         const void* v, const int32_t* page_table, const int32_t* seq_len,
+                         const RowSource& rs, float scale, float* out, float* lse, void* ws,
+                         cudaStream_t s);
+
+// Checks a decode call's arguments, then (with io) the host-to-device copy, the
+// launches and (with io) the device-to-host copy, in that order on the stream.
 dsa_status decode_common(const dsa_dims* d, int mode, const void* q, const void* k,
                          const void* v, const int32_t* page_table, const int32_t* seq_len,
                          const RowSource& rs, float scale, float* out, float* lse, void* ws,
-                         void* stream) {
+                         void* stream, const dsa_host_io* io = nullptr) {
   const dsa_status st = check_dims(d);
   if (st != DSA_OK) return st;
   if (!q || !k || !v || !page_table || !seq_len || !out || !ws) return DSA_ERR_INVALID_ARG;
@@ -238,7 +252,30 @@ dsa_status decode_common(const dsa_dims* d, int mode, const void* q, const void*
   if (!(scale == scale) || !aligned(ws, 256) || !aligned(k, 16) || !aligned(v, 16) ||
       !aligned(q, 16))
     return DSA_ERR_INVALID_ARG;
-  if (d->batch == 0) return DSA_OK;
+  if (io != nullptr && ((io->in_bytes > 0 && (!io->host_in || !io->dev_in)) ||
+                        (io->out_bytes > 0 && (!io->dev_out || !io->host_out))))
+    return DSA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (io != nullptr && io->in_bytes > 0 &&
+      cudaMemcpyAsync(io->dev_in, io->host_in, io->in_bytes, cudaMemcpyHostToDevice, s) !=
+          cudaSuccess)
+    return DSA_ERR_CUDA;
+  const dsa_status rc = d->batch == 0 ? DSA_OK
+                                      : decode_launch(d, mode, q, k, v, page_table, seq_len, rs,
+                                                      scale, out, lse, ws, s);
+  if (rc != DSA_OK) return rc;
+  if (io != nullptr && io->out_bytes > 0 &&
+      cudaMemcpyAsync(io->host_out, io->dev_out, io->out_bytes, cudaMemcpyDeviceToHost, s) !=
+          cudaSuccess)
+    return DSA_ERR_CUDA;
+  return DSA_OK;
+}
+
+// The launches of one decode call (arguments already checked, batch >= 1).
+dsa_status decode_launch(const dsa_dims* d, int mode, const void* q, const void* k,
+                         const void* v, const int32_t* page_table, const int32_t* seq_len,
+                         const RowSource& rs, float scale, float* out, float* lse, void* ws,
+                         cudaStream_t s) {
   const bool kv_bf16 = d->kv_dtype == DSA_BF16;
   const Plan plan = decode_plan(d, mode);
   DecodeLaunch a{};
@@ -276,7 +313,6 @@ dsa_status decode_common(const dsa_dims* d, int mode, const void* q, const void*
   a.lse = lse;
   a.part = partials(ws);
   a.err = err_word(ws);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = kv_bf16 ? launch_decode_bf16(a, mode, s) : launch_decode_f32(a, mode, s);
   if (e != cudaSuccess) return DSA_ERR_CUDA;
   if (a.cluster > 1) return DSA_OK;  // merged inside the clusters
@@ -391,6 +427,25 @@ dsa_status dsa_decode_sparse_masked(const dsa_dims* dims, const void* q, void* k
                        lse, ws, stream);
 }
 
+dsa_status dsa_decode_sparse_masked_io(const dsa_host_io* io, const dsa_dims* dims,
+                                       const void* q, void* k_pages, void* v_pages,
+                                       const int32_t* page_table, const int32_t* seq_len,
+                                       const int32_t* prompt_len, const int32_t* window,
+                                       const uint32_t* keep_mask, const int32_t* request_order,
+                                       const void* k_new, const void* v_new, float scale,
+                                       float* out, float* lse, void* ws, void* stream) {
+  if (io == nullptr) return DSA_ERR_INVALID_ARG;
+  RowSource rs;
+  rs.prompt_len = prompt_len;
+  rs.window = window;
+  rs.keep_mask = keep_mask;
+  rs.order = request_order;
+  rs.k_new = k_new;
+  rs.v_new = v_new;
+  return decode_common(dims, kModeMask, q, k_pages, v_pages, page_table, seq_len, rs, scale, out,
+                       lse, ws, stream, io);
+}
+
 dsa_status dsa_decode_dense(const dsa_dims* dims, const void* q, const void* k_pages,
                             const void* v_pages, const int32_t* page_table,
                             const int32_t* seq_len, float scale, float* out, float* lse,
@@ -439,7 +494,7 @@ dsa_status dsa_attention_mass(const dsa_dims* dims, const void* q, const void* k
                 sm_count() * mass_ctas_per_sm(dims->head_dim, g, kv_bf16, q_bf16),
                 mass_rows_per_pass(dims->head_dim, g, kv_bf16, q_bf16),
                 mass_uses_tensor_cores(kv_bf16, q_bf16, g) ? DSA_MASS_WAVES_MMA : DSA_MASS_WAVES,
-                &a.chunk, &a.num_chunks);
+                false, &a.chunk, &a.num_chunks);
   a.scale_log2 = scale * kLog2e;
   a.mass = mass;
   a.offset_mass = offset_mass;

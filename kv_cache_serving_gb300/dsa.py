@@ -38,6 +38,12 @@ class dsa_dims(ctypes.Structure):
         "max_window", "mask_words", "max_kept", "q_dtype", "kv_dtype")]
 
 
+class dsa_host_io(ctypes.Structure):
+    _fields_ = [("host_in", ctypes.c_void_p), ("dev_in", ctypes.c_void_p),
+                ("in_bytes", ctypes.c_size_t), ("dev_out", ctypes.c_void_p),
+                ("host_out", ctypes.c_void_p), ("out_bytes", ctypes.c_size_t)]
+
+
 _lib = None
 _lib_path = None
 
@@ -67,6 +73,8 @@ def _load():
         "dsa_decode_sparse": ([D, P, P, P, P, P, P, P, F32, P, P, P, P], I32),
         "dsa_evict_pages": ([D, P, P, P, P, P, P, I32, P, P], I32),
         "dsa_decode_sparse_masked": ([D, P, P, P, P, P, P, P, P, P, P, P, F32, P, P, P, P], I32),
+        "dsa_decode_sparse_masked_io": ([ctypes.POINTER(dsa_host_io), D, P, P, P, P, P, P, P, P,
+                                         P, P, P, F32, P, P, P, P], I32),
         "dsa_decode_dense": ([D, P, P, P, P, P, F32, P, P, P, P], I32),
         "dsa_attention_mass": ([D, P, P, P, P, P, P, P, I32, I32, F32, P, P, P, P], I32),
         "dsa_decode_plan": ([D, I32, ctypes.POINTER(I32), ctypes.POINTER(I32),
@@ -201,6 +209,64 @@ def dsa_decode_sparse_masked(dims, q, k_pages, v_pages, page_table, seq_len, pro
         _ptr(v_new, _QKV, "v_new"), float(scale),
         _ptr(out, torch.float32, "out"), _ptr(lse, torch.float32, "lse"), _ptr(ws),
         _stream(stream)), "dsa_decode_sparse_masked")
+
+
+class Prepared:
+    """One C call with its arguments marshalled once; calling the object issues
+    it again with the same pointers (the tensors must stay alive and in place)."""
+
+    def __init__(self, name: str, args: tuple, keep: tuple = ()):
+        self._fn = getattr(_load(), name)
+        self._name = name
+        self._args = args
+        self._keep = keep  # objects the marshalled pointers refer to
+
+    def __call__(self):
+        status = self._fn(*self._args)
+        if status != DSA_OK:
+            raise DSAError(status, self._name)
+
+
+def host_io(host_in, dev_in, dev_out, host_out) -> dsa_host_io:
+    """dsa_host_io over two host tensors (pinned, CPU) and two CUDA tensors:
+    host_in -> dev_in before the call, dev_out -> host_out after it."""
+    for t, cuda, what in ((host_in, False, "host_in"), (dev_in, True, "dev_in"),
+                          (dev_out, True, "dev_out"), (host_out, False, "host_out")):
+        if not isinstance(t, torch.Tensor) or t.is_cuda != cuda or not t.is_contiguous():
+            raise TypeError(f"{what} must be a contiguous {'CUDA' if cuda else 'host'} tensor")
+    nin = host_in.numel() * host_in.element_size()
+    nout = dev_out.numel() * dev_out.element_size()
+    if dev_in.numel() * dev_in.element_size() != nin or \
+            host_out.numel() * host_out.element_size() != nout:
+        raise ValueError("host_io: the two buffers of a copy differ in size")
+    return dsa_host_io(host_in.data_ptr(), dev_in.data_ptr(), nin, dev_out.data_ptr(),
+                       host_out.data_ptr(), nout)
+
+
+def dsa_decode_sparse_masked_io(io, dims, q, k_pages, v_pages, page_table, seq_len, prompt_len,
+                                window, keep_mask, scale, out, lse, ws, stream=None,
+                                request_order=None, k_new=None, v_new=None, prepare=False):
+    """dsa_decode_sparse_masked with the step's host copies in the same call: io
+    (a dsa_host_io, see host_io) is uploaded before the attention and downloaded
+    after it, on the same stream.  With prepare=True nothing is issued: the
+    return value is a Prepared call that issues it each time it is called."""
+    if not isinstance(io, dsa_host_io):
+        raise TypeError("io must be a dsa_host_io")
+    args = (ctypes.byref(io), ctypes.byref(dims), _ptr(q, _QKV, "q"),
+            _ptr(k_pages, _QKV, "k_pages"), _ptr(v_pages, _QKV, "v_pages"),
+            _ptr(page_table, _I32, "page_table"), _ptr(seq_len, _I32, "seq_len"),
+            _ptr(prompt_len, _I32, "prompt_len"), _ptr(window, _I32, "window"),
+            _ptr(keep_mask, _MASK, "keep_mask"), _ptr(request_order, _I32, "request_order"),
+            _ptr(k_new, _QKV, "k_new"), _ptr(v_new, _QKV, "v_new"), float(scale),
+            _ptr(out, torch.float32, "out"), _ptr(lse, torch.float32, "lse"), _ptr(ws),
+            _stream(stream))
+    call = Prepared("dsa_decode_sparse_masked_io", args,
+                    (io, dims, q, k_pages, v_pages, page_table, seq_len, prompt_len, window,
+                     keep_mask, request_order, k_new, v_new, out, lse, ws, stream))
+    if prepare:
+        return call
+    call()
+    return None
 
 
 def dsa_decode_sparse_noalloc(dims, q, k_pages, v_pages, page_table, seq_len, kept_idx,

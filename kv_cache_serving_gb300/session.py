@@ -79,6 +79,11 @@ class PackedIO:
     def download(self):
         self.host_out.copy_(self.dev_out, non_blocking=True)
 
+    def descriptor(self) -> dsa.dsa_host_io:
+        """The two copies as a dsa_host_io, for the calls that issue them
+        themselves (dsa_decode_sparse_masked_io)."""
+        return dsa.host_io(self.host_in, self.dev_in, self.dev_out, self.host_out)
+
 
 class DecodeBatch:
     def __init__(self, *, q, k_pages, v_pages, page_table, seq_len, prompt_len, window,
@@ -155,6 +160,18 @@ class DecodeBatch:
                                      self.keep_mask, self.scale, out, lse, self.ws, stream,
                                      request_order, k_new, v_new)
         return out, lse
+
+    def decode_step_io(self, io: PackedIO, request_order=None, stream=None, k_pages=None,
+                       v_pages=None, prepare=False):
+        """One step from host memory in one C call: io's inputs up, the fused
+        sparse decode, out and lse back into io.host.  The batch must have been
+        packed by pack_io(io); k_pages / v_pages default to the batch's cache.
+        With prepare=True returns a dsa.Prepared that issues the step per call."""
+        return dsa.dsa_decode_sparse_masked_io(
+            io.descriptor(), self.dims, self.q, self.k_pages if k_pages is None else k_pages,
+            self.v_pages if v_pages is None else v_pages, self.page_table, self.seq_len,
+            self.prompt_len, self.window, self.keep_mask, self.scale, self.out, self.lse, self.ws,
+            stream, request_order, prepare=prepare)
 
     def longest_first_order(self):
         """Requests by decreasing estimated kept rows: the request_order that

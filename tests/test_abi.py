@@ -122,3 +122,37 @@ def test_null_pointers_rejected_before_launch():
                                None) == dsa.DSA_ERR_INVALID_ARG
     code = ctypes.c_int32(0)
     assert lib.dsa_get_device_error(None, None, ctypes.byref(code)) == dsa.DSA_ERR_INVALID_ARG
+
+
+def test_host_io_call_checks_before_copying():
+    """dsa_decode_sparse_masked_io rejects a bad call before its upload: no io,
+    an io copy without its buffers, or bad decode arguments (the fake pointers
+    are never dereferenced, so nothing reaches a GPU)."""
+    lib = dsa._load()
+    d = dsa.make_dims(2, 8, 4, 128, 10, 4, 96, 3, 50, "bf16", "bf16")
+    fake = ctypes.c_void_p(1 << 20)
+    D = ctypes.byref(d)
+    ok_io = dsa.dsa_host_io(1 << 20, 1 << 21, 256, 1 << 22, 1 << 23, 256)
+
+    def call(io, keep_mask=fake, dims=D):
+        return lib.dsa_decode_sparse_masked_io(io, dims, fake, fake, fake, fake, fake, fake, fake,
+                                               keep_mask, None, None, None, 0.1, fake, None,
+                                               fake, None)
+    assert call(None) == dsa.DSA_ERR_INVALID_ARG
+    for field in ("host_in", "dev_in", "dev_out", "host_out"):
+        io = dsa.dsa_host_io(1 << 20, 1 << 21, 256, 1 << 22, 1 << 23, 256)
+        setattr(io, field, None)
+        assert call(ctypes.byref(io)) == dsa.DSA_ERR_INVALID_ARG, field
+    # bad decode arguments with a valid io: rejected before the upload
+    assert call(ctypes.byref(ok_io), keep_mask=None) == dsa.DSA_ERR_INVALID_ARG
+    big = dsa.make_dims(2, 8, 4, 128, 10, 4, 1025, 33, 50, "bf16", "bf16")
+    assert call(ctypes.byref(ok_io), dims=ctypes.byref(big)) == dsa.DSA_ERR_UNSUPPORTED
+
+
+def test_host_io_binding_checks_buffers():
+    import torch
+    a = torch.zeros(64, dtype=torch.uint8)
+    with pytest.raises(TypeError):
+        dsa.host_io(a, a, a, a)   # device sides must be CUDA tensors
+    with pytest.raises(TypeError):
+        dsa.dsa_decode_sparse_masked_io(None, None, *([None] * 10))

@@ -116,10 +116,12 @@ def run_both(w, mask=None, bh=None):
         assert np.abs(l - ref_l).max() <= LSE_MAX
         if mode == "sparse":
             ref_sparse = ref_o, ref_l
-    # sparse decode split over thread-block clusters (merged in shared memory)
+    # sparse decode with clusters off (rows split into chunks of separate CTAs,
+    # merged by merge_kernel) and split over thread-block clusters (merged in
+    # shared memory)
     saved = dsa.dsa_get_sparse_cluster()
     try:
-        for ctas in (2, 4):
+        for ctas in (1, 2, 4):
             dsa.dsa_set_sparse_cluster(ctas)
             o1, l1 = [t.clone() for t in bt.decode_sparse()]
             o2, l2 = bt.decode_sparse_masked()
@@ -343,6 +345,41 @@ def test_fused_append_of_the_query_row(name, batch):
     assert torch.equal(bt.k_pages, ref_bt.k_pages) and torch.equal(bt.v_pages, ref_bt.v_pages)
     ref_o, ref_l = oracle.decode(w, sparse=True)
     assert_outputs(out.cpu().numpy(), ref_o, fp32=False)
+
+
+@pytest.mark.parametrize("name,batch", [("llamagen-xl", 6), ("mixed-serving", 12)])
+def test_host_io_step(name, batch):
+    """dsa_decode_sparse_masked_io: a q written only into the pinned host buffer
+    goes up with the call, and out / lse come back into the host buffer with
+    the bits of the device-only call on the uploaded inputs; a prepared call
+    issued again gives them again; the oracle on the new q agrees."""
+    w = wl.generate(wl.scaled(wl.WORKLOADS[name], batch=batch))
+    if w["keep_mask"] is None:
+        w["keep_mask"] = top_mass_masks_from_oracle(w)
+    bt = DecodeBatch.from_workload(w)
+    io, order = bt.pack_io(bt.longest_first_order())
+    gen = torch.Generator().manual_seed(11)
+    q_new = torch.randn(tuple(bt.q.shape), generator=gen).to(bt.q.dtype)
+    io.host["q"].copy_(q_new)
+    io.host["out"].fill_(float("nan"))
+    io.host["lse"].fill_(float("nan"))
+    step = bt.decode_step_io(io, order, prepare=True)
+    step()
+    torch.cuda.synchronize()
+    assert bt.device_error() == 0
+    assert torch.equal(bt.q.cpu(), q_new)
+    host_out, host_lse = io.host["out"].clone(), io.host["lse"].clone()
+    out2, lse2 = bt.decode_sparse_masked(out=torch.empty_like(bt.out), lse=torch.empty_like(bt.lse),
+                                         request_order=order)
+    torch.cuda.synchronize()
+    assert torch.equal(out2.cpu(), host_out) and torch.equal(lse2.cpu(), host_lse)
+    io.host["out"].zero_()
+    step()
+    torch.cuda.synchronize()
+    assert torch.equal(io.host["out"], host_out)
+    ref_o, ref_l = oracle.decode(dict(w, q=q_new), sparse=True)
+    assert_outputs(host_out.numpy().reshape(-1, w["head_dim"]), ref_o, fp32=False)
+    assert np.abs(host_lse.numpy().reshape(-1) - ref_l).max() <= LSE_MAX
 
 
 @pytest.mark.parametrize("name,batch", [("emu3-8b", 8), ("mixed-serving", 24),
