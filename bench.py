@@ -427,29 +427,75 @@ def run_ours(args):
 
     t_step, t_two, t_dec, t_dense = max_over_ranks([t_step, t_two, t_dec, t_dense], device)
 
-    # end-to-end through the API with host buffers: every step is one C call
-    # (dsa_decode_sparse_masked_io) that uploads the step's inputs from pinned
-    # host memory, runs the fused decode and downloads out and lse
+    # end-to-end through the API with host buffers; every step uploads its
+    # packed inputs from pinned host memory, runs the fused decode and
+    # downloads out and lse.  Direct: one C call per step
+    # (dsa_decode_sparse_masked_io).  Recorded: that call recorded once per KV
+    # copy as a dsa_graph, one dsa_graph_launch per step.  Two slots (the
+    # headline): a second slot with its own inputs, outputs, workspace and
+    # stream, step k in slot k % 2, so that one slot's copies overlap the
+    # other's kernels (double-buffered host I/O).
     h2d, d2h = io.h2d_bytes, io.d2h_bytes
     e2e_calls = [bt.decode_step_io(io, order, stream, kp, vp, prepare=True) for kp, vp in pools]
-
-    def e2e_step(k):
-        e2e_calls[k % R]()
-
-    for k in range(min(W, 3)):
-        e2e_step(k)
+    e2e_graphs = [bt.record_step_io(io, stream, order, kp, vp) for kp, vp in pools]
+    bt_b = bt.replicate()
+    io_b, order_b = bt_b.pack_io(None if order is None else order.cpu().numpy())
+    stream_b = torch.cuda.Stream(device)
+    e2e_graphs_b = [bt_b.record_step_io(io_b, stream_b, order_b, kp, vp) for kp, vp in pools]
     torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for k in range(K):
-        e2e_step(k)
-    e1.record(stream)
-    e1.synchronize()
-    t_e2e = e0.elapsed_time(e1) / 1e3
-    (t_e2e,) = max_over_ranks([t_e2e], device)
+
+    def time_e2e(run_step):
+        for k in range(min(W, 3) * 2):
+            run_step(k)
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        stream_b.wait_stream(stream)
+        h0 = time.perf_counter()
+        for k in range(K):
+            run_step(k)
+        host = time.perf_counter() - h0
+        stream.wait_stream(stream_b)
+        e1.record(stream)
+        e1.synchronize()
+        t = e0.elapsed_time(e1) / 1e3
+        (t, host) = max_over_ranks([t, host], device)
+        return t, host
+
+    def two_slots(k):
+        if k % 2 == 0:
+            e2e_graphs[k % R].launch(stream)
+        else:
+            e2e_graphs_b[k % R].launch(stream_b)
+
+    # the same two slots with inputs resident (no copies): how much of the
+    # two-slot gain is the overlap of consecutive kernels rather than of copies
+    def record(call, st):
+        dsa.dsa_graph_begin(st)
+        call()
+        return dsa.dsa_graph_end(st)
+
+    dev_graphs = [[record(lambda b=b_, s_=s_, o=o_, kp=kp, vp=vp: dsa.dsa_decode_sparse_masked(
+                      d, b.q, kp, vp, b.page_table, b.seq_len, b.prompt_len, b.window,
+                      b.keep_mask, b.scale, b.out, b.lse, b.ws, s_, o), s_)
+                   for kp, vp in pools]
+                  for b_, s_, o_ in ((bt, stream, order), (bt_b, stream_b, order_b))]
+
+    def two_slots_device(k):
+        if k % 2 == 0:
+            dev_graphs[0][k % R].launch(stream)
+        else:
+            dev_graphs[1][k % R].launch(stream_b)
+
+    t_e2e_direct, host_direct = time_e2e(lambda k: e2e_calls[k % R]())
+    t_e2e_rec, host_rec = time_e2e(lambda k: e2e_graphs[k % R].launch(stream))
+    t_e2e, host_e2e = time_e2e(two_slots)
+    t_two_dev, _ = time_e2e(two_slots_device)
+    bt.check("end-to-end steps")
+    bt_b.check("end-to-end steps (second slot)")
 
     # attention-mass pass (the characterisation kernel), timed alone
     if K > 0:
@@ -582,8 +628,24 @@ def run_ours(args):
         "e2e": {"value": world * B / (t_e2e / K), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": 1e3 * t_e2e / K,
-                "call": "dsa_decode_sparse_masked_io per step: inputs up from pinned host "
-                        "memory, fused decode, out and lse down, one C call"},
+                "host_us_per_step": 1e6 * host_e2e / K,
+                "call": "dsa_graph_launch per step of a recorded dsa_decode_sparse_masked_io "
+                        "(inputs up from pinned host memory, fused decode, out and lse down); "
+                        "two slots with their own buffers and streams, step k in slot k % 2",
+                "one_slot": {"tokens_per_s": world * B / (t_e2e_rec / K),
+                             "ms_per_step": 1e3 * t_e2e_rec / K,
+                             "host_us_per_step": 1e6 * host_rec / K,
+                             "call": "dsa_graph_launch per step, one slot: every step's "
+                                     "upload, decode and download in sequence"},
+                "direct": {"tokens_per_s": world * B / (t_e2e_direct / K),
+                           "ms_per_step": 1e3 * t_e2e_direct / K,
+                           "host_us_per_step": 1e6 * host_direct / K,
+                           "call": "dsa_decode_sparse_masked_io per step, one slot (one C "
+                                   "call: upload, fused decode, download)"}},
+        "two_slots_device": {
+            "tokens_per_s": world * B / (t_two_dev / K), "ms_per_step": 1e3 * t_two_dev / K,
+            "note": "inputs resident, no copies; the two slots of the e2e run on two streams, "
+                    "so consecutive steps' kernels overlap each other's ramp and tail"},
         "gpu_launches": K * launches,
         "clocks": clocks,
     }

@@ -38,7 +38,11 @@
  * shared by calls that may run concurrently.
  *
  * Ordering: every call is asynchronous on `stream` (a cudaStream_t; NULL is the
- * legacy default stream) and returns once its kernels are enqueued.
+ * legacy default stream) and returns once its kernels are enqueued.  The
+ * kernels are launched as programmatic dependents: a kernel's CTAs may be
+ * scheduled while the previous kernel on the stream is still running, but read
+ * and write no memory before that kernel has completed, so stream order holds
+ * exactly as for plain launches.
  *
  * Errors: calls return a dsa_status and never throw or abort.  Shapes, dtypes,
  * sizes and null pointers are checked on the host before anything is launched
@@ -239,6 +243,39 @@ dsa_status dsa_decode_sparse_masked_io(const dsa_host_io* io, const dsa_dims* di
                                        const uint32_t* keep_mask, const int32_t* request_order,
                                        const void* k_new, const void* v_new, float scale,
                                        float* out, float* lse, void* ws, void* stream);
+
+/*
+ * dsa_graph -- a recorded sequence of libdsa calls, replayed with one launch
+ * (a CUDA graph).  A serving loop whose step issues the same calls on the same
+ * buffers every time records the step once and replays it: the host then pays
+ * one launch per step instead of one per copy and kernel.
+ *   dsa_graph_begin(stream)   starts recording `stream` (not the legacy NULL
+ *                             stream: DSA_ERR_INVALID_ARG).  The libdsa calls
+ *                             issued on it afterwards, by this thread, are
+ *                             recorded, not run; their own return values still
+ *                             report argument errors.  No call that waits on
+ *                             the stream (dsa_get_device_error) may be
+ *                             recorded.  Host buffers in recorded copies must be
+ *                             pinned.
+ *   dsa_graph_end(stream, &g) ends the recording and creates *g, which owns the
+ *                             instantiated graph; a failed recording returns
+ *                             DSA_ERR_CUDA with *g = NULL.  The recording is
+ *                             ended in every case.
+ *   dsa_graph_launch(g, stream)  replays every recorded call, in order, on
+ *                             `stream`, with the pointers and sizes they were
+ *                             recorded with (the buffers must still exist; their
+ *                             contents are read at replay time).
+ *   dsa_graph_destroy(g)      frees g (NULL is a no-op); replays already
+ *                             queued still run (the graph is released when the
+ *                             last one finishes).
+ * The handle is the only resource the library creates; it holds no device
+ * memory of the caller.
+ */
+typedef struct dsa_graph dsa_graph;
+dsa_status dsa_graph_begin(void* stream);
+dsa_status dsa_graph_end(void* stream, dsa_graph** graph);
+dsa_status dsa_graph_launch(const dsa_graph* graph, void* stream);
+dsa_status dsa_graph_destroy(dsa_graph* graph);
 
 /*
  * dsa_decode_dense -- the dense causal baseline: the same as dsa_decode_sparse

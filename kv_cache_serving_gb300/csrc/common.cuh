@@ -28,6 +28,41 @@ __device__ __forceinline__ void set_error(int32_t* err, int32_t code) {
   atomicCAS(err, 0, code);
 }
 
+// Programmatic dependent launch (a no-op for grids launched without it):
+// griddep_wait() returns once the grids this one depends on have completed and
+// their writes are visible; griddep_launch_dependents() lets the next grid on
+// the stream be scheduled once every CTA of this one has issued it.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+#ifndef DSA_PDL
+#define DSA_PDL 1  // kernels launch as programmatic dependents (0: plain launches)
+#endif
+
+// kern<<<grid, block, smem, s>>>(args...) as a programmatic dependent launch:
+// the grid may be scheduled while the previous kernel on the stream drains.
+// Every libdsa kernel starts with griddep_wait(), so none touches memory before
+// its predecessor has completed.
+template <typename... Params, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = DSA_PDL;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -42,6 +42,8 @@ __device__ __forceinline__ int window_rows(const uint32_t* mask, int i, int np, 
 }
 
 __global__ void __launch_bounds__(256) compact_kernel(const CompactLaunch a) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (gw >= a.batch * a.hkv) return;
@@ -79,8 +81,7 @@ __global__ void __launch_bounds__(256) compact_kernel(const CompactLaunch a) {
 cudaError_t launch_compact(const CompactLaunch& a, cudaStream_t s) {
   const int warps = a.batch * a.hkv;
   if (warps == 0) return cudaSuccess;
-  compact_kernel<<<(warps + 7) / 8, 256, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(compact_kernel, dim3((warps + 7) / 8), dim3(256), 0, s, a);
 }
 
 }  // namespace dsa

@@ -183,6 +183,11 @@ __global__ void __launch_bounds__(NWARPS * 32,
   constexpr int kRowBytes = Tl::kRowBytes;
   extern __shared__ __align__(128) unsigned char smem[];
 
+  // Launched as a programmatic dependent: the CTAs may be scheduled while the
+  // previous kernel on the stream drains, but touch no memory before it has
+  // completed; the next launch may then be scheduled the same way.
+  griddep_wait();
+  griddep_launch_dependents();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int c = blockIdx.x, hk = blockIdx.y;
   const int b = a.order != nullptr ? __ldg(a.order + blockIdx.z) : static_cast<int>(blockIdx.z);
@@ -597,6 +602,8 @@ __global__ void __launch_bounds__(NWARPS * 32,
 // log-sum-exp.  Heads whose rows fit one chunk were finished by decode_kernel.
 template <int D, int MODE>
 __global__ void __launch_bounds__(128) merge_kernel(const DecodeLaunch a) {
+  griddep_wait();
+  griddep_launch_dependents();
   constexpr int DPL = D / 32;
   const int lane = threadIdx.x & 31;
   const int gw = blockIdx.x * 4 + (threadIdx.x >> 5);
@@ -643,26 +650,26 @@ cudaError_t launch_decode_one(const DecodeLaunch& a, cudaStream_t s) {
   const int smem = Tl::kSmem;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const dim3 grid(a.num_chunks, a.hkv, a.batch);
-  const dim3 block(Tl::NW * 32);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.num_chunks, a.hkv, a.batch);
+  cfg.blockDim = dim3(Tl::NW * 32);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
   if (a.cluster > 1) {
     // the CTAs of one (request, kv head) form one cluster along x
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = static_cast<unsigned>(a.cluster);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, a);
+  } else {
+    // programmatic dependent launch: scheduled while the previous kernel drains
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = DSA_PDL;
   }
-  kern<<<grid, block, smem, s>>>(a);
-  return cudaGetLastError();
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 // Calls f.template operator()<D, G>() for the built (head_dim, group), or

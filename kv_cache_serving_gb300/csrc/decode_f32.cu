@@ -14,19 +14,19 @@ cudaError_t launch_decode_f32(const DecodeLaunch& a, int mode, cudaStream_t s) {
 }
 
 template <int D>
-void launch_merge_d(const DecodeLaunch& a, int mode, int blocks, cudaStream_t s) {
-  if (mode == kRowsDense) merge_kernel<D, kRowsDense><<<blocks, 128, 0, s>>>(a);
-  else if (mode == kRowsList) merge_kernel<D, kRowsList><<<blocks, 128, 0, s>>>(a);
-  else merge_kernel<D, kRowsMask><<<blocks, 128, 0, s>>>(a);
+cudaError_t launch_merge_d(const DecodeLaunch& a, int mode, int blocks, cudaStream_t s) {
+  const dim3 grid(blocks), block(128);
+  if (mode == kRowsDense) return launch_pdl(merge_kernel<D, kRowsDense>, grid, block, 0, s, a);
+  if (mode == kRowsList) return launch_pdl(merge_kernel<D, kRowsList>, grid, block, 0, s, a);
+  return launch_pdl(merge_kernel<D, kRowsMask>, grid, block, 0, s, a);
 }
 
 cudaError_t launch_merge(const DecodeLaunch& a, int mode, cudaStream_t s) {
   const int pairs = a.batch * a.hq;
   if (pairs == 0 || a.num_chunks <= 1) return cudaSuccess;
   const int blocks = (pairs + 3) / 4;
-  if (a.head_dim == 64) launch_merge_d<64>(a, mode, blocks, s);
-  else launch_merge_d<128>(a, mode, blocks, s);
-  return cudaGetLastError();
+  return a.head_dim == 64 ? launch_merge_d<64>(a, mode, blocks, s)
+                          : launch_merge_d<128>(a, mode, blocks, s);
 }
 
 DecodeShape decode_shape_f32(int head_dim, int group, int mode, int build) {

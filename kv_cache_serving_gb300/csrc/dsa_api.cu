@@ -5,6 +5,7 @@
 #include <cstddef>
 #include <cstdint>
 #include <mutex>
+#include <new>
 
 #include <cuda_runtime.h>
 
@@ -518,6 +519,55 @@ dsa_status dsa_decode_plan(const dsa_dims* dims, int32_t mode, int32_t* chunk,
   if (warps) *warps = p.warps;
   if (tile_rows) *tile_rows = p.tile_rows;
   return DSA_OK;
+}
+
+struct dsa_graph {
+  cudaGraphExec_t exec;
+};
+
+dsa_status dsa_graph_begin(void* stream) {
+  if (stream == nullptr) return DSA_ERR_INVALID_ARG;  // the legacy stream cannot record
+  return from_cuda(
+      cudaStreamBeginCapture(static_cast<cudaStream_t>(stream), cudaStreamCaptureModeThreadLocal));
+}
+
+dsa_status dsa_graph_end(void* stream, dsa_graph** graph) {
+  if (stream == nullptr) return DSA_ERR_INVALID_ARG;
+  if (graph != nullptr) *graph = nullptr;
+  cudaGraph_t g = nullptr;
+  // the recording ends whatever else fails, so the stream is usable again
+  cudaError_t e = cudaStreamEndCapture(static_cast<cudaStream_t>(stream), &g);
+  if (e != cudaSuccess || g == nullptr) {
+    if (g != nullptr) cudaGraphDestroy(g);
+    return DSA_ERR_CUDA;
+  }
+  if (graph == nullptr) {
+    cudaGraphDestroy(g);
+    return DSA_ERR_INVALID_ARG;
+  }
+  cudaGraphExec_t x = nullptr;
+  e = cudaGraphInstantiate(&x, g, 0);
+  cudaGraphDestroy(g);
+  if (e != cudaSuccess) return DSA_ERR_CUDA;
+  dsa_graph* h = new (std::nothrow) dsa_graph{x};
+  if (h == nullptr) {
+    cudaGraphExecDestroy(x);
+    return DSA_ERR_CUDA;
+  }
+  *graph = h;
+  return DSA_OK;
+}
+
+dsa_status dsa_graph_launch(const dsa_graph* graph, void* stream) {
+  if (graph == nullptr) return DSA_ERR_INVALID_ARG;
+  return from_cuda(cudaGraphLaunch(graph->exec, static_cast<cudaStream_t>(stream)));
+}
+
+dsa_status dsa_graph_destroy(dsa_graph* graph) {
+  if (graph == nullptr) return DSA_OK;
+  const cudaError_t e = cudaGraphExecDestroy(graph->exec);
+  delete graph;
+  return from_cuda(e);
 }
 
 dsa_status dsa_set_sparse_cluster(int32_t ctas) {

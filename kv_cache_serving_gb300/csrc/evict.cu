@@ -21,6 +21,8 @@
 namespace dsa {
 
 __global__ void __launch_bounds__(256) evict_kernel(const EvictLaunch a) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int lane = threadIdx.x & 31;
   int pg = -1;  // page this thread unmaps, or -1
@@ -58,8 +60,8 @@ __global__ void __launch_bounds__(256) evict_kernel(const EvictLaunch a) {
 cudaError_t launch_evict(const EvictLaunch& a, cudaStream_t s) {
   const int64_t n = static_cast<int64_t>(a.batch) * a.max_pages;
   if (n == 0) return cudaSuccess;
-  evict_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(evict_kernel, dim3(static_cast<unsigned>((n + 255) / 256)), dim3(256), 0,
+                    s, a);
 }
 
 }  // namespace dsa

@@ -81,6 +81,8 @@ __device__ __forceinline__ int mass_bin(const MassLaunch& a, int j, int o, int P
 
 template <int D, typename KV, int G>
 __global__ void __launch_bounds__(MassTiling<D, KV, G>::NW * 32) mass_kernel(const MassLaunch a) {
+  griddep_wait();
+  griddep_launch_dependents();
   using Tl = MassTiling<D, KV, G>;
   constexpr int T = Tl::T, S = Tl::S, NW = Tl::NW, DPL = Tl::kDPL;
   constexpr int kRowBytes = Tl::kRowBytes;
@@ -284,6 +286,8 @@ struct MassMmaTiling {
 template <int D, int G>
 __global__ void __launch_bounds__(MassMmaTiling<D>::NW * 32)
     mass_mma_kernel(const MassLaunch a) {
+  griddep_wait();
+  griddep_launch_dependents();
   using Tl = MassMmaTiling<D>;
   constexpr int T = Tl::T, S = Tl::S, NW = Tl::NW, RB = T / 16, NK = D / 16;
   constexpr int RPL = (T + 31) / 32;  // rows of a tile per lane (lane + 32 u < T)
@@ -503,6 +507,8 @@ __global__ void __launch_bounds__(MassMmaTiling<D>::NW * 32)
 // One warp per (request, query head): combine chunks, normalise bins, and turn
 // raw window scores into weights.
 __global__ void __launch_bounds__(128) mass_merge_kernel(const MassLaunch a) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int gw = blockIdx.x * 4 + (threadIdx.x >> 5);
   if (gw >= a.batch * a.hq) return;
@@ -550,12 +556,10 @@ cudaError_t launch_mass_kernel(Kern kern, int smem, int threads, const MassLaunc
                                cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<dim3(a.num_chunks, a.hkv, a.batch), threads, smem, s>>>(a);
-  e = cudaGetLastError();
+  e = launch_pdl(kern, dim3(a.num_chunks, a.hkv, a.batch), dim3(threads), smem, s, a);
   if (e != cudaSuccess) return e;
   const int pairs = a.batch * a.hq;
-  mass_merge_kernel<<<(pairs + 3) / 4, 128, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(mass_merge_kernel, dim3((pairs + 3) / 4), dim3(128), 0, s, a);
 }
 
 // Calls f(kernel, dynamic smem, threads per CTA, rows per CTA pass) for the

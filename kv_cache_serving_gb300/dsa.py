@@ -81,6 +81,10 @@ def _load():
                              ctypes.POINTER(I32), ctypes.POINTER(I32), ctypes.POINTER(I32)],
                             I32),
         "dsa_decode_sparse_noalloc": ([D, P, P, P, P, P, P, P, F32, P, P, P, P], I32),
+        "dsa_graph_begin": ([P], I32),
+        "dsa_graph_end": ([P, ctypes.POINTER(P)], I32),
+        "dsa_graph_launch": ([P, P], I32),
+        "dsa_graph_destroy": ([P], I32),
         "dsa_set_sparse_cluster": ([I32], I32),
         "dsa_get_sparse_cluster": ([], I32),
         "dsa_get_device_error": ([P, P, ctypes.POINTER(I32)], I32),
@@ -267,6 +271,58 @@ def dsa_decode_sparse_masked_io(io, dims, q, k_pages, v_pages, page_table, seq_l
         return call
     call()
     return None
+
+
+def dsa_graph_begin(stream):
+    """Start recording libdsa calls on `stream` (a torch.cuda.Stream, not the
+    legacy default stream)."""
+    _check(_load().dsa_graph_begin(_stream(stream)), "dsa_graph_begin")
+
+
+def dsa_graph_end(stream) -> "Graph":
+    """End the recording on `stream`; returns the recorded calls as a Graph."""
+    h = ctypes.c_void_p()
+    _check(_load().dsa_graph_end(_stream(stream), ctypes.byref(h)), "dsa_graph_end")
+    return Graph(h)
+
+
+def dsa_graph_launch(graph: "Graph", stream=None):
+    _check(_load().dsa_graph_launch(graph.handle, _stream(stream)), "dsa_graph_launch")
+
+
+def dsa_graph_destroy(graph: "Graph"):
+    graph.close()
+
+
+class Graph:
+    """Owner of a dsa_graph handle; launch() replays it, close() (or garbage
+    collection) frees it.  Objects a recorded call points into can be attached
+    with keep() so that they live as long as the graph."""
+
+    def __init__(self, handle: ctypes.c_void_p):
+        self.handle = handle
+        self._keep = []
+        self._lib = _load()
+
+    def keep(self, *objs):
+        self._keep.extend(objs)
+        return self
+
+    def launch(self, stream=None):
+        status = self._lib.dsa_graph_launch(self.handle, _stream(stream))
+        if status != DSA_OK:
+            raise DSAError(status, "dsa_graph_launch")
+
+    def close(self):
+        if self.handle:
+            _check(self._lib.dsa_graph_destroy(self.handle), "dsa_graph_destroy")
+            self.handle = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def dsa_decode_sparse_noalloc(dims, q, k_pages, v_pages, page_table, seq_len, kept_idx,

@@ -6,6 +6,7 @@ binding.  PyTorch provides the device memory and the stream, nothing else.
 """
 from __future__ import annotations
 
+import copy
 import math
 
 import numpy as np
@@ -124,6 +125,18 @@ class DecodeBatch:
                    max_window=w["max_window"], mask_words=w["mask_words"],
                    max_kept=w["max_kept"], device=device)
 
+    def replicate(self) -> "DecodeBatch":
+        """A second slot for the same batch shape: the KV cache is shared (not
+        copied); the step inputs, kept lists, outputs and workspace are its own
+        copies, so that two steps can be in flight at once (double-buffered
+        host I/O: one slot's copies overlap the other's kernels)."""
+        other = copy.copy(self)
+        for name in ("q", "page_table", "seq_len", "prompt_len", "window", "grid_w", "keep_mask",
+                     "kept_idx", "kept_cnt", "out", "lse", "ws"):
+            setattr(other, name, getattr(self, name).clone())
+        other._host_lengths = tuple(x.copy() for x in self._host_lengths)
+        return other
+
     def set_keep_mask(self, keep_mask):
         self.keep_mask.copy_(torch.as_tensor(
             np.ascontiguousarray(keep_mask, dtype=np.uint32).view(np.int32)))
@@ -173,6 +186,23 @@ class DecodeBatch:
             self.prompt_len, self.window, self.keep_mask, self.scale, self.out, self.lse, self.ws,
             stream, request_order, prepare=prepare)
 
+    def record_step_io(self, io: PackedIO, stream, request_order=None, k_pages=None,
+                       v_pages=None) -> dsa.Graph:
+        """decode_step_io recorded once as a dsa.Graph on `stream` (a non-default
+        torch.cuda.Stream): each graph.launch(stream) uploads io's inputs, runs
+        the fused decode and downloads out and lse, for one host launch."""
+        dsa.dsa_graph_begin(stream)
+        try:
+            self.decode_step_io(io, request_order, stream, k_pages, v_pages)
+        except BaseException:
+            try:  # end the recording so that the stream is usable again
+                dsa.dsa_graph_end(stream).close()
+            except dsa.DSAError:
+                pass
+            raise
+        graph = dsa.dsa_graph_end(stream)
+        return graph.keep(io, request_order, k_pages, v_pages, self)
+
     def longest_first_order(self):
         """Requests by decreasing estimated kept rows: the request_order that
         shortens the tail of a mixed batch (host-side; the serving host knows
@@ -183,7 +213,7 @@ class DecodeBatch:
         """longest_first_order() when the batch's lengths vary, else None."""
         return schedule_order(self._host_lengths)
 
-    def pack_io(self, order=None) -> PackedIO:
+    def pack_io(self, order=None) -> tuple:
         """Move the step's inputs (q, lengths, masks, page table, order) and
         results (out, lse) into packed buffers; returns the PackedIO and the
         device order tensor (or None)."""

@@ -149,6 +149,14 @@ def test_host_io_call_checks_before_copying():
     assert call(ctypes.byref(ok_io), dims=ctypes.byref(big)) == dsa.DSA_ERR_UNSUPPORTED
 
 
+def test_graph_handles_checked():
+    lib = dsa._load()
+    assert lib.dsa_graph_launch(None, None) == dsa.DSA_ERR_INVALID_ARG
+    assert lib.dsa_graph_destroy(None) == dsa.DSA_OK
+    assert lib.dsa_graph_begin(None) == dsa.DSA_ERR_INVALID_ARG   # legacy stream
+    assert lib.dsa_graph_end(None, None) == dsa.DSA_ERR_INVALID_ARG
+
+
 def test_host_io_binding_checks_buffers():
     import torch
     a = torch.zeros(64, dtype=torch.uint8)

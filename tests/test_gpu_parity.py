@@ -382,6 +382,60 @@ def test_host_io_step(name, batch):
     assert np.abs(host_lse.numpy().reshape(-1) - ref_l).max() <= LSE_MAX
 
 
+@pytest.mark.parametrize("name,batch", [("llamagen-xl", 6), ("emu3-8b", 4)])
+def test_recorded_host_io_step(name, batch):
+    """A dsa_graph of dsa_decode_sparse_masked_io: every replay uploads the q then
+    in the pinned host buffer and downloads the results of that q (the bits of
+    the direct call on it); three replays with three different q."""
+    w = wl.generate(wl.scaled(wl.WORKLOADS[name], batch=batch))
+    bt = DecodeBatch.from_workload(w)
+    io, order = bt.pack_io(bt.longest_first_order())
+    stream = torch.cuda.Stream()
+    graph = bt.record_step_io(io, stream, order)
+    torch.cuda.synchronize()
+    gen = torch.Generator().manual_seed(5)
+    for rep in range(3):
+        q_new = torch.randn(tuple(bt.q.shape), generator=gen).to(bt.q.dtype)
+        io.host["q"].copy_(q_new)
+        io.host["out"].fill_(float("nan"))
+        graph.launch(stream)
+        stream.synchronize()
+        assert bt.device_error() == 0
+        assert torch.equal(bt.q.cpu(), q_new)
+        got_o, got_l = io.host["out"].clone(), io.host["lse"].clone()
+        with torch.cuda.stream(stream):
+            o2, l2 = bt.decode_sparse_masked(out=torch.empty_like(bt.out),
+                                             lse=torch.empty_like(bt.lse), stream=stream,
+                                             request_order=order)
+        stream.synchronize()
+        assert torch.equal(o2.cpu(), got_o) and torch.equal(l2.cpu(), got_l), rep
+        if rep == 0:
+            ref_o, ref_l = oracle.decode(dict(w, q=q_new), sparse=True)
+            assert_outputs(got_o.numpy().reshape(-1, w["head_dim"]), ref_o, fp32=False)
+    # two slots in flight at once on two streams (shared KV cache, own inputs,
+    # outputs and workspaces): each slot gets the results of its own q
+    bt_b = bt.replicate()
+    io_b, order_b = bt_b.pack_io(bt_b.longest_first_order())
+    stream_b = torch.cuda.Stream()
+    graph_b = bt_b.record_step_io(io_b, stream_b, order_b)
+    torch.cuda.synchronize()
+    qa = torch.randn(tuple(bt.q.shape), generator=gen).to(bt.q.dtype)
+    qb = torch.randn(tuple(bt.q.shape), generator=gen).to(bt.q.dtype)
+    io.host["q"].copy_(qa)
+    io_b.host["q"].copy_(qb)
+    for _ in range(2):
+        graph.launch(stream)
+        graph_b.launch(stream_b)
+    torch.cuda.synchronize()
+    assert bt.device_error() == 0 and bt_b.device_error() == 0
+    for q_in, host in ((qa, io.host), (qb, io_b.host)):
+        ref_o, ref_l = oracle.decode(dict(w, q=q_in), sparse=True)
+        assert_outputs(host["out"].numpy().reshape(-1, w["head_dim"]), ref_o, fp32=False)
+        assert np.abs(host["lse"].numpy().reshape(-1) - ref_l).max() <= LSE_MAX
+    graph.close()
+    graph_b.close()
+
+
 @pytest.mark.parametrize("name,batch", [("emu3-8b", 8), ("mixed-serving", 24),
                                         ("llamagen-xl", 8)])
 def test_evict_pages_then_decode_unchanged(name, batch):
