@@ -232,6 +232,11 @@ typedef struct {
  * dsa_decode_sparse_masked on the remaining (device) arguments, then the
  * download dev_out -> host_out.  Everything is asynchronous; host_out holds the
  * results once the stream has passed the call (e.g. cudaStreamSynchronize).
+ * A host buffer that is page-locked and mapped into the device's address space
+ * (cudaHostAlloc, or any page-locked memory under unified addressing) is copied
+ * by a small kernel that reads or writes it directly, without the copy
+ * engines' fixed latency; other host memory goes through cudaMemcpyAsync
+ * (synchronous for pageable memory).
  * All arguments are checked before the upload: a call that returns
  * DSA_ERR_INVALID_ARG or DSA_ERR_UNSUPPORTED has issued nothing.  A failed copy
  * returns DSA_ERR_CUDA.  io must not be NULL.

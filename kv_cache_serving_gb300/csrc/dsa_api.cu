@@ -257,17 +257,14 @@ dsa_status decode_common(const dsa_dims* d, int mode, const void* q, const void*
                         (io->out_bytes > 0 && (!io->dev_out || !io->host_out))))
     return DSA_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (io != nullptr && io->in_bytes > 0 &&
-      cudaMemcpyAsync(io->dev_in, io->host_in, io->in_bytes, cudaMemcpyHostToDevice, s) !=
-          cudaSuccess)
+  if (io != nullptr && copy_host_to_device(io->dev_in, io->host_in, io->in_bytes, s) != cudaSuccess)
     return DSA_ERR_CUDA;
   const dsa_status rc = d->batch == 0 ? DSA_OK
                                       : decode_launch(d, mode, q, k, v, page_table, seq_len, rs,
                                                       scale, out, lse, ws, s);
   if (rc != DSA_OK) return rc;
-  if (io != nullptr && io->out_bytes > 0 &&
-      cudaMemcpyAsync(io->host_out, io->dev_out, io->out_bytes, cudaMemcpyDeviceToHost, s) !=
-          cudaSuccess)
+  if (io != nullptr &&
+      copy_device_to_host(io->host_out, io->dev_out, io->out_bytes, s) != cudaSuccess)
     return DSA_ERR_CUDA;
   return DSA_OK;
 }

@@ -108,6 +108,11 @@ int mass_ctas_per_sm(int head_dim, int group, bool kv_bf16, bool q_bf16);
 cudaError_t launch_compact(const CompactLaunch& a, cudaStream_t s);
 cudaError_t launch_evict(const EvictLaunch& a, cudaStream_t s);
 
+// Host copies of a step (hostio.cu): a copy kernel when the host side is
+// page-locked memory the device can address, else cudaMemcpyAsync.
+cudaError_t copy_host_to_device(void* dev, const void* host, size_t bytes, cudaStream_t s);
+cudaError_t copy_device_to_host(void* host, const void* dev, size_t bytes, cudaStream_t s);
+
 // Builds of the decode kernel.  The sparse calls with bf16 KV have two more
 // besides the default: one for batches of more than two waves of units (more
 // warps per SM), one for batches that fit one wave only with it (5 warps of a

@@ -380,6 +380,18 @@ def test_host_io_step(name, batch):
     ref_o, ref_l = oracle.decode(dict(w, q=q_new), sparse=True)
     assert_outputs(host_out.numpy().reshape(-1, w["head_dim"]), ref_o, fp32=False)
     assert np.abs(host_lse.numpy().reshape(-1) - ref_l).max() <= LSE_MAX
+    # pageable (not page-locked) host buffers: the copies take the copy engine
+    # instead of the copy kernel, with the same bytes moved
+    page_in = torch.empty(io.host_in.shape, dtype=io.host_in.dtype)
+    page_in.copy_(io.host_in)
+    page_out = torch.full(io.host_out.shape, 255, dtype=io.host_out.dtype)
+    assert not page_in.is_pinned() and not page_out.is_pinned()
+    desc = dsa.host_io(page_in, io.dev_in, io.dev_out, page_out)
+    dsa.dsa_decode_sparse_masked_io(desc, bt.dims, bt.q, bt.k_pages, bt.v_pages, bt.page_table,
+                                    bt.seq_len, bt.prompt_len, bt.window, bt.keep_mask, bt.scale,
+                                    bt.out, bt.lse, bt.ws, None, order)
+    torch.cuda.synchronize()
+    assert torch.equal(page_out, io.host_out)
 
 
 @pytest.mark.parametrize("name,batch", [("llamagen-xl", 6), ("emu3-8b", 4)])
