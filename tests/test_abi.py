@@ -157,6 +157,24 @@ def test_graph_handles_checked():
     assert lib.dsa_graph_end(None, None) == dsa.DSA_ERR_INVALID_ARG
 
 
+def test_prepared_call_reissues_and_raises():
+    """dsa.Prepared keeps the marshalled arguments and re-issues the call;
+    a non-OK status raises (host-only entry point, no GPU)."""
+    saved = dsa.dsa_get_sparse_cluster()
+    try:
+        set4 = dsa.Prepared("dsa_set_sparse_cluster", (ctypes.c_int32(4),))
+        dsa.dsa_set_sparse_cluster(0)
+        set4()
+        assert dsa.dsa_get_sparse_cluster() == 4
+        dsa.dsa_set_sparse_cluster(1)
+        set4()
+        assert dsa.dsa_get_sparse_cluster() == 4
+        with pytest.raises(dsa.DSAError):
+            dsa.Prepared("dsa_set_sparse_cluster", (ctypes.c_int32(-1),))()
+    finally:
+        dsa.dsa_set_sparse_cluster(saved)
+
+
 def test_host_io_binding_checks_buffers():
     import torch
     a = torch.zeros(64, dtype=torch.uint8)
