@@ -333,7 +333,7 @@ def run_ours(args):
     # vary), from the host-side lengths a serving host has when it builds the
     # batch; the step's inputs and results live in packed buffers so that the
     # end-to-end run moves them in one copy each way
-    io, order = bt.pack_io(bt.schedule_order())
+    packed, order = bt.pack_io(bt.schedule_order())
     bt.build_index()
     torch.cuda.synchronize()
     bt.check("build_index")
@@ -435,13 +435,14 @@ def run_ours(args):
     # headline): a second slot with its own inputs, outputs, workspace and
     # stream, step k in slot k % 2, so that one slot's copies overlap the
     # other's kernels (double-buffered host I/O).
-    h2d, d2h = io.h2d_bytes, io.d2h_bytes
-    e2e_calls = [bt.decode_step_io(io, order, stream, kp, vp, prepare=True) for kp, vp in pools]
-    e2e_graphs = [bt.record_step_io(io, stream, order, kp, vp) for kp, vp in pools]
+    h2d, d2h = packed.h2d_bytes, packed.d2h_bytes
+    e2e_calls = [bt.decode_step_io(packed, order, stream, kp, vp, prepare=True)
+                 for kp, vp in pools]
+    e2e_graphs = [bt.record_step_io(packed, stream, order, kp, vp) for kp, vp in pools]
     bt_b = bt.replicate()
-    io_b, order_b = bt_b.pack_io(None if order is None else order.cpu().numpy())
+    packed_b, order_b = bt_b.pack_io(None if order is None else order.cpu().numpy())
     stream_b = torch.cuda.Stream(device)
-    e2e_graphs_b = [bt_b.record_step_io(io_b, stream_b, order_b, kp, vp) for kp, vp in pools]
+    e2e_graphs_b = [bt_b.record_step_io(packed_b, stream_b, order_b, kp, vp) for kp, vp in pools]
     torch.cuda.synchronize()
 
     def time_e2e(run_step):
