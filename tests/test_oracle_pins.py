@@ -342,6 +342,67 @@ def test_mass_equal_scores_hand_counts():
     assert np.max(np.abs(om[0] - want)) < 1e-15
 
 
+def read_mass_cases():
+    cases = []
+    with open(os.path.join(GOLDEN, "mass_diagonal_bins.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            head, rest = line.split(":")
+            counts, diag = rest.split("|")
+            name, *nums = head.split()
+            cases.append((name, *(int(x) for x in nums), [int(x) for x in counts.split()],
+                          expand_ranges(diag.split())))
+    return cases
+
+
+@pytest.mark.parametrize("case", read_mass_cases(), ids=lambda c: c[0])
+def test_mass_diagonal_bin_hand_counts(case):
+    """Equal scores (all keys zero) with r_diag >= 1: every bin is its hand-counted
+    number of rows / L, including bands k*w +- r that cross the window edge, the
+    local band or the prompt (fixture mass_diagonal_bins.txt)."""
+    name, L, P, W, w, r_local, r_diag, counts, diag = case
+    assert sum(counts) == L and len(diag) == counts[2]
+    D = 4
+    pages = (L + 15) // 16
+    gen = torch.Generator().manual_seed(L)
+    inp = dict(q=torch.randn(1, 1, D, generator=gen),
+               k_pages=torch.zeros(pages + 1, 16, 1, D), v_pages=torch.zeros(pages + 1, 16, 1, D),
+               page_table=np.array([list(range(pages, 0, -1))], np.int32),
+               seq_len=np.array([L], np.int32), prompt_len=np.array([P], np.int32),
+               window=np.array([W], np.int32), grid_w=np.array([w], np.int32),
+               keep_mask=np.zeros((1, 1, 1), np.uint32), max_window=W + 3)
+    m4, om = oracle.mass(inp, r_local=r_local, r_diag=r_diag)
+    assert np.max(np.abs(m4[0] - np.array(counts) / L)) < 1e-15
+    want = np.zeros(W + 4)
+    want[:min(W, L - 1) + 1] = 1 / L
+    assert np.max(np.abs(om[0] - want)) < 1e-15
+
+
+def test_mass_diagonal_and_other_bins_vs_torch_softmax():
+    """Random scores: the diagonal bin is the torch softmax weight summed over the
+    offsets {k*w + r : k >= 1, |r| <= r_diag} (enumerated as a set) that lie in
+    (r_local, W] and below the prompt boundary; other is the remainder."""
+    inp, klog, vlog, offs = logical_problem(23, B=4, Hq=2, Hkv=1, D=16)
+    B, Hq, D = inp["q"].shape
+    inp["grid_w"] = np.array([3, 5, 7, 4], np.int32)
+    for r_local, r_diag in ((0, 1), (2, 2), (1, 3)):
+        m4, _ = oracle.mass(inp, r_local=r_local, r_diag=r_diag, with_offsets=False)
+        for b in range(B):
+            L, P, W, w = (int(inp[k][b]) for k in ("seq_len", "prompt_len", "window", "grid_w"))
+            i = L - 1
+            near = {k * w + r for k in range(1, W // w + 2) for r in range(-r_diag, r_diag + 1)}
+            diag_o = [o for o in near if r_local < o <= W and 0 <= i - o and i - o >= P]
+            for h in range(Hq):
+                s = (klog[b][:, 0].double() @ inp["q"][b, h].double()) / math.sqrt(D)
+                a = torch.softmax(s, dim=0).numpy()
+                t = b * Hq + h
+                want_diag = sum(a[i - o] for o in diag_o)
+                assert abs(m4[t, 2] - want_diag) < 1e-12, (b, h, r_local, r_diag)
+                assert abs(m4[t, 3] - (1.0 - m4[t, :3].sum())) < 1e-12
+
+
 def test_mass_vs_torch_softmax():
     inp, klog, vlog, offs = logical_problem(21, B=3, Hq=4, Hkv=2, D=16)
     B, Hq, D = inp["q"].shape
