@@ -10,7 +10,7 @@ C file's header for the page sections each function follows.
 
 Functions whose parity is pinned by ``tests/test_oracle_pins.py``:
 ``kept_set``, ``mask_matrix``, ``sparsity``, ``attend_rows``, ``decode``,
-``mass``.  ``top_mass_keep_mask`` lives with the input generators (it is a
+``multi``, ``mass``, ``evictable_pages``.  ``top_mass_keep_mask`` lives with the input generators (it is a
 selection rule, not the method's arithmetic).
 """
 from __future__ import annotations
@@ -83,6 +83,8 @@ def _load():
         lib.oracle_decode.restype = i32
         lib.oracle_mass.argtypes = [ctypes.POINTER(Problem), i32, i32, p, i32, p, p, i32]
         lib.oracle_mass.restype = i32
+        lib.oracle_multi.argtypes = [ctypes.POINTER(Problem), p, i32, p, p, i32]
+        lib.oracle_multi.restype = i32
         _lib = lib
     return _lib
 
@@ -166,7 +168,8 @@ class _Bound:
         v, vd = _raw(inp["v_pages"])
         assert kd == vd
         self.keep = [q, k, v]
-        B, Hq, D = inp["q"].shape
+        # q is [B][Hq][D] (one query per request) or [B][Q][Hq][D] (several)
+        B, Hq, D = inp["q"].shape[0], inp["q"].shape[-2], inp["q"].shape[-1]
         num_pages, page, Hkv, D2 = inp["k_pages"].shape
         assert page == PAGE and D2 == D
         pt = _np(inp["page_table"], np.int32)
@@ -219,6 +222,25 @@ def decode(inp: dict, sparse: bool, bh=None, scale: float | None = None,
                            nthreads or default_threads())
     if rc != 0:
         raise ValueError(f"oracle_decode failed with status {rc}")
+    return out, lse
+
+
+def multi(inp: dict, q_len, scale: float | None = None, nthreads: int | None = None):
+    """fp64 attention of several query tokens per request under the mask:
+    inp["q"] is [B][Q][Hq][D]; the q_len[b] query tokens of request b are its
+    last cache rows L-q_len .. L-1, each attending over its own kept set.
+    Returns (out [B][Q][Hq][D], lse [B][Q][Hq]); slots t >= q_len[b] are NaN."""
+    lib = _load()
+    bound = _Bound(inp, scale)
+    B, Q, Hq, D = inp["q"].shape
+    ql = _np(q_len, np.int32)
+    assert ql.shape == (B,)
+    out = np.full((B, Q, Hq, D), np.nan, dtype=np.float64)
+    lse = np.full((B, Q, Hq), np.nan, dtype=np.float64)
+    rc = lib.oracle_multi(ctypes.byref(bound.pr), _ptr(ql), Q, _ptr(out), _ptr(lse),
+                          nthreads or default_threads())
+    if rc != 0:
+        raise ValueError(f"oracle_multi failed with status {rc}")
     return out, lse
 
 

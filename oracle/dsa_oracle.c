@@ -258,6 +258,63 @@ static int decode_one(const oracle_problem* pr, int sparse, int32_t b, int32_t h
 }
 
 /* ---------------------------------------------------------------------------
+ * Several query tokens of one request under the same mask [DAS-formula],
+ * [DAS-abstract]: the last n rows of the cache are the query tokens
+ * i = L-n .. L-1 (their K/V rows are already in the cache, as when a chunk of
+ * prompt or image tokens is prefilled at once).  Query i attends over its own
+ * causal kept set, the decode rule of oracle_kept_set with L = i+1 (reading:
+ * the pages define the mask per query position, so every query of the chunk
+ * uses it unchanged).  One (request, query slot t, query head h).
+ * ------------------------------------------------------------------------- */
+static int multi_one(const oracle_problem* pr, const int32_t* q_len, int32_t max_q, int32_t b,
+                     int32_t t, int32_t h, double* out, double* lse) {
+  const int32_t D = pr->head_dim;
+  const int32_t g = pr->hq / pr->hkv;
+  const int32_t hk = h / g;
+  const int32_t L = pr->seq_len[b], n = q_len[b];
+  const int32_t P = pr->prompt_len[b], W = pr->window[b];
+  if (L < 1 || L > pr->max_pages * OR_PAGE || n < 0 || n > L || n > max_q || t < 0 || t >= n ||
+      W > pr->max_window || W > pr->mask_words * 32)
+    return OR_BAD_REQUEST;
+  const int32_t i = L - n + t;
+  int32_t* idx = (int32_t*)malloc((size_t)(i + 1) * sizeof(int32_t));
+  if (!idx) return OR_NO_MEMORY;
+  const int32_t cnt = oracle_kept_set(i + 1, P, W,
+                                      pr->keep_mask + ((size_t)b * pr->hkv + hk) * pr->mask_words,
+                                      idx);
+  if (cnt < 0) {
+    free(idx);
+    return cnt;
+  }
+  double* q = (double*)malloc((size_t)D * sizeof(double));
+  double* k = (double*)malloc((size_t)(cnt > 0 ? cnt : 1) * D * sizeof(double));
+  double* v = (double*)malloc((size_t)(cnt > 0 ? cnt : 1) * D * sizeof(double));
+  int rc = OR_OK;
+  if (!q || !k || !v) rc = OR_NO_MEMORY;
+  if (rc == OR_OK) {
+    for (int32_t e = 0; e < D; ++e)
+      q[e] = widen(pr->q, (((size_t)b * max_q + t) * pr->hq + h) * D + e, pr->q_dtype);
+    for (int32_t r = 0; r < cnt && rc == OR_OK; ++r) {
+      size_t off;
+      if (!row_offset(pr, b, hk, idx[r], &off)) {
+        rc = OR_BAD_REQUEST;
+        break;
+      }
+      for (int32_t e = 0; e < D; ++e) {
+        k[(size_t)r * D + e] = widen(pr->k_pages, off + e, pr->kv_dtype);
+        v[(size_t)r * D + e] = widen(pr->v_pages, off + e, pr->kv_dtype);
+      }
+    }
+  }
+  if (rc == OR_OK) oracle_attend_rows(D, q, k, v, cnt, pr->scale, out, lse);
+  free(q);
+  free(k);
+  free(v);
+  free(idx);
+  return rc;
+}
+
+/* ---------------------------------------------------------------------------
  * Attention mass of one (request, query head) over the dense causal softmax
  * [DAS-abstract: concentration on prompt and local tokens, diagonal pattern],
  * [DAS-method: raster order puts spatial neighbours at offsets k*w +- r].
@@ -337,7 +394,9 @@ static int mass_one(const oracle_problem* pr, int32_t b, int32_t h, int32_t r_lo
  * ------------------------------------------------------------------------- */
 typedef struct {
   const oracle_problem* pr;
-  int kind; /* 0 dense, 1 sparse, 2 mass */
+  int kind; /* 0 dense, 1 sparse, 2 mass, 3 several queries per request */
+  const int32_t* q_len;
+  int32_t max_q;
   const int32_t* bh;
   int32_t n_bh;
   int32_t r_local, r_diag;
@@ -358,8 +417,13 @@ static void* worker(void* arg) {
     int32_t t = ts->next++;
     pthread_mutex_unlock(&ts->lock);
     if (t >= ts->n_bh) break;
-    int32_t b, h;
-    if (ts->bh) {
+    int32_t b, h, qt = 0;
+    if (ts->kind == 3) {
+      /* task t = (b, query slot, head) in row-major order over [batch][max_q][hq] */
+      b = t / (ts->max_q * pr->hq);
+      qt = (t / pr->hq) % ts->max_q;
+      h = t % pr->hq;
+    } else if (ts->bh) {
       b = ts->bh[2 * t];
       h = ts->bh[2 * t + 1];
     } else {
@@ -369,6 +433,10 @@ static void* worker(void* arg) {
     int rc;
     if (b < 0 || b >= pr->batch || h < 0 || h >= pr->hq) {
       rc = OR_BAD_ARG;
+    } else if (ts->kind == 3) {
+      rc = qt < ts->q_len[b] ? multi_one(pr, ts->q_len, ts->max_q, b, qt, h,
+                                         ts->out + (size_t)t * pr->head_dim, ts->lse + t)
+                             : OR_OK; /* slots past q_len are left as they are */
     } else if (ts->kind == 2) {
       rc = mass_one(pr, b, h, ts->r_local, ts->r_diag, ts->mass + (size_t)t * 4,
                     ts->offset_mass ? ts->offset_mass + (size_t)t * (pr->max_window + 1) : NULL);
@@ -440,5 +508,24 @@ int32_t oracle_mass(const oracle_problem* pr, int32_t r_local, int32_t r_diag,
   ts.r_diag = r_diag;
   ts.mass = mass;
   ts.offset_mass = offset_mass;
+  return run_tasks(&ts, nthreads);
+}
+
+/* Attention of several query tokens per request (multi_one) for every
+ * (request, query slot t < q_len[b], head): q is [batch][max_q][hq][head_dim],
+ * out [batch][max_q][hq][head_dim], lse [batch][max_q][hq]; slots t >= q_len[b]
+ * are not written. */
+int32_t oracle_multi(const oracle_problem* pr, const int32_t* q_len, int32_t max_q, double* out,
+                     double* lse, int32_t nthreads) {
+  if (!check_problem(pr) || !q_len || max_q < 0 || !out || !lse) return OR_BAD_ARG;
+  task_set ts;
+  memset(&ts, 0, sizeof ts);
+  ts.pr = pr;
+  ts.kind = 3;
+  ts.q_len = q_len;
+  ts.max_q = max_q;
+  ts.n_bh = pr->batch * max_q * pr->hq;
+  ts.out = out;
+  ts.lse = lse;
   return run_tasks(&ts, nthreads);
 }

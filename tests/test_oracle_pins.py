@@ -322,6 +322,123 @@ def test_closed_forms_equal_and_one_hot_scores():
 
 
 # ---------------------------------------------------------------------------
+# several query tokens per request (chunked prefill under the same mask)
+# ---------------------------------------------------------------------------
+
+def test_multi_worked_example_all_queries_at_once():
+    """The worked example's eight queries as one chunk (P = 0, band B = 2, W = 4):
+    with equal scores and one-hot values the output of query t is its attention
+    weights, 1/count on the hand-derived band rows max(0, t-2) .. t."""
+    g = read_kv("worked_example_n8_w4_b2.txt")
+    N, W, B = int(g["N"][0]), int(g["W"][0]), int(g["B"][0])
+    counts = [int(x) for x in g["prefill_kept_counts"]]
+    assert sum(counts) == int(g["causal_sum"][0])
+    D = N
+    k = torch.zeros(1, 16, 1, D)
+    v = torch.zeros(1, 16, 1, D)
+    v[0, :N, 0, :] = torch.eye(N)                       # v_j = e_j
+    inp = dict(q=torch.randn(1, N, 1, D, generator=torch.Generator().manual_seed(8)),
+               k_pages=k, v_pages=v, page_table=np.array([[0]], np.int32),
+               seq_len=np.array([N], np.int32), prompt_len=np.array([0], np.int32),
+               window=np.array([W], np.int32),
+               keep_mask=wl.offsets_to_bits(range(1, B + 1), W, 1).reshape(1, 1, 1),
+               max_window=W)
+    out, lse = oracle.multi(inp, q_len=[N])
+    for t in range(N):
+        want = np.zeros(D)
+        want[max(0, t - B):t + 1] = 1.0 / counts[t]
+        assert np.max(np.abs(out[0, t, 0] - want)) < 1e-15, t
+        assert abs(lse[0, t, 0] - math.log(counts[t])) < 1e-15
+
+
+def multi_problem(seed, dtype="f32", B=3, Hq=4, Hkv=2, D=16, Qmax=7):
+    inp, klog, vlog, offs = logical_problem(seed, B=B, Hq=Hq, Hkv=Hkv, D=D, dtype=dtype)
+    rng = np.random.default_rng(seed + 1)
+    L = inp["seq_len"]
+    ql = np.array([int(rng.integers(0, min(Qmax, int(L[b])) + 1)) for b in range(B)], np.int32)
+    ql[0] = min(Qmax, int(L[0]))                         # at least one full chunk
+    g = torch.Generator().manual_seed(seed + 2)
+    dt = inp["q"].dtype
+    inp["q"] = torch.randn(B, Qmax, Hq, D, generator=g).to(dt)
+    return inp, klog, vlog, offs, ql
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_multi_vs_torch_sdpa_boolean_mask(dtype):
+    """Every query token of every request against torch float64 SDPA over the
+    test's own logical sequence, with a boolean [q_len, L] mask built from the
+    drawn offsets (not from the bit encoding)."""
+    for seed in (31, 32, 33):
+        inp, klog, vlog, offs, ql = multi_problem(seed, dtype)
+        B, Q, Hq, D = inp["q"].shape
+        g = Hq // inp["k_pages"].shape[2]
+        out, lse = oracle.multi(inp, q_len=ql)
+        scale = 1.0 / math.sqrt(D)
+        for b in range(B):
+            L, P, W = (int(inp[k][b]) for k in ("seq_len", "prompt_len", "window"))
+            n = int(ql[b])
+            assert np.isnan(out[b, n:]).all() and np.isnan(lse[b, n:]).all()
+            for t in range(n):
+                i = L - n + t
+                for h in range(Hq):
+                    keep = set(offs[b, h // g])
+                    allowed = [j <= i and (j < P or i == j or (i - j <= W and (i - j) in keep))
+                               for j in range(L)]
+                    o, l = sdpa_rows(inp["q"][b, t, h], klog[b][:, h // g], vlog[b][:, h // g],
+                                     allowed, scale)
+                    assert np.max(np.abs(out[b, t, h] - o)) < 1e-12
+                    assert abs(lse[b, t, h] - l) < 1e-12
+
+
+def test_multi_all_kept_is_causal_attention():
+    """An all-ones mask with W >= L keeps every earlier row: the chunk's queries
+    then see the bottom-right-aligned causal mask over the whole sequence."""
+    inp, klog, vlog, offs, ql = multi_problem(34, "f32")
+    B, Q, Hq, D = inp["q"].shape
+    g = Hq // inp["k_pages"].shape[2]
+    inp["window"] = np.full(B, inp["max_window"], np.int32)
+    inp["prompt_len"] = np.zeros(B, np.int32)
+    inp["keep_mask"] = np.full_like(inp["keep_mask"], 0xFFFFFFFF)
+    inp["seq_len"] = np.minimum(inp["seq_len"], inp["max_window"]).astype(np.int32)
+    ql = np.minimum(ql, inp["seq_len"]).astype(np.int32)
+    out, lse = oracle.multi(inp, q_len=ql)
+    for b in range(B):
+        L, n = int(inp["seq_len"][b]), int(ql[b])
+        if n == 0:
+            assert np.isnan(out[b]).all()
+            continue
+        causal = torch.ones(n, L, dtype=torch.bool).tril(diagonal=L - n)
+        for h in range(Hq):
+            qq = inp["q"][b, :n, h].double().view(1, 1, n, D)
+            kk = klog[b][:L, h // g].double().view(1, 1, L, D)
+            vv = vlog[b][:L, h // g].double().view(1, 1, L, D)
+            o = torch.nn.functional.scaled_dot_product_attention(qq, kk, vv, attn_mask=causal)
+            assert np.max(np.abs(out[b, :n, h] - o[0, 0].numpy())) < 1e-12
+
+
+def test_multi_skipped_rows_have_no_effect():
+    """Rows no query of the chunk keeps may hold anything (NaN, huge, negative)."""
+    inp, klog, vlog, offs, ql = multi_problem(35, "bf16")
+    base, lbase = oracle.multi(inp, q_len=ql)
+    g = inp["q"].shape[2] // inp["k_pages"].shape[2]
+
+    def kept(b, hk):
+        L, P, W = (int(inp[k][b]) for k in ("seq_len", "prompt_len", "window"))
+        rows = set()
+        for t in range(int(ql[b])):
+            rows.update(oracle.kept_set(L - int(ql[b]) + t + 1, P, W,
+                                        inp["keep_mask"][b, hk]).tolist())
+        return sorted(rows)
+
+    for value in (float("nan"), 1e30, -3.0):
+        p = wl.poison_unread(inp, kept, value)
+        out, lse = oracle.multi(p, q_len=ql)
+        assert np.array_equal(out, base, equal_nan=True)
+        assert np.array_equal(lse, lbase, equal_nan=True)
+    assert g == 2
+
+
+# ---------------------------------------------------------------------------
 # attention mass
 # ---------------------------------------------------------------------------
 
