@@ -7,9 +7,13 @@ from the keep mask (index compaction), gathers the kept K/V rows, runs the
 online softmax and PV, and (when rows are split) the LSE merge follows.  The
 same step as two calls, dsa_build_index (kept lists to HBM) + dsa_decode_sparse,
 and that decode alone are timed beside it.  Inputs are synthetic (seeded),
-shaped like the LlamaGen-XL-like workload by default (--workload llamagen-xl);
-others: --workload janus-pro-7b | emu3-8b | mixed-serving.  The dense causal decode of the same batch and the
-attention-mass pass are timed beside it.
+shaped like the mixed serving batch by default (--workload mixed-serving: 128
+requests, GQA group 4, head_dim 128, lengths up to P+4096, the largest
+single-GPU workload); others: --workload janus-pro-7b | llamagen-xl | emu3-8b.
+The dense causal decode of the same batch and the attention-mass pass are timed
+beside it, and (one GPU, unless --no-other-workloads) every other workload gets
+a compact line of its own under "workloads": fused step, roofline fraction,
+dense step, speedup and kept fraction.
 
 Timing: W eager warm-up steps, then K steps captured in one CUDA graph and
 replayed once between CUDA events (per-step = elapsed / K).  Consecutive steps
@@ -92,8 +96,10 @@ def parse_args():
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=10)
-    p.add_argument("--workload", default="llamagen-xl",
-                   choices=["llamagen-xl", "janus-pro-7b", "emu3-8b", "mixed-serving"])
+    p.add_argument("--workload", default="mixed-serving",
+                   choices=["mixed-serving", "janus-pro-7b", "llamagen-xl", "emu3-8b"])
+    p.add_argument("--no-other-workloads", action="store_true",
+                   help="skip the compact per-workload measurements of the other workloads")
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="CPU time budget of the oracle baseline sample")
@@ -307,6 +313,86 @@ def to_cpu_workload(w, bt):
     return c
 
 
+def kv_replicas(bt, kv_bytes, device, cap=64):
+    """The batch's KV pool plus copies, so that the rows R consecutive steps touch
+    exceed 4x the L2 (or as many copies as half the free memory holds)."""
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    pool = bt.k_pages.numel() * bt.k_pages.element_size() * 2
+    free, _ = torch.cuda.mem_get_info(device)
+    R = max(1, math.ceil(4 * l2 / max(kv_bytes, 1)))
+    R = int(max(1, min(R, cap, (0.5 * free) // pool)))
+    return [(bt.k_pages, bt.v_pages)] + [(bt.k_pages.clone(), bt.v_pages.clone())
+                                         for _ in range(R - 1)], l2
+
+
+def measure_compact(name, K, W, device, stream, peak):
+    """One workload's fused sparse step, two-call decode and dense decode, each a
+    K-step CUDA graph over rotating KV copies (as the headline), as a compact
+    dict."""
+    cfg = wl.WORKLOADS[name]
+    w = wl.generate(cfg, device=str(device))
+    bt = DecodeBatch.from_workload(w, device=device)
+    if cfg.mask == "top_mass":
+        _, om = bt.attention_mass(r_local=2, r_diag=2)
+        w["keep_mask"] = wl.top_mass_keep_mask(om.cpu().numpy(), w["window"], w["hkv"],
+                                               w["mask_words"], band=cfg.band,
+                                               frac=cfg.top_mass_frac)
+        bt.set_keep_mask(w["keep_mask"])
+    order = bt.schedule_order()
+    order = None if order is None else torch.as_tensor(order).to(device)
+    bt.build_index()
+    torch.cuda.synchronize()
+    bt.check(f"{name}: build_index")
+    by = step_bytes(w, bt.kept_idx.cpu().numpy(), bt.kept_cnt.cpu().numpy())
+    pools, l2 = kv_replicas(bt, by["kv"], device)
+    R, d = len(pools), bt.dims
+    out_2, lse_2 = torch.empty_like(bt.out), torch.empty_like(bt.lse)
+    out_d, lse_d = torch.empty_like(bt.out), torch.empty_like(bt.lse)
+
+    def fused(k):
+        kp, vp = pools[k % R]
+        dsa.dsa_decode_sparse_masked(d, bt.q, kp, vp, bt.page_table, bt.seq_len, bt.prompt_len,
+                                     bt.window, bt.keep_mask, bt.scale, bt.out, bt.lse, bt.ws,
+                                     stream, order)
+
+    def decode_only(k):
+        kp, vp = pools[k % R]
+        dsa.dsa_decode_sparse(d, bt.q, kp, vp, bt.page_table, bt.seq_len, bt.kept_idx,
+                              bt.kept_cnt, bt.scale, out_2, lse_2, bt.ws, stream)
+
+    def dense(k):
+        kp, vp = pools[k % R]
+        dsa.dsa_decode_dense(d, bt.q, kp, vp, bt.page_table, bt.seq_len, bt.scale, out_d, lse_d,
+                             bt.ws, stream)
+
+    for k in range(W):
+        fused(k)
+        decode_only(k)
+        dense(k)
+    torch.cuda.synchronize()
+    bt.check(f"{name}: warm-up")
+    graphs = [graph_of(f, K, stream) for f in (fused, decode_only, dense)]
+    for g in graphs:
+        g.replay()
+    torch.cuda.synchronize()
+    t_f, t_d, t_x = (time_graph(g, stream) / K for g in graphs)
+    bt.check(f"{name}: timed")
+    res = {
+        "workload": cfg.name, "batch": w["batch"], "hq": w["hq"], "hkv": w["hkv"],
+        "head_dim": w["head_dim"],
+        "step_us": 1e6 * t_f, "tokens_per_s": w["batch"] / t_f, "bytes": by["masked"],
+        "gbs": by["masked"] / t_f / 1e9, "frac": by["masked"] / t_f / 1e9 / peak,
+        "decode_only_us": 1e6 * t_d, "decode_only_frac": by["sparse_decode"] / t_d / 1e9 / peak,
+        "dense_us": 1e6 * t_x, "dense_frac": by["dense"] / t_x / 1e9 / peak,
+        "speedup": t_x / t_f, "kept_fraction": by["rows"] / by["dense_rows"],
+        "ideal_speedup": by["dense_rows"] / max(by["rows"], 1),
+        "kv_copies": R,
+    }
+    del graphs, pools, bt, w
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args):
     if args.sparse_cluster >= 0:
         dsa.dsa_set_sparse_cluster(args.sparse_cluster)
@@ -315,13 +401,20 @@ def run_ours(args):
     device = torch.device("cuda", local)
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=device)
+    # one non-default stream for everything (graph capture needs one)
+    stream = torch.cuda.Stream(device)
+    torch.cuda.set_stream(stream)
+    peak, peak_src = hbm_peak()
+    others = []
+    if world == 1 and not args.no_other_workloads:
+        for name in wl.WORKLOADS:
+            if name not in (args.workload, "tiny-fp32"):
+                others.append(measure_compact(name, max(10, min(args.steps, 50)),
+                                              max(3, min(args.warmup, 5)), device, stream, peak))
     cfg = wl.WORKLOADS[args.workload]
     w = wl.generate(cfg, seed=rank_seed(cfg, rank), device=str(device))
     bt = DecodeBatch.from_workload(w, device=device)
     torch.cuda.synchronize()
-    # one non-default stream for everything (graph capture needs one)
-    stream = torch.cuda.Stream(device)
-    torch.cuda.set_stream(stream)
 
     mass_ms = None
     if cfg.mask == "top_mass":
@@ -344,13 +437,8 @@ def run_ours(args):
     by = step_bytes(w, kept_idx, kept_cnt)
 
     # KV replicas so that consecutive steps never find their rows in L2
-    l2 = torch.cuda.get_device_properties(device).L2_cache_size
-    pool = bt.k_pages.numel() * bt.k_pages.element_size() * 2
-    free, _ = torch.cuda.mem_get_info(device)
-    R = max(1, math.ceil(4 * l2 / max(by["kv"], 1)))
-    R = int(max(1, min(R, 64, (0.5 * free) // pool)))
-    pools = [(bt.k_pages, bt.v_pages)] + [(bt.k_pages.clone(), bt.v_pages.clone())
-                                          for _ in range(R - 1)]
+    pools, l2 = kv_replicas(bt, by["kv"], device)
+    R = len(pools)
     d = bt.dims
     K, W = args.steps, args.warmup
 
@@ -553,7 +641,6 @@ def run_ours(args):
     B = w["batch"]
     step_s = t_step / K
     tokens = world * B / step_s
-    peak, peak_src = hbm_peak()
     chunk, nch, launches, warps, tile_rows = dsa.dsa_decode_plan(d, dsa.PLAN_MASKED)
     launches_two = dsa.dsa_decode_plan(d, dsa.PLAN_SPARSE)[2]
     achieved = by["masked"] / step_s / 1e9
@@ -628,23 +715,25 @@ def run_ours(args):
             "bound": "hbm", "bytes": mass_bytes, "achieved": mass_bytes / (mass_ms * 1e-3) / 1e9,
             "peak": peak, "unit": "GB/s", "frac": mass_bytes / (mass_ms * 1e-3) / 1e9 / peak},
         "eviction": eviction,
-        "e2e": {"value": world * B / (t_e2e / K), "unit": "tokens/s",
+        "e2e": {"value": world * B / (t_e2e_direct / K), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": 1e3 * t_e2e / K,
-                "host_us_per_step": 1e6 * host_e2e / K,
-                "call": "dsa_graph_launch per step of a recorded dsa_decode_sparse_masked_io "
-                        "(inputs up from pinned host memory, fused decode, out and lse down); "
-                        "two slots with their own buffers and streams, step k in slot k % 2",
-                "one_slot": {"tokens_per_s": world * B / (t_e2e_rec / K),
-                             "ms_per_step": 1e3 * t_e2e_rec / K,
-                             "host_us_per_step": 1e6 * host_rec / K,
-                             "call": "dsa_graph_launch per step, one slot: every step's "
-                                     "upload, decode and download in sequence"},
-                "direct": {"tokens_per_s": world * B / (t_e2e_direct / K),
-                           "ms_per_step": 1e3 * t_e2e_direct / K,
-                           "host_us_per_step": 1e6 * host_direct / K,
-                           "call": "dsa_decode_sparse_masked_io per step, one slot (one C "
-                                   "call: upload, fused decode, download)"}},
+                "ms_per_step": 1e3 * t_e2e_direct / K,
+                "host_us_per_step": 1e6 * host_direct / K,
+                "call": "dsa_decode_sparse_masked_io per step, one batch at a time: one C call "
+                        "uploads the packed inputs from pinned host memory, runs the fused "
+                        "decode and downloads out and lse",
+                "one_slot_graph": {"tokens_per_s": world * B / (t_e2e_rec / K),
+                                   "ms_per_step": 1e3 * t_e2e_rec / K,
+                                   "host_us_per_step": 1e6 * host_rec / K,
+                                   "call": "the same call recorded once as a dsa_graph, one "
+                                           "dsa_graph_launch per step, one batch at a time"},
+                "two_slot_pipeline": {"tokens_per_s": world * B / (t_e2e / K),
+                                      "ms_per_step": 1e3 * t_e2e / K,
+                                      "host_us_per_step": 1e6 * host_e2e / K,
+                                      "call": "two micro-batches in flight: two slots with their "
+                                              "own buffers and streams, step k in slot k % 2 "
+                                              "(recorded dsa_graph per slot), so one slot's copies "
+                                              "and kernel overlap the other's"}},
         "two_slots_device": {
             "tokens_per_s": world * B / (t_two_dev / K), "ms_per_step": 1e3 * t_two_dev / K,
             "note": "inputs resident, no copies; the two slots of the e2e run on two streams, "
@@ -652,6 +741,8 @@ def run_ours(args):
         "gpu_launches": K * launches,
         "clocks": clocks,
     }
+    if others:
+        result["workloads"] = others
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         w_cpu = to_cpu_workload(w, bt)

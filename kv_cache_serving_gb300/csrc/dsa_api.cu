@@ -229,17 +229,20 @@ struct RowSource {
   const void* v_new = nullptr;
 };
 
-dsa_status decode_launch(const dsa_dims* d, int mode, const void* q, const void* k,
-                         const void* v, const int32_t* page_table, const int32_t* seq_len,
-                         const RowSource& rs, float scale, float* out, float* lse, void* ws,
-                         cudaStream_t s);
+dsa_status decode_launch(const dsa_dims* d, int mode, const Plan& plan, const void* q,
+                         const void* k, const void* v, const int32_t* page_table,
+                         const int32_t* seq_len, const RowSource& rs, float scale, float* out,
+                         float* lse, void* ws, cudaStream_t s);
 
 // Checks a decode call's arguments, then (with io) the host-to-device copy, the
 // launches and (with io) the device-to-host copy, in that order on the stream.
+// `plan`, when given, is the split to launch with (computed once by a caller
+// that sized its scratch from it); else decode_plan() is taken here.
 dsa_status decode_common(const dsa_dims* d, int mode, const void* q, const void* k,
                          const void* v, const int32_t* page_table, const int32_t* seq_len,
                          const RowSource& rs, float scale, float* out, float* lse, void* ws,
-                         void* stream, const dsa_host_io* io = nullptr) {
+                         void* stream, const dsa_host_io* io = nullptr,
+                         const Plan* plan = nullptr) {
   const dsa_status st = check_dims(d);
   if (st != DSA_OK) return st;
   if (!q || !k || !v || !page_table || !seq_len || !out || !ws) return DSA_ERR_INVALID_ARG;
@@ -259,9 +262,11 @@ dsa_status decode_common(const dsa_dims* d, int mode, const void* q, const void*
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (io != nullptr && copy_host_to_device(io->dev_in, io->host_in, io->in_bytes, s) != cudaSuccess)
     return DSA_ERR_CUDA;
-  const dsa_status rc = d->batch == 0 ? DSA_OK
-                                      : decode_launch(d, mode, q, k, v, page_table, seq_len, rs,
-                                                      scale, out, lse, ws, s);
+  dsa_status rc = DSA_OK;
+  if (d->batch > 0) {
+    const Plan p = plan != nullptr ? *plan : decode_plan(d, mode);
+    rc = decode_launch(d, mode, p, q, k, v, page_table, seq_len, rs, scale, out, lse, ws, s);
+  }
   if (rc != DSA_OK) return rc;
   if (io != nullptr &&
       copy_device_to_host(io->host_out, io->dev_out, io->out_bytes, s) != cudaSuccess)
@@ -270,12 +275,11 @@ dsa_status decode_common(const dsa_dims* d, int mode, const void* q, const void*
 }
 
 // The launches of one decode call (arguments already checked, batch >= 1).
-dsa_status decode_launch(const dsa_dims* d, int mode, const void* q, const void* k,
-                         const void* v, const int32_t* page_table, const int32_t* seq_len,
-                         const RowSource& rs, float scale, float* out, float* lse, void* ws,
-                         cudaStream_t s) {
+dsa_status decode_launch(const dsa_dims* d, int mode, const Plan& plan, const void* q,
+                         const void* k, const void* v, const int32_t* page_table,
+                         const int32_t* seq_len, const RowSource& rs, float scale, float* out,
+                         float* lse, void* ws, cudaStream_t s) {
   const bool kv_bf16 = d->kv_dtype == DSA_BF16;
-  const Plan plan = decode_plan(d, mode);
   DecodeLaunch a{};
   a.q = q;
   a.q_bf16 = d->q_dtype == DSA_BF16;
@@ -638,7 +642,9 @@ extern "C" dsa_status dsa_decode_sparse_noalloc(const dsa_dims* dims, const void
   if (!q || !k_pages || !v_pages || !page_table || !seq_len || !kept_idx || !kept_cnt || !out)
     return DSA_ERR_INVALID_ARG;
   // Scratch this call needs: the header plus one partial per (request, query
-  // head, chunk), counted even when a single chunk leaves it unused.
+  // head, chunk), counted even when a single chunk leaves it unused.  The plan
+  // is taken once and the launch uses it, so the split checked here is the one
+  // launched even if dsa_set_sparse_cluster runs meanwhile on another thread.
   const Plan plan = decode_plan(dims, kModeList);
   const size_t need = kWsHeader + static_cast<size_t>(dims->batch) * dims->hq *
                                       static_cast<size_t>(plan.num_chunks > 0 ? plan.num_chunks
@@ -655,7 +661,7 @@ extern "C" dsa_status dsa_decode_sparse_noalloc(const dsa_dims* dims, const void
   rs.kept_idx = kept_idx;
   rs.kept_cnt = kept_cnt;
   const dsa_status rc = decode_common(dims, kModeList, q, k_pages, v_pages, page_table, seq_len,
-                                      rs, scale, out, lse, ws, stream);
+                                      rs, scale, out, lse, ws, stream, nullptr, &plan);
   if (rc != DSA_OK) return rc;
   if (dev_error != nullptr &&
       cudaMemcpyAsync(dev_error, ws, sizeof(int32_t), cudaMemcpyDeviceToDevice, s) != cudaSuccess)

@@ -214,17 +214,17 @@ def test_mixed_serving_reduced_batch():
 
 
 @pytest.mark.parametrize("name", ["llamagen-xl", "janus-pro-7b", "emu3-8b", "mixed-serving"])
-def test_workload_full_size_sampled(name):
-    """Full-size batches in the launch configuration the benchmark uses; kept lists compared in full, outputs on 48 sampled (b, h) pairs."""
+def test_workload_full_size(name):
+    """Full-size batches in the launch configuration the benchmark uses (its
+    builds, request order, waves and tails): kept lists and the outputs of every
+    (request, head) pair compared with the oracle, sparse and dense."""
     w = wl.generate(wl.WORKLOADS[name])
-    rng = np.random.default_rng(100 + list(wl.WORKLOADS).index(name))
-    bh = [(int(rng.integers(w["batch"])), int(rng.integers(w["hq"]))) for _ in range(48)]
     mask = None
     if name == "mixed-serving":
         _, om = oracle.mass(w, bh=None, with_offsets=True)
         om = om.reshape(w["batch"], w["hq"], -1)
         mask = wl.top_mass_keep_mask(om, w["window"], w["hkv"], w["mask_words"])
-    run_both(w, mask=mask, bh=bh)
+    run_both(w, mask=mask)
 
 
 @pytest.mark.parametrize("name,batch", [("mixed-serving", 64), ("janus-pro-7b", 20),
@@ -232,7 +232,7 @@ def test_workload_full_size_sampled(name):
 def test_small_batch_build(name, batch):
     """Batches that need two waves of the default build: the small-batch build
     (5 warps, one stage) where it fits them in one wave, kept lists and the
-    fused call, sampled pairs vs the oracle."""
+    fused call, every pair vs the oracle."""
     w = wl.generate(wl.scaled(wl.WORKLOADS[name], batch=batch))
     mask = top_mass_masks_from_oracle(w) if w["keep_mask"] is None else None
     bt = DecodeBatch.from_workload(w, keep_mask=mask)
@@ -243,9 +243,7 @@ def test_small_batch_build(name, batch):
         # build (on the tensor-core engine it holds no more CTAs, so the plan keeps
         # the default build there)
         assert plan[3] == 5, plan
-    rng = np.random.default_rng(7 + batch)
-    bh = [(int(rng.integers(w["batch"])), int(rng.integers(w["hq"]))) for _ in range(40)]
-    run_both(w, mask=mask, bh=bh)
+    run_both(w, mask=mask)
 
 
 # ---------------------------------------------------------------------------

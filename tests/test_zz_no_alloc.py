@@ -33,11 +33,8 @@ def test_noalloc_rejects_batches_beyond_its_scratch():
     assert dsa.dsa_status_string(st) == "DSA_ERR_SCRATCH_LIMIT"
 
 
-@pytest.mark.gpu
-@pytest.mark.parametrize("name,batch", [("janus-pro-7b", 12), ("mixed-serving", 16)])
-def test_noalloc_matches_workspace_entry_point(name, batch):
+def _batch(name, batch):
     from kv_cache_serving_gb300.session import DecodeBatch
-    assert torch.cuda.is_available()
     w = wl.generate(wl.scaled(wl.WORKLOADS[name], batch=batch))
     mask = w["keep_mask"]
     if mask is None:   # mixed-serving masks: band plus a fixed pattern of offsets
@@ -45,16 +42,23 @@ def test_noalloc_matches_workspace_entry_point(name, batch):
         for b in range(w["batch"]):
             offs = list(range(1, 9)) + list(range(9, int(w["window"][b]) + 1, 3))
             mask[b, :] = wl.offsets_to_bits(offs, int(w["window"][b]), w["mask_words"])
-    bt = DecodeBatch.from_workload(w, keep_mask=mask)
+    w = dict(w, keep_mask=mask)
+    bt = DecodeBatch.from_workload(w)
     bt.build_index()
-    ref_out, ref_lse = bt.decode_sparse()
-    ref_out, ref_lse = ref_out.clone(), ref_lse.clone()
+    return w, bt
+
+
+def _check_two_calls(w, bt):
+    """Two no-alloc calls in a row give the bits of dsa_decode_sparse on the same
+    plan, and both stay within the bf16 bars of the fp64 oracle."""
+    import oracle
+    ref_out, ref_lse = [t.clone() for t in bt.decode_sparse()]
     torch.cuda.synchronize()
     assert bt.device_error() == 0
     chunks = dsa.dsa_decode_plan(bt.dims, dsa.PLAN_SPARSE)[1]
     assert 256 + w["batch"] * w["hq"] * chunks * (w["head_dim"] + 2) * 4 <= \
         dsa.NOALLOC_SCRATCH_BYTES
-
+    want, want_lse = oracle.decode(w, sparse=True)
     for call in range(2):   # the scratch keeps the previous call's contents
         out = torch.full_like(ref_out, float("nan"))
         lse = torch.full_like(ref_lse, float("nan"))
@@ -64,7 +68,37 @@ def test_noalloc_matches_workspace_entry_point(name, batch):
                                       err)
         torch.cuda.synchronize()
         assert int(err.item()) == 0, call
-        diff = (out - ref_out).abs()
-        assert torch.isfinite(out).all()
-        assert diff.max().item() <= BF16_MAX and diff.mean().item() <= BF16_MEAN, call
-        assert (lse - ref_lse).abs().max().item() <= LSE_MAX, call
+        # same kernels, same plan, same summation order: the same bits
+        assert torch.equal(out, ref_out) and torch.equal(lse, ref_lse), call
+        diff = np.abs(out.cpu().numpy().reshape(want.shape).astype(np.float64) - want)
+        assert np.isfinite(diff).all()
+        assert diff.max() <= BF16_MAX and diff.mean() <= BF16_MEAN, call
+        assert np.abs(lse.cpu().numpy().reshape(-1) - want_lse).max() <= LSE_MAX, call
+    return chunks
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name,batch", [("janus-pro-7b", 12), ("mixed-serving", 16)])
+def test_noalloc_matches_workspace_entry_point(name, batch):
+    assert torch.cuda.is_available()
+    w, bt = _batch(name, batch)
+    _check_two_calls(w, bt)
+
+
+@pytest.mark.gpu
+def test_noalloc_split_rows_merge_through_the_fixed_scratch():
+    """Clusters off and a batch small enough that each (request, kv head) is cut
+    into several chunks: the chunk partials go through the fixed scratch array
+    and are combined by the merge kernel, call after call."""
+    assert torch.cuda.is_available()
+    saved = dsa.dsa_get_sparse_cluster()
+    try:
+        dsa.dsa_set_sparse_cluster(1)
+        w, bt = _batch("janus-pro-7b", 2)
+        plan = dsa.dsa_decode_plan(bt.dims, dsa.PLAN_SPARSE)
+        assert plan[1] > 1 and plan[2] == 2, plan   # several chunks, merge launch
+        cnt = bt.kept_cnt.cpu().numpy()
+        assert (cnt > plan[0]).all()                # every unit really is split
+        _check_two_calls(w, bt)
+    finally:
+        dsa.dsa_set_sparse_cluster(saved)
