@@ -90,7 +90,9 @@ enum {
   DSA_DEV_TIMEOUT = 7,      /* a bounded wait for an async copy gave up    */
   DSA_DEV_BAD_GRID_W = 8,   /* grid width < 1 (attention mass)             */
   DSA_DEV_BAD_ORDER = 9,    /* request_order entry outside 0..batch-1      */
-  DSA_DEV_FREE_LIST_FULL = 10 /* dsa_evict_pages: more pages than capacity   */
+  DSA_DEV_FREE_LIST_FULL = 10, /* dsa_evict_pages: more pages than capacity  */
+  DSA_DEV_BAD_QLEN = 11     /* dsa_prefill_sparse: q_len < 0 or above
+                               min(seq_len, max_q)                          */
 };
 
 /* Problem sizes, shared by all calls on one KV cache. */
@@ -315,6 +317,40 @@ dsa_status dsa_attention_mass(const dsa_dims* dims, const void* q, const void* k
                               const int32_t* grid_w, int32_t r_local, int32_t r_diag,
                               float scale, float* mass, float* offset_mass, void* ws,
                               void* stream);
+
+/*
+ * dsa_prefill_sparse -- several query tokens per request under the same mask:
+ * a chunk of prompt or image tokens prefilled at once, or several image tokens
+ * decoded in one step.  The last q_len[b] rows of request b's cache are its
+ * query tokens i = L_b - q_len[b] + t, t = 0 .. q_len[b]-1 (their K/V rows must
+ * already be in the cache), and query i attends over its own causal kept set,
+ * the set of dsa_build_index for a request of length i+1:
+ *   K_i(b,hk) = { j < min(P_b, i+1) } U { i } U { i-o : 1 <= o <= W_b, bit o-1, i-o >= P_b }
+ * -- the core formula of the paper-daily summary (section 核心公式) read at
+ * every query position, with masked entries removed.  The arXiv abstract
+ * reports prefill attention to be diffuse, so a chunk gains less from the mask
+ * than a decode step; the call serves chunks that keep the decode mask.
+ *   max_q             query slots per request (>= 0; 0 is a no-op)
+ *   q                 [batch][max_q][hq][head_dim] bf16 (device); slot t of
+ *                     request b is query token L_b - q_len[b] + t
+ *   k_pages, v_pages, page_table, seq_len, prompt_len, window, keep_mask
+ *                     as in dsa_decode_sparse_masked (K/V bf16)
+ *   q_len             [batch] int32 (device), 0 <= q_len[b] <= min(L_b, max_q)
+ *   scale             softmax scale, normally 1/sqrt(head_dim)
+ *   out   (out)       [batch][max_q][hq][head_dim] float32; slots t >= q_len[b]
+ *                     are not written
+ *   lse   (out)       [batch][max_q][hq] float32 natural-log LSE, or NULL
+ * Rows of the scanned range that no query of a CTA's tile keeps are not read.
+ * q and KV must be bf16 and max_window <= 32768, else DSA_ERR_UNSUPPORTED.  An
+ * invalid per-request value (seq_len, prompt_len, window as above; q_len gives
+ * DSA_DEV_BAD_QLEN) sets the error word and NaN in that request's slots.
+ */
+dsa_status dsa_prefill_sparse(const dsa_dims* dims, int32_t max_q, const void* q,
+                              const void* k_pages, const void* v_pages,
+                              const int32_t* page_table, const int32_t* seq_len,
+                              const int32_t* q_len, const int32_t* prompt_len,
+                              const int32_t* window, const uint32_t* keep_mask, float scale,
+                              float* out, float* lse, void* ws, void* stream);
 
 /*
  * dsa_evict_pages -- unmap the pages no later decode step can read, and hand

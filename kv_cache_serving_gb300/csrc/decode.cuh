@@ -74,6 +74,11 @@ namespace dsa {
 #ifndef DSA_DECODE_WARPS
 #define DSA_DECODE_WARPS 4
 #endif
+// Cluster launches (sparse decode split over a thread-block cluster) are also
+// programmatic dependents when set.
+#ifndef DSA_PDL_CLUSTER
+#define DSA_PDL_CLUSTER 0
+#endif
 
 template <int D, typename KV, int G, bool MMA = false, int NWARPS = DSA_DECODE_WARPS,
           int STAGE_BYTES = DSA_DECODE_STAGE_BYTES, int STAGES = DSA_DECODE_STAGES>
@@ -655,20 +660,24 @@ cudaError_t launch_decode_one(const DecodeLaunch& a, cudaStream_t s) {
   cfg.blockDim = dim3(Tl::NW * 32);
   cfg.dynamicSmemBytes = static_cast<size_t>(smem);
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
+  int na = 0;
   if (a.cluster > 1) {
     // the CTAs of one (request, kv head) form one cluster along x
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(a.cluster);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-  } else {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = static_cast<unsigned>(a.cluster);
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  if (a.cluster <= 1 || DSA_PDL_CLUSTER) {
     // programmatic dependent launch: scheduled while the previous kernel drains
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = DSA_PDL;
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = DSA_PDL;
+    ++na;
   }
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = na;
   return cudaLaunchKernelEx(&cfg, kern, a);
 }
 

@@ -505,6 +505,53 @@ dsa_status dsa_attention_mass(const dsa_dims* dims, const void* q, const void* k
   return from_cuda(launch_mass(a, dims->kv_dtype == DSA_BF16, static_cast<cudaStream_t>(stream)));
 }
 
+dsa_status dsa_prefill_sparse(const dsa_dims* dims, int32_t max_q, const void* q,
+                              const void* k_pages, const void* v_pages,
+                              const int32_t* page_table, const int32_t* seq_len,
+                              const int32_t* q_len, const int32_t* prompt_len,
+                              const int32_t* window, const uint32_t* keep_mask, float scale,
+                              float* out, float* lse, void* ws, void* stream) {
+  const dsa_status st = check_dims(dims);
+  if (st != DSA_OK) return st;
+  if (max_q < 0 || !q || !k_pages || !v_pages || !page_table || !seq_len || !q_len ||
+      !prompt_len || !window || !keep_mask || !out || !ws)
+    return DSA_ERR_INVALID_ARG;
+  if (!(scale == scale) || !aligned(ws, 256) || !aligned(q, 16) || !aligned(k_pages, 16) ||
+      !aligned(v_pages, 16) || !aligned(out, 8) || !aligned(lse, 4))
+    return DSA_ERR_INVALID_ARG;
+  if (dims->q_dtype != DSA_BF16 || dims->kv_dtype != DSA_BF16 ||
+      dims->max_window > kMultiMaxWindow)
+    return DSA_ERR_UNSUPPORTED;
+  if (dims->hkv > 65535 || dims->batch > 65535) return DSA_ERR_UNSUPPORTED;  // grid y, z
+  if (dims->batch == 0 || max_q == 0) return DSA_OK;
+  MultiLaunch a{};
+  a.q = q;
+  a.k = k_pages;
+  a.v = v_pages;
+  a.page_table = page_table;
+  a.seq_len = seq_len;
+  a.q_len = q_len;
+  a.prompt_len = prompt_len;
+  a.window = window;
+  a.keep_mask = keep_mask;
+  a.batch = dims->batch;
+  a.hq = dims->hq;
+  a.hkv = dims->hkv;
+  a.head_dim = dims->head_dim;
+  a.max_pages = dims->max_pages_per_req;
+  a.num_pages = dims->num_pages;
+  a.max_window = dims->max_window;
+  a.mask_words = dims->mask_words;
+  a.max_q = max_q;
+  const int per_cta = multi_queries_per_cta(dims->hq / dims->hkv);
+  a.q_tiles = static_cast<int32_t>(ceil_div(max_q, per_cta));
+  a.scale_log2 = scale * kLog2e;
+  a.out = out;
+  a.lse = lse;
+  a.err = err_word(ws);
+  return from_cuda(launch_multi(a, static_cast<cudaStream_t>(stream)));
+}
+
 dsa_status dsa_decode_plan(const dsa_dims* dims, int32_t mode, int32_t* chunk,
                            int32_t* num_chunks, int32_t* launches, int32_t* warps,
                            int32_t* tile_rows) {

@@ -85,6 +85,25 @@ struct EvictLaunch {
   int32_t* err;
 };
 
+// Several query tokens per request (prefill.cu): q [batch][max_q][hq][head_dim].
+struct MultiLaunch {
+  const void* q;
+  const void* k;
+  const void* v;
+  const int32_t* page_table;
+  const int32_t* seq_len;
+  const int32_t* q_len;       // [batch] query tokens of each request (its last rows)
+  const int32_t* prompt_len;
+  const int32_t* window;
+  const uint32_t* keep_mask;  // [batch][hkv][mask_words]
+  int32_t batch, hq, hkv, head_dim, max_pages, num_pages, max_window, mask_words, max_q;
+  int32_t q_tiles;            // CTAs along the query axis of one (request, kv head)
+  float scale_log2;
+  float* out;                 // [batch][max_q][hq][head_dim]
+  float* lse;                 // [batch][max_q][hq] or null
+  int32_t* err;
+};
+
 // Row sources of a decode launch (`mode` below).
 constexpr int kModeDense = 0;  // rows 0..L-1
 constexpr int kModeList = 1;   // kept_idx / kept_cnt from dsa_build_index
@@ -106,6 +125,12 @@ int mass_rows_per_pass(int head_dim, int group, bool kv_bf16, bool q_bf16);
 bool mass_uses_tensor_cores(bool kv_bf16, bool q_bf16, int group);
 int mass_ctas_per_sm(int head_dim, int group, bool kv_bf16, bool q_bf16);
 cudaError_t launch_compact(const CompactLaunch& a, cudaStream_t s);
+// Several query tokens per request: bf16 q and KV only; queries per CTA for a
+// group size (the CTA holds 64 (query, head) rows).
+cudaError_t launch_multi(const MultiLaunch& a, cudaStream_t s);
+int multi_queries_per_cta(int group);
+// Largest max_window of the multi-query call (its mask words sit in shared memory).
+constexpr int kMultiMaxWindow = 32768;
 cudaError_t launch_evict(const EvictLaunch& a, cudaStream_t s);
 
 // Host copies of a step (hostio.cu): a copy kernel when the host side is

@@ -1,0 +1,396 @@
+// prefill.cu -- several query tokens per request under the diagonal-aware mask
+// (a chunk of prompt or image tokens prefilled, or several image tokens decoded,
+// in one step).
+//
+// Method: the masked softmax of "Understanding and Exploiting Diagonal Attention
+// Sparsity in Autoregressive Image Generation" (paper-daily summary, section
+// 核心公式 / core formula), applied at every query position of the chunk: the
+// last n rows of a request's cache are its query tokens i = L-n .. L-1, and
+// query i attends over its own causal kept set -- every prompt row j < P, the
+// row i itself, and the window rows i-o (1 <= o <= W) whose mask bit o-1 is
+// set (arXiv abstract: entries along the diagonal inside the recent window are
+// skipped).  The abstract also reports prefill attention to be diffuse; the
+// call serves chunks whose queries share one mask, as decode steps do.
+//
+// Work decomposition: grid (query tile, kv head, request).  A CTA holds 64
+// (query, head) rows -- 64/G consecutive query tokens times the G query heads
+// of one kv head -- and scans the union of their kept rows: the prompt rows
+// [0, min(P, i_last+1)) and the window range [max(., i_first-W), i_last].
+// This is a dense contraction (every staged K/V row meets up to 64 query rows),
+// so it runs on the tensor cores: each warp owns 16 (query, head) rows, its q
+// fragments stay in registers, S = q K^T and O += P V are mma.sync m16n8k16
+// (bf16 in, fp32 accumulate), the online softmax runs in the log2 domain, and a
+// (query, row) pair the query does not keep is masked to -inf before it.
+//
+// Staging: blocks of 32 consecutive row positions, K then V, in a ring of
+// DSA_MQ_STAGES stages shared by the CTA's warps.  Warp 0 fills a stage with one
+// bulk async copy per K row and per V row (completing on the stage's "full"
+// mbarrier with the expected byte count); every warp arrives on the stage's
+// "empty" mbarrier once its reads are done, and warp 0 refills the stage after
+// that.  A row in the scanned range that no query of the tile keeps is never
+// read: its slot is zero-filled instead, so skipped rows have no effect even
+// when they hold NaN (0 x NaN would be NaN inside the mma).  Every wait is
+// bounded (DSA_DEV_TIMEOUT).
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+#include "mma.cuh"
+
+#ifndef DSA_MQ_STAGES
+#define DSA_MQ_STAGES 3
+#endif
+
+namespace dsa {
+namespace {
+
+constexpr int kMqWarps = 4;               // warps per CTA
+constexpr int kMqRows = 16 * kMqWarps;    // (query, head) rows per CTA
+constexpr int kMqBlock = 32;              // K/V rows per staged block
+
+template <int D>
+struct MqTiling {
+  static constexpr int kRowBytes = D * 2;              // bf16
+  static constexpr int kStride = kRowBytes + 16;       // padded: conflict-free ldmatrix
+  static constexpr int kStage = 2 * kMqBlock * kStride;  // K rows, then V rows
+  static constexpr int kS = DSA_MQ_STAGES;
+  static constexpr int kBarOff = kS * kStage;          // full[kS], empty[kS]
+  static constexpr int kMaskOff = kBarOff + 2 * kS * 8;
+  static int smem(int mask_words) { return kMaskOff + mask_words * 4; }
+  static_assert(kStage % 128 == 0, "stage alignment");
+};
+
+// Two floats as packed bf16 (lo in the low half), round to nearest even.
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Any set bit among bits lo..hi (inclusive, 0 <= lo <= hi) of the words at m.
+__device__ __forceinline__ bool any_bit(const uint32_t* m, int lo, int hi) {
+  for (int w = lo >> 5; w <= (hi >> 5); ++w) {
+    uint32_t x = m[w];
+    if (w == (lo >> 5)) x &= 0xffffffffu << (lo & 31);
+    if (w == (hi >> 5) && (hi & 31) != 31) x &= (2u << (hi & 31)) - 1u;
+    if (x != 0u) return true;
+  }
+  return false;
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(kMqWarps * 32, 2) multi_kernel(const MultiLaunch a) {
+  using Tl = MqTiling<D>;
+  constexpr int QT = kMqRows / G;   // query tokens per CTA
+  constexpr int NKD = D / 16;       // k-steps of S = q K^T
+  constexpr int NTD = D / 8;        // 8-column tiles of O
+  constexpr int S = Tl::kS;
+  extern __shared__ __align__(128) unsigned char smem[];
+
+  griddep_wait();
+  griddep_launch_dependents();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g4 = lane >> 2, tig = lane & 3;
+  const int qtile = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
+  const int L = a.seq_len[b], n = a.q_len[b], P = a.prompt_len[b], W = a.window[b];
+  int code = 0;
+  if (L < 1 || L > a.max_pages * kPage) code = DSA_DEV_BAD_SEQ_LEN;
+  else if (n < 0 || n > L || n > a.max_q) code = DSA_DEV_BAD_QLEN;
+  else if (P < 0) code = DSA_DEV_BAD_PROMPT;
+  else if (W < 0 || W > a.max_window) code = DSA_DEV_BAD_WINDOW;
+  const int t0 = qtile * QT;
+  if (code != 0) {
+    // q_len is not trusted: NaN into every slot this CTA covers
+    if (qtile == 0 && hk == 0 && threadIdx.x == 0) set_error(a.err, code);
+    for (int x = threadIdx.x; x < QT * G * D; x += kMqWarps * 32) {
+      const int t = t0 + x / (G * D);
+      if (t >= a.max_q) break;
+      const size_t qh = (static_cast<size_t>(b) * a.max_q + t) * a.hq + hk * G + (x / D) % G;
+      a.out[qh * D + x % D] = __int_as_float(0x7fc00000);
+      if (a.lse != nullptr && x % D == 0) a.lse[qh] = __int_as_float(0x7fc00000);
+    }
+    return;
+  }
+  if (t0 >= n) return;
+  const int t1 = min(t0 + QT, n);
+  const int i_first = L - n + t0, i_last = L - n + t1 - 1;
+  // scanned positions: prompt rows [0, nA), then window rows [bstart, i_last]
+  const int nA = min(P, i_last + 1);
+  const int bstart = max(nA, i_first - W);
+  const int R = nA + (i_last >= bstart ? i_last - bstart + 1 : 0);
+  const int nblocks = (R + kMqBlock - 1) / kMqBlock;
+  auto row_of = [&](int p) { return p < nA ? p : bstart + (p - nA); };
+
+  uint32_t* msk = reinterpret_cast<uint32_t*>(smem + Tl::kMaskOff);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Tl::kBarOff);
+  uint64_t* empty = full + S;
+  {
+    const uint32_t* mrow = a.keep_mask + (static_cast<size_t>(b) * a.hkv + hk) * a.mask_words;
+    for (int x = threadIdx.x; x < a.mask_words; x += kMqWarps * 32) msk[x] = __ldg(mrow + x);
+  }
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kMqWarps);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  const bf16_t* kg = reinterpret_cast<const bf16_t*>(a.k);
+  const bf16_t* vg = reinterpret_cast<const bf16_t*>(a.v);
+  const int32_t* pt = a.page_table + static_cast<size_t>(b) * a.max_pages;
+
+  // Warp 0: stage block `blk` into stage s.  Lane l serves position 32 blk + l.
+  auto produce = [&](int blk, int s) {
+    const int p = blk * kMqBlock + lane;
+    const int j = p < R ? row_of(p) : 0;
+    bool need = false;
+    if (p < R) {
+      if (j < nA || j >= i_first) {
+        need = true;  // a prompt row (query i_last keeps it) or a query's own row
+      } else {
+        // kept by query i in [i_first, i_last] iff bit (i-j-1) is set, i-j <= W
+        const int lo = i_first - j, hi = min(W, i_last - j);
+        need = lo <= hi && any_bit(msk, lo - 1, hi - 1);
+      }
+    }
+    unsigned char* kst = smem + s * Tl::kStage;
+    unsigned char* vst = kst + kMqBlock * Tl::kStride;
+    const unsigned need_mask = __ballot_sync(0xffffffffu, need);
+    if (!need) {
+      // not read: zeros (finite under p = 0) in the K and V slots of this row
+#pragma unroll
+      for (int x = 0; x < Tl::kRowBytes; x += 16) {
+        *reinterpret_cast<uint4*>(kst + lane * Tl::kStride + x) = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(vst + lane * Tl::kStride + x) = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    // this warp's earlier generic accesses of the stage before the async writes
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0)
+      mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(__popc(need_mask) * 2 * Tl::kRowBytes));
+    __syncwarp();
+    if (need) {
+      int pg = __ldg(pt + (j >> 4));
+      if (static_cast<unsigned>(pg) >= static_cast<unsigned>(a.num_pages)) {
+        set_error(a.err, DSA_DEV_BAD_PAGE);
+        pg = 0;
+      }
+      const size_t off = ((static_cast<size_t>(pg) * kPage + (j & (kPage - 1))) * a.hkv + hk) * D;
+      bulk_copy_g2s(kst + lane * Tl::kStride, kg + off, Tl::kRowBytes, &full[s]);
+      bulk_copy_g2s(vst + lane * Tl::kStride, vg + off, Tl::kRowBytes, &full[s]);
+    }
+  };
+
+  int produced = 0;
+  if (warp == 0) {
+    for (; produced < S && produced < nblocks; ++produced) produce(produced, produced);
+  }
+
+  // This thread's two (query, head) rows of the warp's 16: r0 = g4, r1 = g4 + 8.
+  const int pr0 = warp * 16 + g4, pr1 = pr0 + 8;
+  const bool v0 = t0 + pr0 / G < t1, v1 = t0 + pr1 / G < t1;
+  const int iq0 = i_first + pr0 / G, iq1 = i_first + pr1 / G;
+  const size_t qrow0 = (static_cast<size_t>(b) * a.max_q + t0 + pr0 / G) * a.hq + hk * G + pr0 % G;
+  const size_t qrow1 = (static_cast<size_t>(b) * a.max_q + t0 + pr1 / G) * a.hq + hk * G + pr1 % G;
+  const bool warp_active = t0 + (warp * 16) / G < t1;
+  uint32_t qa[NKD][4];
+  {
+    const uint32_t* q32 = reinterpret_cast<const uint32_t*>(a.q);
+#pragma unroll
+    for (int kk = 0; kk < NKD; ++kk) {
+      const int c = (16 * kk + 2 * tig) / 2;  // 32-bit word of the pair
+      qa[kk][0] = v0 ? __ldg(q32 + qrow0 * (D / 2) + c) : 0u;
+      qa[kk][1] = v1 ? __ldg(q32 + qrow1 * (D / 2) + c) : 0u;
+      qa[kk][2] = v0 ? __ldg(q32 + qrow0 * (D / 2) + c + 4) : 0u;
+      qa[kk][3] = v1 ? __ldg(q32 + qrow1 * (D / 2) + c + 4) : 0u;
+    }
+  }
+  float o[NTD][4];
+#pragma unroll
+  for (int nt = 0; nt < NTD; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) o[nt][e] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+  // kept(i, j) for a valid query i and a scanned row j
+  auto kept = [&](int i, int j) -> bool {
+    if (j > i) return false;
+    if (j < P) return true;
+    const int off = i - j;
+    if (off == 0) return true;
+    if (off > W) return false;
+    return (msk[(off - 1) >> 5] >> ((off - 1) & 31)) & 1u;
+  };
+
+  bool failed = false;
+  int k = 0;
+  for (; k < nblocks; ++k) {
+    const int s = k % S;
+    if (!__all_sync(0xffffffffu, mbar_wait(&full[s], static_cast<uint32_t>(k / S) & 1u))) {
+      failed = true;
+      break;
+    }
+    if (warp_active) {
+      const unsigned char* kst = smem + s * Tl::kStage;
+      const unsigned char* vst = kst + kMqBlock * Tl::kStride;
+      // S = q K^T over the block's 32 rows: four 8-row tiles
+      float sc[4][4];
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sc[nt][e] = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < NKD; ++kk)
+#pragma unroll
+        for (int np = 0; np < 2; ++np) {
+          uint32_t bf[4];
+          ldsm_x4(bf, kst + (np * 16 + ((lane >> 4) & 1) * 8 + (lane & 7)) * Tl::kStride +
+                          (16 * kk + ((lane >> 3) & 1) * 8) * 2);
+          mma_bf16(sc[2 * np], qa[kk], bf[0], bf[1]);
+          mma_bf16(sc[2 * np + 1], qa[kk], bf[2], bf[3]);
+        }
+      // scale; mask pairs the query does not keep (and positions past R)
+      const int p0 = k * kMqBlock;
+      const bool plain = p0 + kMqBlock <= nA && p0 + kMqBlock - 1 <= i_first;
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int p = p0 + nt * 8 + 2 * tig + c;
+          const int j = row_of(p);
+          const bool in = p < R;
+          const bool k0 = v0 && in && (plain || kept(iq0, j));
+          const bool k1 = v1 && in && (plain || kept(iq1, j));
+          sc[nt][c] = k0 ? sc[nt][c] * a.scale_log2 : -INFINITY;
+          sc[nt][2 + c] = k1 ? sc[nt][2 + c] * a.scale_log2 : -INFINITY;
+        }
+      // online softmax of rows r0 (elements 0, 1) and r1 (elements 2, 3)
+      float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        mx0 = fmaxf(mx0, fmaxf(sc[nt][0], sc[nt][1]));
+        mx1 = fmaxf(mx1, fmaxf(sc[nt][2], sc[nt][3]));
+      }
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      // a row with no kept entry yet keeps m = -inf, o = l = 0
+      const float al0 = mn0 == -INFINITY ? 1.f : exp2f(m0 - mn0);
+      const float al1 = mn1 == -INFINITY ? 1.f : exp2f(m1 - mn1);
+      const float bs0 = mn0 == -INFINITY ? 0.f : mn0, bs1 = mn1 == -INFINITY ? 0.f : mn1;
+      m0 = mn0;
+      m1 = mn1;
+      float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        sc[nt][0] = exp2f(sc[nt][0] - bs0);
+        sc[nt][1] = exp2f(sc[nt][1] - bs0);
+        sc[nt][2] = exp2f(sc[nt][2] - bs1);
+        sc[nt][3] = exp2f(sc[nt][3] - bs1);
+        ps0 += sc[nt][0] + sc[nt][1];
+        ps1 += sc[nt][2] + sc[nt][3];
+      }
+      l0 = l0 * al0 + ps0;
+      l1 = l1 * al1 + ps1;
+#pragma unroll
+      for (int nt = 0; nt < NTD; ++nt) {
+        o[nt][0] *= al0;
+        o[nt][1] *= al0;
+        o[nt][2] *= al1;
+        o[nt][3] *= al1;
+      }
+      // O += P V: P (bf16) straight from the score registers as A fragments
+#pragma unroll
+      for (int j2 = 0; j2 < 2; ++j2) {
+        uint32_t pa[4];
+        pa[0] = pack_bf16(sc[2 * j2][0], sc[2 * j2][1]);
+        pa[1] = pack_bf16(sc[2 * j2][2], sc[2 * j2][3]);
+        pa[2] = pack_bf16(sc[2 * j2 + 1][0], sc[2 * j2 + 1][1]);
+        pa[3] = pack_bf16(sc[2 * j2 + 1][2], sc[2 * j2 + 1][3]);
+#pragma unroll
+        for (int dp = 0; dp < NTD / 2; ++dp) {
+          uint32_t bf[4];
+          ldsm_x4_trans(bf, vst + (16 * j2 + ((lane >> 3) & 1) * 8 + (lane & 7)) * Tl::kStride +
+                                (16 * dp + (lane >> 4) * 8) * 2);
+          mma_bf16(o[2 * dp], pa, bf[0], bf[1]);
+          mma_bf16(o[2 * dp + 1], pa, bf[2], bf[3]);
+        }
+      }
+    }
+    // this warp's reads of the stage are done
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+    if (warp == 0 && k + S < nblocks) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&empty[s], static_cast<uint32_t>(k / S) & 1u))) {
+        failed = true;
+        ++k;  // block k itself was consumed
+        break;
+      }
+      produce(k + S, s);
+      ++produced;
+    }
+  }
+  if (failed) {
+    if (lane == 0) set_error(a.err, DSA_DEV_TIMEOUT);
+    // copies warp 0 issued and nobody waited for: give them a bounded chance to land
+    if (warp == 0)
+      for (int kb = k; kb < produced; ++kb)
+        mbar_wait(&full[kb % S], static_cast<uint32_t>(kb / S) & 1u);
+    return;
+  }
+  if (!warp_active) return;
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+  const float r0 = 1.f / l0, r1 = 1.f / l1;
+#pragma unroll
+  for (int nt = 0; nt < NTD; ++nt) {
+    const int d = 8 * nt + 2 * tig;
+    if (v0) *reinterpret_cast<float2*>(a.out + qrow0 * D + d) = make_float2(o[nt][0] * r0, o[nt][1] * r0);
+    if (v1) *reinterpret_cast<float2*>(a.out + qrow1 * D + d) = make_float2(o[nt][2] * r1, o[nt][3] * r1);
+  }
+  if (a.lse != nullptr && tig == 0) {
+    if (v0) a.lse[qrow0] = (m0 + log2f(l0)) * kLn2;
+    if (v1) a.lse[qrow1] = (m1 + log2f(l1)) * kLn2;
+  }
+}
+
+template <int D, int G>
+cudaError_t launch_multi_one(const MultiLaunch& a, cudaStream_t s) {
+  const int smem = MqTiling<D>::smem(a.mask_words);
+  auto kern = multi_kernel<D, G>;
+  const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(kern, dim3(a.q_tiles, a.hkv, a.batch), dim3(kMqWarps * 32),
+                    static_cast<size_t>(smem), s, a);
+}
+
+}  // namespace
+
+int multi_queries_per_cta(int group) { return kMqRows / group; }
+
+cudaError_t launch_multi(const MultiLaunch& a, cudaStream_t s) {
+  const int g = a.hq / a.hkv;
+#define DSA_MQ_CASE(DD, GG) \
+  if (a.head_dim == DD && g == GG) return launch_multi_one<DD, GG>(a, s);
+  DSA_MQ_CASE(64, 1)
+  DSA_MQ_CASE(64, 2)
+  DSA_MQ_CASE(64, 4)
+  DSA_MQ_CASE(64, 8)
+  DSA_MQ_CASE(128, 1)
+  DSA_MQ_CASE(128, 2)
+  DSA_MQ_CASE(128, 4)
+  DSA_MQ_CASE(128, 8)
+#undef DSA_MQ_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace dsa

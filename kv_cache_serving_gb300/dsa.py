@@ -18,7 +18,8 @@ DSA_OK, DSA_ERR_INVALID_ARG, DSA_ERR_UNSUPPORTED, DSA_ERR_CUDA, DSA_ERR_DEVICE, 
 NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 DSA_F32, DSA_BF16 = 0, 1
 DEV_ERRORS = {0: "OK", 1: "BAD_SEQ_LEN", 2: "BAD_PROMPT", 3: "BAD_WINDOW", 4: "BAD_PAGE",
-              5: "BAD_INDEX", 6: "BAD_COUNT", 7: "TIMEOUT", 8: "BAD_GRID_W"}
+              5: "BAD_INDEX", 6: "BAD_COUNT", 7: "TIMEOUT", 8: "BAD_GRID_W", 9: "BAD_ORDER",
+              10: "FREE_LIST_FULL", 11: "BAD_QLEN"}
 PAGE = 16
 
 
@@ -76,6 +77,7 @@ def _load():
         "dsa_decode_sparse_masked_io": ([ctypes.POINTER(dsa_host_io), D, P, P, P, P, P, P, P, P,
                                          P, P, P, F32, P, P, P, P], I32),
         "dsa_decode_dense": ([D, P, P, P, P, P, F32, P, P, P, P], I32),
+        "dsa_prefill_sparse": ([D, I32, P, P, P, P, P, P, P, P, P, F32, P, P, P, P], I32),
         "dsa_attention_mass": ([D, P, P, P, P, P, P, P, I32, I32, F32, P, P, P, P], I32),
         "dsa_decode_plan": ([D, I32, ctypes.POINTER(I32), ctypes.POINTER(I32),
                              ctypes.POINTER(I32), ctypes.POINTER(I32), ctypes.POINTER(I32)],
@@ -346,6 +348,23 @@ def dsa_decode_dense(dims, q, k_pages, v_pages, page_table, seq_len, scale, out,
         _ptr(v_pages, _QKV, "v_pages"), _ptr(page_table, _I32, "page_table"),
         _ptr(seq_len, _I32, "seq_len"), float(scale), _ptr(out, torch.float32, "out"),
         _ptr(lse, torch.float32, "lse"), _ptr(ws), _stream(stream)), "dsa_decode_dense")
+
+
+def dsa_prefill_sparse(dims, q, k_pages, v_pages, page_table, seq_len, q_len, prompt_len,
+                       window, keep_mask, scale, out, lse, ws, stream=None):
+    """Several query tokens per request under the mask: q is [batch, max_q, hq,
+    head_dim] bf16; the q_len[b] query tokens of request b are its last cache
+    rows.  out [batch, max_q, hq, head_dim] f32, lse [batch, max_q, hq] f32 or None."""
+    if q.dim() != 4:
+        raise ValueError("q must be [batch, max_q, hq, head_dim]")
+    _check(_load().dsa_prefill_sparse(
+        ctypes.byref(dims), int(q.shape[1]), _ptr(q, torch.bfloat16, "q"),
+        _ptr(k_pages, torch.bfloat16, "k_pages"), _ptr(v_pages, torch.bfloat16, "v_pages"),
+        _ptr(page_table, _I32, "page_table"), _ptr(seq_len, _I32, "seq_len"),
+        _ptr(q_len, _I32, "q_len"), _ptr(prompt_len, _I32, "prompt_len"),
+        _ptr(window, _I32, "window"), _ptr(keep_mask, _MASK, "keep_mask"), float(scale),
+        _ptr(out, torch.float32, "out"), _ptr(lse, torch.float32, "lse"), _ptr(ws),
+        _stream(stream)), "dsa_prefill_sparse")
 
 
 def dsa_attention_mass(dims, q, k_pages, page_table, seq_len, prompt_len, window, grid_w,

@@ -124,6 +124,29 @@ def test_null_pointers_rejected_before_launch():
     assert lib.dsa_get_device_error(None, None, ctypes.byref(code)) == dsa.DSA_ERR_INVALID_ARG
 
 
+def test_prefill_call_checks_before_launch():
+    """dsa_prefill_sparse: host checks (no GPU): a missing q_len, a negative
+    max_q, fp32 KV or a window past 32768 are refused; max_q = 0 or an empty
+    batch is a no-op that touches nothing."""
+    lib = dsa._load()
+    fake = ctypes.c_void_p(1 << 20)
+    d = dsa.make_dims(2, 8, 2, 128, 10, 4, 96, 3, 50, "bf16", "bf16")
+    D = ctypes.byref(d)
+
+    def call(dims=D, max_q=4, q_len=fake):
+        return lib.dsa_prefill_sparse(dims, max_q, fake, fake, fake, fake, fake, q_len, fake,
+                                      fake, fake, 0.1, fake, None, fake, None)
+    assert call(q_len=None) == dsa.DSA_ERR_INVALID_ARG
+    assert call(max_q=-1) == dsa.DSA_ERR_INVALID_ARG
+    assert call(max_q=0) == dsa.DSA_OK
+    f32 = dsa.make_dims(2, 8, 2, 128, 10, 4, 96, 3, 50, "bf16", "f32")
+    assert call(dims=ctypes.byref(f32)) == dsa.DSA_ERR_UNSUPPORTED
+    wide = dsa.make_dims(2, 8, 2, 128, 10, 4, 32769, 1025, 50, "bf16", "bf16")
+    assert call(dims=ctypes.byref(wide)) == dsa.DSA_ERR_UNSUPPORTED
+    empty = dsa.make_dims(0, 8, 2, 128, 10, 4, 96, 3, 50, "bf16", "bf16")
+    assert call(dims=ctypes.byref(empty)) == dsa.DSA_OK
+
+
 def test_host_io_call_checks_before_copying():
     """dsa_decode_sparse_masked_io rejects a bad call before its upload: no io,
     an io copy without its buffers, or bad decode arguments (the fake pointers

@@ -1,0 +1,176 @@
+"""Parity of dsa_prefill_sparse (several query tokens per request under the
+mask) with the fp64 CPU oracle, through the C ABI.
+
+Bars as for decode (bf16 q/KV, fp32 accumulation): max |gpu - oracle| <= 2e-2,
+mean <= 2e-3 over every written element; lse max <= 1e-4.  Slots past q_len
+must be left untouched.  Rows that no query of the chunk keeps are never read:
+NaN / huge values there change nothing, bit for bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from kv_cache_serving_gb300 import dsa
+from kv_cache_serving_gb300 import workloads as wl
+from kv_cache_serving_gb300.session import DecodeBatch
+
+pytestmark = pytest.mark.gpu
+
+BF16_MAX, BF16_MEAN, LSE_MAX = 2e-2, 2e-3, 1e-4
+SENTINEL = -12345.0
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    assert torch.cuda.is_available(), "GPU tests need CUDA"
+    torch.cuda.init()
+
+
+def chunk_inputs(w, qmax, seed, q_len=None):
+    """q [B, qmax, Hq, D] bf16 and q_len [B] (ragged, at most min(L, qmax))."""
+    rng = np.random.default_rng(seed)
+    B, Hq, D = w["batch"], w["hq"], w["head_dim"]
+    L = w["seq_len"]
+    if q_len is None:
+        q_len = np.array([int(rng.integers(0, min(qmax, int(L[b])) + 1)) for b in range(B)],
+                         np.int32)
+        q_len[0] = min(qmax, int(L[0]))
+    q = torch.randn(B, qmax, Hq, D, generator=torch.Generator().manual_seed(seed)).to(
+        torch.bfloat16)
+    return q, np.asarray(q_len, np.int32)
+
+
+def run_prefill(bt, q, q_len, check_error=True):
+    dev = bt.device
+    out = torch.full(tuple(q.shape), SENTINEL, dtype=torch.float32, device=dev)
+    lse = torch.full(tuple(q.shape[:3]), SENTINEL, dtype=torch.float32, device=dev)
+    ql = torch.as_tensor(q_len).to(dev)
+    dsa.dsa_prefill_sparse(bt.dims, q.to(dev), bt.k_pages, bt.v_pages, bt.page_table, bt.seq_len,
+                           ql, bt.prompt_len, bt.window, bt.keep_mask, bt.scale, out, lse, bt.ws)
+    torch.cuda.synchronize()
+    if check_error:
+        assert bt.device_error() == 0
+    return out.cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
+
+
+def compare(w, q, q_len, out, lse, mask=None):
+    inp = dict(w, q=q)
+    if mask is not None:
+        inp["keep_mask"] = mask
+    ref, ref_lse = oracle.multi(inp, q_len)
+    B = w["batch"]
+    for b in range(B):
+        n = int(q_len[b])
+        assert (out[b, n:] == SENTINEL).all() and (lse[b, n:] == SENTINEL).all(), b
+    written = ~np.isnan(ref)
+    assert np.isfinite(out[written]).all()
+    err = np.abs(out[written] - ref[written])
+    if err.size:
+        assert err.max() <= BF16_MAX, err.max()
+        assert err.mean() <= BF16_MEAN, err.mean()
+    lw = ~np.isnan(ref_lse)
+    if lw.any():
+        assert np.abs(lse[lw] - ref_lse[lw]).max() <= LSE_MAX
+    return ref, ref_lse
+
+
+def small_cfg(D, G, batch=5, hkv=2, Lmax=400, Pmax=100, W=64, seed=0):
+    return wl.Config(f"mq-{D}-{G}", batch, hkv * G, hkv, D, "bf16", (0, Pmax), (8,), None, W,
+                     ("abs", 1, Lmax), "random", band=2, seed=seed)
+
+
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+@pytest.mark.parametrize("D", [64, 128])
+def test_prefill_small_every_build(D, G):
+    """Every (head_dim, group): ragged q_len spanning several query tiles and
+    row blocks, prompt-only and window queries, shuffled pages."""
+    w = wl.generate(small_cfg(D, G, seed=10 * D + G), spare_pages=3)
+    bt = DecodeBatch.from_workload(w)
+    qmax = 2 * dsa_queries_per_cta(G) + 5
+    q, ql = chunk_inputs(w, qmax, seed=D + G)
+    out, lse = run_prefill(bt, q, ql)
+    compare(w, q, ql, out, lse)
+
+
+def dsa_queries_per_cta(G):
+    return 64 // G
+
+
+@pytest.mark.parametrize("name,batch,qmax", [("janus-pro-7b", 6, 64), ("llamagen-xl", 8, 24),
+                                             ("emu3-8b", 2, 40), ("mixed-serving", 6, 48)])
+def test_prefill_workload_shapes(name, batch, qmax):
+    w = wl.generate(wl.scaled(wl.WORKLOADS[name], batch=batch))
+    mask = None
+    if w["keep_mask"] is None:
+        _, om = oracle.mass(w, r_local=2, r_diag=2)
+        mask = wl.top_mass_keep_mask(om.reshape(w["batch"], w["hq"], -1), w["window"], w["hkv"],
+                                     w["mask_words"], band=w["config"].band,
+                                     frac=w["config"].top_mass_frac)
+    bt = DecodeBatch.from_workload(w, keep_mask=mask)
+    q, ql = chunk_inputs(w, qmax, seed=batch)
+    out, lse = run_prefill(bt, q, ql)
+    compare(w, q, ql, out, lse, mask)
+
+
+def test_prefill_whole_sequences_and_edges():
+    """q_len = L (every row a query, prompt queries included), q_len = 0, a
+    window of 0, an empty mask and an all-ones mask in one batch."""
+    cfg = small_cfg(128, 4, batch=6, Lmax=150, Pmax=40, W=64, seed=5)
+    w = wl.generate(cfg)
+    L = w["seq_len"]
+    w["window"][1] = 0
+    w["keep_mask"][2] = 0
+    w["keep_mask"][3] = 0xFFFFFFFF
+    qmax = int(L.max())
+    ql = np.array([int(L[0]), 0, int(L[2]), min(int(L[3]), 17), 1, int(L[5])], np.int32)
+    bt = DecodeBatch.from_workload(w)
+    q, ql = chunk_inputs(w, qmax, seed=6, q_len=ql)
+    out, lse = run_prefill(bt, q, ql)
+    compare(w, q, ql, out, lse)
+
+
+def test_prefill_single_query_is_a_decode_step():
+    """q_len = 1 is a decode step: within the bars of the decode oracle."""
+    w = wl.generate(wl.scaled(wl.WORKLOADS["janus-pro-7b"], batch=4))
+    bt = DecodeBatch.from_workload(w)
+    q4 = w["q"].view(w["batch"], 1, w["hq"], w["head_dim"]).contiguous()
+    ql = np.ones(w["batch"], np.int32)
+    out, lse = run_prefill(bt, q4, ql)
+    ref, ref_lse = oracle.decode(w, sparse=True)
+    err = np.abs(out.reshape(ref.shape) - ref)
+    assert err.max() <= BF16_MAX and err.mean() <= BF16_MEAN
+    assert np.abs(lse.reshape(-1) - ref_lse).max() <= LSE_MAX
+
+
+def test_prefill_skipped_rows_are_never_read():
+    w = wl.generate(wl.scaled(wl.WORKLOADS["janus-pro-7b"], batch=4), spare_pages=5)
+    q, ql = chunk_inputs(w, 40, seed=9)
+    bt = DecodeBatch.from_workload(w)
+    base, lbase = run_prefill(bt, q, ql)
+
+    def kept(b, hk):
+        L, P, W = (int(w[k][b]) for k in ("seq_len", "prompt_len", "window"))
+        rows = set()
+        for t in range(int(ql[b])):
+            rows.update(oracle.kept_set(L - int(ql[b]) + t + 1, P, W,
+                                        w["keep_mask"][b, hk]).tolist())
+        return sorted(rows)
+
+    for value in (float("nan"), 1e30):
+        p = wl.poison_unread(w, kept, value)
+        bt2 = DecodeBatch.from_workload(p)
+        out, lse = run_prefill(bt2, q, ql)
+        assert np.array_equal(out, base) and np.array_equal(lse, lbase)
+
+
+def test_prefill_invalid_q_len_is_flagged():
+    w = wl.generate(wl.scaled(wl.WORKLOADS["llamagen-xl"], batch=3))
+    bt = DecodeBatch.from_workload(w)
+    q, ql = chunk_inputs(w, 8, seed=3)
+    ql = ql.copy()
+    ql[1] = int(w["seq_len"][1]) + 1          # more queries than rows
+    out, lse = run_prefill(bt, q, ql, check_error=False)
+    assert bt.device_error() == 11            # DSA_DEV_BAD_QLEN
+    assert np.isnan(out[1]).all() and np.isnan(lse[1]).all()
+    dsa.dsa_clear_device_error(bt.ws)
