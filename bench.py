@@ -106,7 +106,7 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--busy-seconds", type=float, default=1.5,
                    help="GPU busy time around the timed region for clock sampling")
-    p.add_argument("--profile", choices=["index", "sparse", "masked", "dense", "mass"],
+    p.add_argument("--profile", choices=["index", "sparse", "masked", "dense", "mass", "prefill"],
                    help="no timing: run W + K eager launches of one call on one KV pool "
                         "(a small, self-contained case for ncu) and exit")
     p.add_argument("--sparse-cluster", type=int, default=-1,
@@ -393,6 +393,149 @@ def measure_compact(name, K, W, device, stream, peak):
     return res
 
 
+def prefill_inputs(w, q_len, device):
+    """q [B, Q, Hq, D] bf16 (seeded) and the device q_len for a chunk of the
+    last q_len rows of every request."""
+    B, Hq, D = w["batch"], w["hq"], w["head_dim"]
+    gen = torch.Generator(device=device).manual_seed(w["seed"] + 77)
+    q = torch.randn((B, q_len, Hq, D), generator=gen, device=device,
+                    dtype=torch.float32).to(torch.bfloat16)
+    ql = torch.full((B,), q_len, dtype=torch.int32, device=device)
+    return q, ql
+
+
+def prefill_bytes(w, q_len, dense=False):
+    """Algorithmic bytes of one chunk: the union over the chunk's queries of their
+    kept rows (each read once per (request, kv head)), q, out and lse; and the
+    flops of the kept (query, row) pairs."""
+    import itertools
+    B, Hq, Hkv, D = w["batch"], w["hq"], w["hkv"], w["head_dim"]
+    g = Hq // Hkv
+    rows = pairs = 0
+    for b, hk in itertools.product(range(B), range(Hkv)):
+        L, P, W = (int(w[k][b]) for k in ("seq_len", "prompt_len", "window"))
+        n = min(q_len, L)
+        if dense:
+            rows += L
+            pairs += sum(L - n + t + 1 for t in range(n))
+            continue
+        bits = w["keep_mask"][b, hk]
+        offs = [o for o in range(1, W + 1) if (int(bits[(o - 1) >> 5]) >> ((o - 1) & 31)) & 1]
+        union = set()
+        for t in range(n):
+            i = L - n + t
+            kept = set(range(min(P, i + 1))) | {i} | {i - o for o in offs if i - o >= P}
+            pairs += len(kept)
+            union |= kept
+        rows += len(union)
+    qb = B * q_len * Hq * D * 2
+    ob = B * q_len * Hq * (D + 1) * 4
+    return rows * 2 * D * 2 + qb + ob, 4 * D * pairs * g
+
+
+def measure_prefill(name, q_len, K, W, device, stream, peak):
+    """dsa_prefill_sparse on one workload, the last q_len rows of every request
+    as the query chunk, against the same kernel with every row kept (dense
+    causal), each a K-step CUDA graph over rotating KV copies."""
+    cfg = wl.WORKLOADS[name]
+    w = wl.generate(cfg, device=str(device))
+    bt = DecodeBatch.from_workload(w, device=device)
+    q, ql = prefill_inputs(w, q_len, device)
+    out = torch.empty(tuple(q.shape), dtype=torch.float32, device=device)
+    lse = torch.empty(tuple(q.shape[:3]), dtype=torch.float32, device=device)
+    by, flops = prefill_bytes(w, q_len)
+    by_d, flops_d = prefill_bytes(w, q_len, dense=True)
+    pools, _ = kv_replicas(bt, by, device)
+    R = len(pools)
+    # dense causal: every earlier row kept (window past every length, all bits set)
+    Lmax = int(w["seq_len"].max())
+    words = wl.mask_words_for(Lmax)
+    dd = dsa.make_dims(w["batch"], w["hq"], w["hkv"], w["head_dim"], w["num_pages"],
+                       w["max_pages"], Lmax, words, w["max_kept"], "bf16", "bf16")
+    win_d = torch.as_tensor(w["seq_len"]).to(device)
+    mask_d = torch.full((w["batch"], w["hkv"], words), -1, dtype=torch.int32, device=device)
+    ws_d = dsa.alloc_workspace(dd, device)
+
+    def sparse(k):
+        kp, vp = pools[k % R]
+        dsa.dsa_prefill_sparse(bt.dims, q, kp, vp, bt.page_table, bt.seq_len, ql, bt.prompt_len,
+                               bt.window, bt.keep_mask, bt.scale, out, lse, bt.ws, stream)
+
+    def dense(k):
+        kp, vp = pools[k % R]
+        dsa.dsa_prefill_sparse(dd, q, kp, vp, bt.page_table, bt.seq_len, ql, bt.prompt_len,
+                               win_d, mask_d, bt.scale, out, lse, ws_d, stream)
+
+    for k in range(W):
+        sparse(k)
+        dense(k)
+    torch.cuda.synchronize()
+    bt.check("prefill warm-up")
+    dsa.check_device_error(ws_d, "prefill warm-up (dense)")
+    gs, gd = graph_of(sparse, K, stream), graph_of(dense, K, stream)
+    gs.replay()
+    gd.replay()
+    torch.cuda.synchronize()
+    ts, td = time_graph(gs, stream) / K, time_graph(gd, stream) / K
+    bt.check("prefill timed")
+    res = {
+        "call": "dsa_prefill_sparse: the last q_len rows of every request as query tokens, "
+                "each over its own kept set",
+        "workload": cfg.name, "batch": w["batch"], "q_len": q_len,
+        "us": 1e6 * ts, "query_tokens_per_s": w["batch"] * q_len / ts,
+        "bytes": by, "gbs": by / ts / 1e9, "frac_hbm": by / ts / 1e9 / peak,
+        "tflops": flops / ts / 1e12,
+        "dense_causal_us": 1e6 * td, "dense_gbs": by_d / td / 1e9,
+        "speedup": td / ts, "kv_copies": R,
+    }
+    del gs, gd, pools, bt, w
+    torch.cuda.empty_cache()
+    return res
+
+
+def measure_evicted_batch(cfg, batch_after, K, device, stream, peak):
+    """The memory side of the mask: after eviction a request keeps only its
+    prompt, its window and a partial page resident, so the KV pool that held
+    the batch before eviction holds batch_after requests.  Draw a batch of
+    that size, evict its pages, and time the fused step on it (CUDA graph,
+    K steps)."""
+    w = wl.generate(wl.scaled(cfg, batch=batch_after), device=str(device))
+    bt = DecodeBatch.from_workload(w, device=device)
+    if cfg.mask == "top_mass":
+        _, om = bt.attention_mass(r_local=2, r_diag=2)
+        bt.set_keep_mask(wl.top_mass_keep_mask(om.cpu().numpy(), w["window"], w["hkv"],
+                                               w["mask_words"], band=cfg.band,
+                                               frac=cfg.top_mass_frac))
+    _, nfree = bt.evict_pages()
+    order = bt.schedule_order()
+    order = None if order is None else torch.as_tensor(order).to(device)
+    mapped = int((w["page_table"] >= 0).sum())
+
+    def fused(k):
+        bt.decode_sparse_masked(request_order=order, stream=stream)
+
+    for k in range(3):
+        fused(k)
+    torch.cuda.synchronize()
+    bt.check("evicted batch")
+    g = graph_of(fused, K, stream)
+    g.replay()
+    torch.cuda.synchronize()
+    t = time_graph(g, stream) / K
+    bt.check("evicted batch timed")
+    page_bytes = 16 * w["hkv"] * w["head_dim"] * 2 * 2
+    res = {"batch_after": batch_after, "step_us_after": 1e6 * t,
+           "tokens_per_s_after": batch_after / t,
+           "resident_kv_bytes_at_batch_after": (mapped - int(nfree.item())) * page_bytes,
+           "note": "the same steady-state KV pool (the batch's pages before eviction) holds "
+                   "batch_after requests once pages no later step reads are evicted; the "
+                   "step is timed on that batch after its own eviction (one KV copy, its "
+                   "kept rows exceed 4x L2)"}
+    del g, bt, w
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args):
     if args.sparse_cluster >= 0:
         dsa.dsa_set_sparse_cluster(args.sparse_cluster)
@@ -411,6 +554,10 @@ def run_ours(args):
             if name not in (args.workload, "tiny-fp32"):
                 others.append(measure_compact(name, max(10, min(args.steps, 50)),
                                               max(3, min(args.warmup, 5)), device, stream, peak))
+    prefill = None
+    if world == 1 and not args.no_other_workloads:
+        prefill = measure_prefill("janus-pro-7b", 32, max(10, min(args.steps, 50)),
+                                  max(3, min(args.warmup, 5)), device, stream, peak)
     cfg = wl.WORKLOADS[args.workload]
     w = wl.generate(cfg, seed=rank_seed(cfg, rank), device=str(device))
     bt = DecodeBatch.from_workload(w, device=device)
@@ -629,6 +776,12 @@ def run_ours(args):
                 "resident_kv_bytes_before": mapped * page_bytes,
                 "resident_kv_bytes_after": (mapped - evicted) * page_bytes,
                 "evict_us": 1e3 * e0.elapsed_time(e1)}
+    if world == 1 and not args.no_other_workloads and w["dtype"] == "bf16" and evicted > 0:
+        # requests of this workload that the same pool holds once evicted pages are reused
+        batch_after = min(int(w["batch"] * mapped / max(mapped - evicted, 1)), 16 * w["batch"])
+        eviction.update(measure_evicted_batch(cfg, batch_after, max(10, min(K, 50)), device,
+                                              stream, peak))
+        eviction["tokens_per_s_before"] = world * w["batch"] / (t_step / K)
 
     # attention mass: every K row of every request (no V), q, the bins and the
     # per-offset weights (written as raw scores, then normalised by the merge)
@@ -743,6 +896,8 @@ def run_ours(args):
     }
     if others:
         result["workloads"] = others
+    if prefill is not None:
+        result["prefill"] = prefill
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         w_cpu = to_cpu_workload(w, bt)
@@ -830,7 +985,14 @@ def run_profile(args):
     bt.build_index()
     order = bt.schedule_order()
     order = None if order is None else torch.as_tensor(order).to(device)
-    call = {"index": bt.build_index, "sparse": bt.decode_sparse,
+    q4, ql = prefill_inputs(w, 32, device)
+    o4 = torch.empty(tuple(q4.shape), dtype=torch.float32, device=device)
+    l4 = torch.empty(tuple(q4.shape[:3]), dtype=torch.float32, device=device)
+
+    def prefill_call():
+        dsa.dsa_prefill_sparse(bt.dims, q4, bt.k_pages, bt.v_pages, bt.page_table, bt.seq_len, ql,
+                               bt.prompt_len, bt.window, bt.keep_mask, bt.scale, o4, l4, bt.ws)
+    call = {"prefill": prefill_call, "index": bt.build_index, "sparse": bt.decode_sparse,
             "masked": lambda: bt.decode_sparse_masked(request_order=order),
             "dense": bt.decode_dense,
             "mass": lambda: bt.attention_mass(r_local=2, r_diag=2)}[args.profile]

@@ -135,6 +135,11 @@ size_t dsa_workspace_size(const dsa_dims* dims);
  *   kept_idx  (out)              [batch][hkv][max_kept] int32 (device)
  *   kept_cnt  (out)              [batch][hkv] int32 (device)
  * A count above max_kept sets DSA_DEV_BAD_COUNT and stores count 0.
+ * For batches of at most 1024 requests the call also leaves in `ws` a request
+ * schedule -- the requests by decreasing total kept rows, ties by index --
+ * tagged with the batch size; dsa_decode_sparse on the same workspace hands
+ * its requests to the GPU in that order (long requests first, so they do not
+ * form the tail of the launch).  Results never depend on it.
  */
 dsa_status dsa_build_index(const dsa_dims* dims, const int32_t* seq_len,
                            const int32_t* prompt_len, const int32_t* window,
@@ -155,6 +160,8 @@ dsa_status dsa_build_index(const dsa_dims* dims, const int32_t* seq_len,
  *   scale             softmax scale, normally 1/sqrt(head_dim)
  *   out   (out)       [batch][hq][head_dim] float32
  *   lse   (out)       [batch][hq] float32, or NULL
+ * Requests are scheduled in the order dsa_build_index left in `ws` when it was
+ * written for this batch size, else in batch order (same results either way).
  */
 dsa_status dsa_decode_sparse(const dsa_dims* dims, const void* q, const void* k_pages,
                              const void* v_pages, const int32_t* page_table,

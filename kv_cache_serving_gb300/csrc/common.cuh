@@ -21,8 +21,16 @@ constexpr uint64_t kWaitLimitNs = 500ull * 1000 * 1000;  // give up on a copy af
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-// Workspace: [0, 256) header (error word at offset 0), then per-call partials.
+// Workspace: [0, 256) header, then per-call regions.  Header words: 0 the
+// device error word; 1 the tag of the request schedule dsa_build_index leaves
+// for dsa_decode_sparse (kSchedMagic ^ batch when valid); 2 the count of
+// index-compaction CTAs done (the last one writes the schedule, then resets it).
 constexpr size_t kWsHeader = 256;
+constexpr int kWsSchedTag = 1;
+constexpr int kWsDoneCount = 2;
+constexpr int32_t kSchedMagic = 0x5c4ed000;
+// Largest batch whose schedule the index compaction sorts (one CTA, rank sort).
+constexpr int kSchedMaxBatch = 1024;
 
 __device__ __forceinline__ void set_error(int32_t* err, int32_t code) {
   atomicCAS(err, 0, code);

@@ -9,7 +9,8 @@
 // reports attention concentrates on.
 //
 // One warp per (b, hk).  Prompt rows are written as a plain range, window rows
-// by window_rows() (ballot + popcount prefix, sorted with no sort).
+// by window_rows() (ballot + popcount prefix, sorted with no sort).  The last
+// CTA also leaves a request schedule in the workspace for the decode.
 #include "common.cuh"
 #include "internal.h"
 
@@ -41,40 +42,73 @@ __device__ __forceinline__ int window_rows(const uint32_t* mask, int i, int np, 
   return n;
 }
 
+// One warp per (request, kv head); the last CTA to finish also writes the
+// request schedule: requests by decreasing total kept rows (ties by index),
+// the order in which dsa_decode_sparse hands them to the GPU so that long
+// requests do not end up in the tail of the launch.
 __global__ void __launch_bounds__(256) compact_kernel(const CompactLaunch a) {
   griddep_wait();
   griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (gw >= a.batch * a.hkv) return;
-  const int b = gw / a.hkv;
-  const int L = a.seq_len[b], P = a.prompt_len[b], W = a.window[b];
-  int code = 0;
-  if (L < 1 || L > a.max_pages * kPage) code = DSA_DEV_BAD_SEQ_LEN;
-  else if (P < 0) code = DSA_DEV_BAD_PROMPT;
-  else if (W < 0 || W > a.max_window) code = DSA_DEV_BAD_WINDOW;
-  if (code != 0) {
-    if (lane == 0) {
-      set_error(a.err, code);
-      a.kept_cnt[gw] = 0;
+  if (gw < a.batch * a.hkv) {
+    const int b = gw / a.hkv;
+    const int L = a.seq_len[b], P = a.prompt_len[b], W = a.window[b];
+    int code = 0;
+    if (L < 1 || L > a.max_pages * kPage) code = DSA_DEV_BAD_SEQ_LEN;
+    else if (P < 0) code = DSA_DEV_BAD_PROMPT;
+    else if (W < 0 || W > a.max_window) code = DSA_DEV_BAD_WINDOW;
+    if (code != 0) {
+      if (lane == 0) {
+        set_error(a.err, code);
+        a.kept_cnt[gw] = 0;
+      }
+    } else {
+      const int i = L - 1;
+      const int np = min(P, L);
+      int32_t* out = a.kept_idx + static_cast<size_t>(gw) * a.max_kept;
+      const uint32_t* mask = a.keep_mask + static_cast<size_t>(gw) * a.mask_words;
+      const int cap = a.max_kept;
+      for (int j = lane; j < np && j < cap; j += 32) out[j] = j;
+      const int n_win = window_rows(mask, i, np, W, lane, out + min(np, cap), max(0, cap - np));
+      int n = np + n_win;
+      if (lane == 0) {
+        if (n > cap) {
+          set_error(a.err, DSA_DEV_BAD_COUNT);
+          n = 0;
+        }
+        a.kept_cnt[gw] = n;
+      }
     }
-    return;
   }
-  const int i = L - 1;
-  const int np = min(P, L);
-  int32_t* out = a.kept_idx + static_cast<size_t>(gw) * a.max_kept;
-  const uint32_t* mask = a.keep_mask + static_cast<size_t>(gw) * a.mask_words;
-  const int cap = a.max_kept;
-
-  for (int j = lane; j < np && j < cap; j += 32) out[j] = j;
-  const int n_win = window_rows(mask, i, np, W, lane, out + min(np, cap), max(0, cap - np));
-  int n = np + n_win;
-  if (lane == 0) {
-    if (n > cap) {
-      set_error(a.err, DSA_DEV_BAD_COUNT);
-      n = 0;
-    }
-    a.kept_cnt[gw] = n;
+  if (a.sched == nullptr || a.batch > kSchedMaxBatch) return;
+  // last CTA done: every CTA's counts are visible to it (fence, then count)
+  __shared__ int last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) last = atomicAdd(a.done_count, 1) == static_cast<int>(gridDim.x) - 1;
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  __shared__ int est[kSchedMaxBatch];
+  for (int b = threadIdx.x; b < a.batch; b += blockDim.x) {
+    int sum = 0;
+    for (int hk = 0; hk < a.hkv; ++hk) sum += __ldcg(a.kept_cnt + static_cast<size_t>(b) * a.hkv + hk);
+    est[b] = sum;
+  }
+  __syncthreads();
+  // rank of request b: requests with more rows, or as many and a smaller index
+  for (int b = threadIdx.x; b < a.batch; b += blockDim.x) {
+    const int e = est[b];
+    int rank = 0;
+    for (int c = 0; c < a.batch; ++c) rank += (est[c] > e) || (est[c] == e && c < b);
+    a.sched[rank] = b;
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    *a.sched_tag = kSchedMagic ^ a.batch;
+    *a.done_count = 0;
   }
 }
 

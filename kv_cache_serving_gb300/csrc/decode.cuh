@@ -33,7 +33,8 @@
 //
 // Builds (warps per CTA, stage bytes, stages) are template parameters: the
 // default one, and for the sparse calls with bf16 KV a big-batch build (more
-// warps per SM) and a small-batch build (one wave of CTAs); the host plan
+// warps per SM), a small-batch build (one wave of CTAs) and a wide build (one
+// 8-warp CTA per unit for batches of at most one unit per SM); the host plan
 // picks one per call.
 #pragma once
 
@@ -62,6 +63,9 @@ namespace dsa {
 #ifndef DSA_DECODE_WARPS_SMALL
 #define DSA_DECODE_WARPS_SMALL 5
 #endif
+#ifndef DSA_DECODE_WARPS_WIDE
+#define DSA_DECODE_WARPS_WIDE 8
+#endif
 #ifndef DSA_DECODE_STAGE_BYTES_DENSE
 #define DSA_DECODE_STAGE_BYTES_DENSE 4096  // dense rows: long, split into many chunks
 #endif
@@ -77,7 +81,7 @@ namespace dsa {
 // Cluster launches (sparse decode split over a thread-block cluster) are also
 // programmatic dependents when set.
 #ifndef DSA_PDL_CLUSTER
-#define DSA_PDL_CLUSTER 0
+#define DSA_PDL_CLUSTER 1
 #endif
 
 template <int D, typename KV, int G, bool MMA = false, int NWARPS = DSA_DECODE_WARPS,
@@ -195,7 +199,12 @@ __global__ void __launch_bounds__(NWARPS * 32,
   griddep_launch_dependents();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int c = blockIdx.x, hk = blockIdx.y;
-  const int b = a.order != nullptr ? __ldg(a.order + blockIdx.z) : static_cast<int>(blockIdx.z);
+  int b = a.order != nullptr ? __ldg(a.order + blockIdx.z) : static_cast<int>(blockIdx.z);
+  if (MODE == kRowsList && a.sched != nullptr) {
+    // the schedule dsa_build_index left, when it was written for this batch size
+    const int tag = a.sched_tag[0], sb = a.sched[blockIdx.z];
+    if (tag == a.sched_expect) b = sb;
+  }
   if (static_cast<unsigned>(b) >= static_cast<unsigned>(a.batch)) {
     if (c == 0 && hk == 0 && threadIdx.x == 0) set_error(a.err, DSA_DEV_BAD_ORDER);
     return;
@@ -714,17 +723,19 @@ template <int G, bool QMIX, int BUILD>
 constexpr int build_warps() {
   return BUILD == kBuildBig
              ? ((QMIX && G >= 2) ? DSA_DECODE_WARPS_BIG_MMA : DSA_DECODE_WARPS_BIG)
-             : (BUILD == kBuildSmall ? DSA_DECODE_WARPS_SMALL : DSA_DECODE_WARPS);
+             : (BUILD == kBuildSmall  ? DSA_DECODE_WARPS_SMALL
+                : BUILD == kBuildWide ? DSA_DECODE_WARPS_WIDE
+                                      : DSA_DECODE_WARPS);
 }
 template <int MODE, int BUILD>
 constexpr int build_stage_bytes() {
-  return BUILD == kBuildBig     ? DSA_DECODE_STAGE_BYTES_BIG
-         : BUILD == kBuildSmall ? DSA_DECODE_STAGE_BYTES
-                                : default_stage_bytes(MODE);
+  return BUILD == kBuildBig                             ? DSA_DECODE_STAGE_BYTES_BIG
+         : (BUILD == kBuildSmall || BUILD == kBuildWide) ? DSA_DECODE_STAGE_BYTES
+                                                         : default_stage_bytes(MODE);
 }
 template <int BUILD>
 constexpr int build_stages() {
-  return BUILD == kBuildSmall ? 1 : DSA_DECODE_STAGES;
+  return (BUILD == kBuildSmall || BUILD == kBuildWide) ? 1 : DSA_DECODE_STAGES;
 }
 
 template <typename KV, int MODE, int BUILD>
@@ -749,6 +760,8 @@ cudaError_t launch_decode_mode(const DecodeLaunch& a, cudaStream_t s) {
     if (a.build == kBuildBig) return launch_decode_dispatch<KV, MODE, kBuildBig>(a, s);
   if constexpr (has_build<KV>(MODE, kBuildSmall))
     if (a.build == kBuildSmall) return launch_decode_dispatch<KV, MODE, kBuildSmall>(a, s);
+  if constexpr (has_build<KV>(MODE, kBuildWide))
+    if (a.build == kBuildWide) return launch_decode_dispatch<KV, MODE, kBuildWide>(a, s);
   return launch_decode_dispatch<KV, MODE, kBuildDefault>(a, s);
 }
 
@@ -784,6 +797,8 @@ DecodeShape decode_shape_mode(int head_dim, int group, int build) {
     if (build == kBuildBig) return decode_shape_m<KV, MODE, kBuildBig>(head_dim, group);
   if constexpr (has_build<KV>(MODE, kBuildSmall))
     if (build == kBuildSmall) return decode_shape_m<KV, MODE, kBuildSmall>(head_dim, group);
+  if constexpr (has_build<KV>(MODE, kBuildWide))
+    if (build == kBuildWide) return decode_shape_m<KV, MODE, kBuildWide>(head_dim, group);
   return decode_shape_m<KV, MODE, kBuildDefault>(head_dim, group);
 }
 

@@ -153,6 +153,18 @@ size_t unit_ints_region(const dsa_dims* d) {
   return round_up(static_cast<size_t>(d->batch) * d->hkv * sizeof(int32_t), 256);
 }
 
+// [batch] request schedule dsa_build_index leaves for dsa_decode_sparse, after
+// the kept counts of the fused call.
+int32_t* sched_region(const dsa_dims* d, void* ws) {
+  return reinterpret_cast<int32_t*>(reinterpret_cast<unsigned char*>(ws) + kWsHeader +
+                                    partials_region(d) + unit_ints_region(d));
+}
+
+size_t sched_bytes(const dsa_dims* d) {
+  return round_up(static_cast<size_t>(d->batch) * sizeof(int32_t), 256);
+}
+
+
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 struct Plan {
@@ -176,9 +188,32 @@ DecodeShape decode_shape(const dsa_dims* d, int mode, int build) {
                                  : decode_shape_f32(d->head_dim, g, mode, build);
 }
 
+// The wide build takes a unit in one CTA when its kept rows need at most this
+// many passes of the CTA's warps.
+constexpr int kWideMaxPasses = 4;
+
 Plan decode_plan(const dsa_dims* d, int mode) {
   const int64_t n_max = mode == kModeDense ? dense_rows(d) : d->max_kept;
   const int64_t units = static_cast<int64_t>(d->batch) * d->hkv;
+  const int setting = g_sparse_cluster.load(std::memory_order_relaxed);
+  if (mode != kModeDense && setting == 0 && units <= sm_count()) {
+    // at most one unit per SM: each unit in one 8-warp CTA (rows spread over its
+    // warps, merged in shared memory), no cluster and no merge launch
+    const DecodeShape wide = decode_shape(d, mode, kBuildWide);
+    if (wide.build == kBuildWide &&
+        n_max <= static_cast<int64_t>(kWideMaxPasses) * wide.rows_per_pass) {
+      Plan p{};
+      p.quantum = wide.rows_per_pass;
+      p.per_sm = wide.ctas_per_sm;
+      p.warps = wide.warps;
+      p.tile_rows = wide.tile_rows;
+      p.build = kBuildWide;
+      p.cluster = 1;
+      p.num_chunks = 1;
+      p.chunk = static_cast<int>(ceil_div(n_max, p.quantum) * p.quantum);
+      return p;
+    }
+  }
   DecodeShape sh = decode_shape(d, mode, kBuildDefault);
   const int64_t slots = static_cast<int64_t>(sm_count()) * sh.ctas_per_sm;
   if (mode != kModeDense && units > 2 * slots) {
@@ -200,7 +235,7 @@ Plan decode_plan(const dsa_dims* d, int mode) {
   p.tile_rows = sh.tile_rows;
   p.build = sh.build;
   p.cluster = 1;
-  int ncl = g_sparse_cluster.load(std::memory_order_relaxed);
+  int ncl = setting;
   if (ncl == 0) ncl = sparse_cluster_auto(units, sm_count() * p.per_sm);
   while (ncl > sh.cluster_limit) ncl /= 2;
   if (mode != kModeDense && ncl > 1 && n_max > p.quantum) {
@@ -227,6 +262,7 @@ struct RowSource {
   const int32_t* order = nullptr;
   const void* k_new = nullptr;
   const void* v_new = nullptr;
+  bool use_sched = false;  // kModeList: the schedule dsa_build_index left in ws
 };
 
 dsa_status decode_launch(const dsa_dims* d, int mode, const Plan& plan, const void* q,
@@ -294,6 +330,11 @@ dsa_status decode_launch(const dsa_dims* d, int mode, const Plan& plan, const vo
   a.keep_mask = rs.keep_mask;
   a.unit_rows = mode == kModeMask ? unit_rows(d, ws) : nullptr;
   a.order = rs.order;
+  if (rs.use_sched) {
+    a.sched = sched_region(d, ws);
+    a.sched_tag = err_word(ws) + kWsSchedTag;
+    a.sched_expect = kSchedMagic ^ d->batch;
+  }
   a.k_new = rs.k_new;
   a.v_new = rs.v_new;
   a.max_window = d->max_window;
@@ -345,7 +386,7 @@ const char* dsa_status_string(dsa_status status) {
 
 size_t dsa_workspace_size(const dsa_dims* dims) {
   if (check_dims(dims) != DSA_OK) return 0;
-  return kWsHeader + partials_region(dims) + unit_ints_region(dims);
+  return kWsHeader + partials_region(dims) + unit_ints_region(dims) + sched_bytes(dims);
 }
 
 dsa_status dsa_build_index(const dsa_dims* dims, const int32_t* seq_len,
@@ -371,6 +412,9 @@ dsa_status dsa_build_index(const dsa_dims* dims, const int32_t* seq_len,
   a.mask_words = dims->mask_words;
   a.max_kept = dims->max_kept;
   a.err = err_word(ws);
+  a.sched = sched_region(dims, ws);
+  a.sched_tag = err_word(ws) + kWsSchedTag;
+  a.done_count = err_word(ws) + kWsDoneCount;
   return from_cuda(launch_compact(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -407,6 +451,7 @@ dsa_status dsa_decode_sparse(const dsa_dims* dims, const void* q, const void* k_
   RowSource rs;
   rs.kept_idx = kept_idx;
   rs.kept_cnt = kept_cnt;
+  rs.use_sched = true;
   return decode_common(dims, kModeList, q, k_pages, v_pages, page_table, seq_len, rs, scale, out,
                        lse, ws, stream);
 }
@@ -543,7 +588,8 @@ dsa_status dsa_prefill_sparse(const dsa_dims* dims, int32_t max_q, const void* q
   a.max_window = dims->max_window;
   a.mask_words = dims->mask_words;
   a.max_q = max_q;
-  const int per_cta = multi_queries_per_cta(dims->hq / dims->hkv);
+  a.warps = multi_warps(max_q, dims->hq / dims->hkv);
+  const int per_cta = multi_queries_per_cta(a.warps, dims->hq / dims->hkv);
   a.q_tiles = static_cast<int32_t>(ceil_div(max_q, per_cta));
   a.scale_log2 = scale * kLog2e;
   a.out = out;

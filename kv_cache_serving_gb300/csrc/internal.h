@@ -29,6 +29,9 @@ struct DecodeLaunch {
   const uint32_t* keep_mask;  // kRowsMask only: [batch][hkv][mask_words]
   int32_t* unit_rows;         // kRowsMask only: [batch][hkv] kept count or -error
   const int32_t* order;       // [batch] request scheduled at each grid z, or null (z itself)
+  const int32_t* sched;       // kRowsList: [batch] schedule left by dsa_build_index, used
+  const int32_t* sched_tag;   //   when *sched_tag == sched_expect (else z itself), or null
+  int32_t sched_expect;
   const void* k_new;          // [batch][hkv][head_dim] K/V of row seq_len-1, or null (the
   const void* v_new;          //   cache already holds it); written into its page slot
   int32_t batch, hq, hkv, head_dim, max_pages, num_pages, max_kept;
@@ -72,6 +75,9 @@ struct CompactLaunch {
   int32_t* kept_cnt;
   int32_t batch, hkv, max_pages, max_window, mask_words, max_kept;
   int32_t* err;
+  int32_t* sched;       // [batch] requests by decreasing kept rows (written by the last CTA)
+  int32_t* sched_tag;   // set to kSchedMagic ^ batch once sched is written
+  int32_t* done_count;  // CTAs done; zero between calls
 };
 
 struct EvictLaunch {
@@ -98,6 +104,7 @@ struct MultiLaunch {
   const uint32_t* keep_mask;  // [batch][hkv][mask_words]
   int32_t batch, hq, hkv, head_dim, max_pages, num_pages, max_window, mask_words, max_q;
   int32_t q_tiles;            // CTAs along the query axis of one (request, kv head)
+  int32_t warps;              // warps per CTA (multi_warps)
   float scale_log2;
   float* out;                 // [batch][max_q][hq][head_dim]
   float* lse;                 // [batch][max_q][hq] or null
@@ -125,10 +132,12 @@ int mass_rows_per_pass(int head_dim, int group, bool kv_bf16, bool q_bf16);
 bool mass_uses_tensor_cores(bool kv_bf16, bool q_bf16, int group);
 int mass_ctas_per_sm(int head_dim, int group, bool kv_bf16, bool q_bf16);
 cudaError_t launch_compact(const CompactLaunch& a, cudaStream_t s);
-// Several query tokens per request: bf16 q and KV only; queries per CTA for a
-// group size (the CTA holds 64 (query, head) rows).
+// Several query tokens per request: bf16 q and KV only.  Warps per CTA for a
+// call (2 when max_q x group fits 32 (query, head) rows, else 4) and the query
+// tokens a CTA of that many warps holds.
 cudaError_t launch_multi(const MultiLaunch& a, cudaStream_t s);
-int multi_queries_per_cta(int group);
+int multi_warps(int max_q, int group);
+int multi_queries_per_cta(int warps, int group);
 // Largest max_window of the multi-query call (its mask words sit in shared memory).
 constexpr int kMultiMaxWindow = 32768;
 cudaError_t launch_evict(const EvictLaunch& a, cudaStream_t s);
@@ -138,11 +147,13 @@ cudaError_t launch_evict(const EvictLaunch& a, cudaStream_t s);
 cudaError_t copy_host_to_device(void* dev, const void* host, size_t bytes, cudaStream_t s);
 cudaError_t copy_device_to_host(void* host, const void* dev, size_t bytes, cudaStream_t s);
 
-// Builds of the decode kernel.  The sparse calls with bf16 KV have two more
+// Builds of the decode kernel.  The sparse calls with bf16 KV have three more
 // besides the default: one for batches of more than two waves of units (more
 // warps per SM), one for batches that fit one wave only with it (5 warps of a
-// single stage, each warp about one tile of a unit).
-enum : int { kBuildDefault = 0, kBuildBig = 1, kBuildSmall = 2 };
+// single stage, each warp about one tile of a unit), and one for batches of at
+// most one unit per SM (8 warps of a single stage: a unit's rows spread over
+// the warps of one CTA, merged in its shared memory, no cluster).
+enum : int { kBuildDefault = 0, kBuildBig = 1, kBuildSmall = 2, kBuildWide = 3 };
 
 // Host-side facts about one build of the decode kernel, for the chunk choice.
 struct DecodeShape {

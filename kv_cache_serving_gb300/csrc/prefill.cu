@@ -12,9 +12,10 @@
 // skipped).  The abstract also reports prefill attention to be diffuse; the
 // call serves chunks whose queries share one mask, as decode steps do.
 //
-// Work decomposition: grid (query tile, kv head, request).  A CTA holds 64
-// (query, head) rows -- 64/G consecutive query tokens times the G query heads
-// of one kv head -- and scans the union of their kept rows: the prompt rows
+// Work decomposition: grid (query tile, kv head, request).  A CTA holds 16 NW
+// (query, head) rows (NW = 2 or 4 warps, the fewest that hold max_q x G) --
+// 16 NW/G consecutive query tokens times the G query heads of one kv head --
+// and scans the union of their kept rows: the prompt rows
 // [0, min(P, i_last+1)) and the window range [max(., i_first-W), i_last].
 // This is a dense contraction (every staged K/V row meets up to 64 query rows),
 // so it runs on the tensor cores: each warp owns 16 (query, head) rows, its q
@@ -25,12 +26,13 @@
 // Staging: blocks of 32 consecutive row positions, K then V, in a ring of
 // DSA_MQ_STAGES stages shared by the CTA's warps.  Warp 0 fills a stage with one
 // bulk async copy per K row and per V row (completing on the stage's "full"
-// mbarrier with the expected byte count); every warp arrives on the stage's
-// "empty" mbarrier once its reads are done, and warp 0 refills the stage after
-// that.  A row in the scanned range that no query of the tile keeps is never
-// read: its slot is zero-filled instead, so skipped rows have no effect even
-// when they hold NaN (0 x NaN would be NaN inside the mma).  Every wait is
-// bounded (DSA_DEV_TIMEOUT).
+// mbarrier with the expected byte count), the rows' page ids held in its
+// registers; every warp arrives on the stage's "empty" mbarrier once its reads
+// are done, and warp 0 refills that stage before it computes the next block.
+// A row in the scanned range that no query of the tile keeps is never read:
+// its slot is zero-filled instead, so skipped rows have no effect even when
+// they hold NaN (0 x NaN would be NaN inside the mma).  Every wait is bounded
+// (DSA_DEV_TIMEOUT).
 #include <math.h>
 
 #include "common.cuh"
@@ -44,9 +46,8 @@
 namespace dsa {
 namespace {
 
-constexpr int kMqWarps = 4;               // warps per CTA
-constexpr int kMqRows = 16 * kMqWarps;    // (query, head) rows per CTA
 constexpr int kMqBlock = 32;              // K/V rows per staged block
+constexpr int kMqHeld = 3;                // page ids the producer warp holds per lane
 
 template <int D>
 struct MqTiling {
@@ -78,10 +79,11 @@ __device__ __forceinline__ bool any_bit(const uint32_t* m, int lo, int hi) {
   return false;
 }
 
-template <int D, int G>
-__global__ void __launch_bounds__(kMqWarps * 32, 2) multi_kernel(const MultiLaunch a) {
+template <int D, int G, int NW>
+__global__ void __launch_bounds__(NW * 32) multi_kernel(const MultiLaunch a) {
   using Tl = MqTiling<D>;
-  constexpr int QT = kMqRows / G;   // query tokens per CTA
+  constexpr int kMqWarps = NW;      // warps per CTA, 16 (query, head) rows each
+  constexpr int QT = 16 * NW / G;   // query tokens per CTA
   constexpr int NKD = D / 16;       // k-steps of S = q K^T
   constexpr int NTD = D / 8;        // 8-column tiles of O
   constexpr int S = Tl::kS;
@@ -141,6 +143,22 @@ __global__ void __launch_bounds__(kMqWarps * 32, 2) multi_kernel(const MultiLaun
   const bf16_t* kg = reinterpret_cast<const bf16_t*>(a.k);
   const bf16_t* vg = reinterpret_cast<const bf16_t*>(a.v);
   const int32_t* pt = a.page_table + static_cast<size_t>(b) * a.max_pages;
+  // Page slots of the scanned rows: those of the prompt range, then those of
+  // the window range.  The producer warp holds up to 32 * kMqHeld of them (lane
+  // l: slots l, l + 32, ...), loaded once, so a block's copies wait on no
+  // page-table load; longer ranges load their page ids per block.
+  const int slotsA = nA > 0 ? ((nA - 1) >> 4) + 1 : 0;
+  const int sB0 = bstart >> 4;
+  const int nslots = slotsA + (R > nA ? (i_last >> 4) - sB0 + 1 : 0);
+  const bool held = nslots <= 32 * kMqHeld;
+  int hpg[kMqHeld] = {0, 0, 0};
+  if (warp == 0 && held) {
+#pragma unroll
+    for (int h = 0; h < kMqHeld; ++h) {
+      const int x = lane + 32 * h;
+      if (x < nslots) hpg[h] = __ldg(pt + (x < slotsA ? x : sB0 + (x - slotsA)));
+    }
+  }
 
   // Warp 0: stage block `blk` into stage s.  Lane l serves position 32 blk + l.
   auto produce = [&](int blk, int s) {
@@ -159,6 +177,16 @@ __global__ void __launch_bounds__(kMqWarps * 32, 2) multi_kernel(const MultiLaun
     unsigned char* kst = smem + s * Tl::kStage;
     unsigned char* vst = kst + kMqBlock * Tl::kStride;
     const unsigned need_mask = __ballot_sync(0xffffffffu, need);
+    // page id of this lane's row: from the held ids (every lane takes part)
+    int hp = 0;
+    if (held) {
+      const int x = p < nA ? (j >> 4) : slotsA + ((j >> 4) - sB0);
+#pragma unroll
+      for (int h = 0; h < kMqHeld; ++h) {
+        const int v = __shfl_sync(0xffffffffu, hpg[h], x & 31);
+        if ((x >> 5) == h) hp = v;
+      }
+    }
     if (!need) {
       // not read: zeros (finite under p = 0) in the K and V slots of this row
 #pragma unroll
@@ -174,7 +202,7 @@ __global__ void __launch_bounds__(kMqWarps * 32, 2) multi_kernel(const MultiLaun
       mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(__popc(need_mask) * 2 * Tl::kRowBytes));
     __syncwarp();
     if (need) {
-      int pg = __ldg(pt + (j >> 4));
+      int pg = held ? hp : __ldg(pt + (j >> 4));
       if (static_cast<unsigned>(pg) >= static_cast<unsigned>(a.num_pages)) {
         set_error(a.err, DSA_DEV_BAD_PAGE);
         pg = 0;
@@ -230,6 +258,18 @@ __global__ void __launch_bounds__(kMqWarps * 32, 2) multi_kernel(const MultiLaun
   int k = 0;
   for (; k < nblocks; ++k) {
     const int s = k % S;
+    // warp 0 refills the stage of block k-1 (once every warp is done with it)
+    // before computing block k, so that its copies fly during that work
+    if (warp == 0 && k >= 1 && k - 1 + S < nblocks) {
+      const int sp = (k - 1) % S;
+      if (!__all_sync(0xffffffffu,
+                      mbar_wait(&empty[sp], static_cast<uint32_t>((k - 1) / S) & 1u))) {
+        failed = true;
+        break;
+      }
+      produce(k - 1 + S, sp);
+      ++produced;
+    }
     if (!__all_sync(0xffffffffu, mbar_wait(&full[s], static_cast<uint32_t>(k / S) & 1u))) {
       failed = true;
       break;
@@ -327,15 +367,6 @@ __global__ void __launch_bounds__(kMqWarps * 32, 2) multi_kernel(const MultiLaun
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
-    if (warp == 0 && k + S < nblocks) {
-      if (!__all_sync(0xffffffffu, mbar_wait(&empty[s], static_cast<uint32_t>(k / S) & 1u))) {
-        failed = true;
-        ++k;  // block k itself was consumed
-        break;
-      }
-      produce(k + S, s);
-      ++produced;
-    }
   }
   if (failed) {
     if (lane == 0) set_error(a.err, DSA_DEV_TIMEOUT);
@@ -363,19 +394,26 @@ __global__ void __launch_bounds__(kMqWarps * 32, 2) multi_kernel(const MultiLaun
   }
 }
 
-template <int D, int G>
-cudaError_t launch_multi_one(const MultiLaunch& a, cudaStream_t s) {
+template <int D, int G, int NW>
+cudaError_t launch_multi_nw(const MultiLaunch& a, cudaStream_t s) {
   const int smem = MqTiling<D>::smem(a.mask_words);
-  auto kern = multi_kernel<D, G>;
+  auto kern = multi_kernel<D, G, NW>;
   const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(a.q_tiles, a.hkv, a.batch), dim3(kMqWarps * 32),
+  return launch_pdl(kern, dim3(a.q_tiles, a.hkv, a.batch), dim3(NW * 32),
                     static_cast<size_t>(smem), s, a);
+}
+
+template <int D, int G>
+cudaError_t launch_multi_one(const MultiLaunch& a, cudaStream_t s) {
+  return a.warps == 2 ? launch_multi_nw<D, G, 2>(a, s) : launch_multi_nw<D, G, 4>(a, s);
 }
 
 }  // namespace
 
-int multi_queries_per_cta(int group) { return kMqRows / group; }
+int multi_warps(int max_q, int group) { return static_cast<int64_t>(max_q) * group <= 32 ? 2 : 4; }
+
+int multi_queries_per_cta(int warps, int group) { return 16 * warps / group; }
 
 cudaError_t launch_multi(const MultiLaunch& a, cudaStream_t s) {
   const int g = a.hq / a.hkv;
