@@ -440,6 +440,12 @@ def measure_prefill(name, q_len, K, W, device, stream, peak):
     cfg = wl.WORKLOADS[name]
     w = wl.generate(cfg, device=str(device))
     bt = DecodeBatch.from_workload(w, device=device)
+    if cfg.mask == "top_mass":
+        _, om = bt.attention_mass(r_local=2, r_diag=2)
+        w["keep_mask"] = wl.top_mass_keep_mask(om.cpu().numpy(), w["window"], w["hkv"],
+                                               w["mask_words"], band=cfg.band,
+                                               frac=cfg.top_mass_frac)
+        bt.set_keep_mask(w["keep_mask"])
     q, ql = prefill_inputs(w, q_len, device)
     out = torch.empty(tuple(q.shape), dtype=torch.float32, device=device)
     lse = torch.empty(tuple(q.shape[:3]), dtype=torch.float32, device=device)

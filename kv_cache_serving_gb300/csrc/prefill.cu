@@ -40,13 +40,18 @@
 #include "mma.cuh"
 
 #ifndef DSA_MQ_STAGES
-#define DSA_MQ_STAGES 3
+#define DSA_MQ_STAGES 2
 #endif
 
 namespace dsa {
 namespace {
 
-constexpr int kMqBlock = 32;              // K/V rows per staged block
+#ifndef DSA_MQ_BLOCK
+#define DSA_MQ_BLOCK 32
+#endif
+constexpr int kMqBlock = DSA_MQ_BLOCK;    // K/V rows per staged block (16 or 32)
+static_assert(kMqBlock == 16 || kMqBlock == 32, "block rows");
+constexpr int kMqNT = kMqBlock / 8;       // 8-row tiles of S per block
 constexpr int kMqHeld = 3;                // page ids the producer warp holds per lane
 
 template <int D>
@@ -79,8 +84,20 @@ __device__ __forceinline__ bool any_bit(const uint32_t* m, int lo, int hi) {
   return false;
 }
 
+// Resident CTAs per SM the 2-warp and 4-warp builds must allow for (register
+// budget: 168 per thread either way, no spills).  With two 17 KB stages, six
+// 2-warp CTAs fit an SM: Janus-like 32-token chunk 176 -> 143 us against the
+// compiler's own choice (176 registers, smem for 4 CTAs of 3 stages).
+#ifndef DSA_MQ_MINB2
+#define DSA_MQ_MINB2 6
+#endif
+#ifndef DSA_MQ_MINB4
+#define DSA_MQ_MINB4 3
+#endif
+
 template <int D, int G, int NW>
-__global__ void __launch_bounds__(NW * 32) multi_kernel(const MultiLaunch a) {
+__global__ void __launch_bounds__(NW * 32, NW == 2 ? DSA_MQ_MINB2 : DSA_MQ_MINB4)
+    multi_kernel(const MultiLaunch a) {
   using Tl = MqTiling<D>;
   constexpr int kMqWarps = NW;      // warps per CTA, 16 (query, head) rows each
   constexpr int QT = 16 * NW / G;   // query tokens per CTA
@@ -160,9 +177,12 @@ __global__ void __launch_bounds__(NW * 32) multi_kernel(const MultiLaunch a) {
     }
   }
 
-  // Warp 0: stage block `blk` into stage s.  Lane l serves position 32 blk + l.
+  // Warp 0: stage block `blk` into stage s.  32-row blocks: lane l copies the K
+  // and V rows of position 32 blk + l; 16-row blocks: lanes 0-15 the K rows and
+  // lanes 16-31 the V rows of positions 16 blk + (l % 16).
   auto produce = [&](int blk, int s) {
-    const int p = blk * kMqBlock + lane;
+    const int r = lane & (kMqBlock - 1);
+    const int p = blk * kMqBlock + r;
     const int j = p < R ? row_of(p) : 0;
     bool need = false;
     if (p < R) {
@@ -187,19 +207,22 @@ __global__ void __launch_bounds__(NW * 32) multi_kernel(const MultiLaunch a) {
         if ((x >> 5) == h) hp = v;
       }
     }
+    constexpr int kCopies = kMqBlock == 32 ? 2 : 1;  // bulk copies per lane
+    const bool do_k = kMqBlock == 32 || lane < 16, do_v = kMqBlock == 32 || lane >= 16;
     if (!need) {
       // not read: zeros (finite under p = 0) in the K and V slots of this row
 #pragma unroll
       for (int x = 0; x < Tl::kRowBytes; x += 16) {
-        *reinterpret_cast<uint4*>(kst + lane * Tl::kStride + x) = make_uint4(0u, 0u, 0u, 0u);
-        *reinterpret_cast<uint4*>(vst + lane * Tl::kStride + x) = make_uint4(0u, 0u, 0u, 0u);
+        if (do_k) *reinterpret_cast<uint4*>(kst + r * Tl::kStride + x) = make_uint4(0u, 0u, 0u, 0u);
+        if (do_v) *reinterpret_cast<uint4*>(vst + r * Tl::kStride + x) = make_uint4(0u, 0u, 0u, 0u);
       }
     }
     // this warp's earlier generic accesses of the stage before the async writes
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0)
-      mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(__popc(need_mask) * 2 * Tl::kRowBytes));
+      mbar_arrive_expect_tx(&full[s],
+                            static_cast<uint32_t>(__popc(need_mask) * kCopies * Tl::kRowBytes));
     __syncwarp();
     if (need) {
       int pg = held ? hp : __ldg(pt + (j >> 4));
@@ -208,8 +231,8 @@ __global__ void __launch_bounds__(NW * 32) multi_kernel(const MultiLaunch a) {
         pg = 0;
       }
       const size_t off = ((static_cast<size_t>(pg) * kPage + (j & (kPage - 1))) * a.hkv + hk) * D;
-      bulk_copy_g2s(kst + lane * Tl::kStride, kg + off, Tl::kRowBytes, &full[s]);
-      bulk_copy_g2s(vst + lane * Tl::kStride, vg + off, Tl::kRowBytes, &full[s]);
+      if (do_k) bulk_copy_g2s(kst + r * Tl::kStride, kg + off, Tl::kRowBytes, &full[s]);
+      if (do_v) bulk_copy_g2s(vst + r * Tl::kStride, vg + off, Tl::kRowBytes, &full[s]);
     }
   };
 
@@ -243,6 +266,14 @@ __global__ void __launch_bounds__(NW * 32) multi_kernel(const MultiLaunch a) {
 #pragma unroll
     for (int e = 0; e < 4; ++e) o[nt][e] = 0.f;
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  // Lane offsets of the ldmatrix rows inside a stage.  K (x4, two 8-row tiles of
+  // one 16-dim slice): row np*16 + 8*(lane>>4 & 1) + (lane & 7), bytes
+  // 16*(lane>>3 & 1) into the slice.  V (x4 trans, 16 rows x two 8-dim tiles):
+  // row 8*(lane>>3 & 1) + (lane & 7), bytes 16*(lane>>4) into the 16-dim slice.
+  const uint32_t smem_u32 = smem_addr(smem);
+  const uint32_t k_lane_off =
+      (((lane >> 4) & 1) * 8 + (lane & 7)) * Tl::kStride + ((lane >> 3) & 1) * 16;
+  const uint32_t v_lane_off = (((lane >> 3) & 1) * 8 + (lane & 7)) * Tl::kStride + (lane >> 4) * 16;
 
   // kept(i, j) for a valid query i and a scanned row j
   auto kept = [&](int i, int j) -> bool {
@@ -275,43 +306,64 @@ __global__ void __launch_bounds__(NW * 32) multi_kernel(const MultiLaunch a) {
       break;
     }
     if (warp_active) {
-      const unsigned char* kst = smem + s * Tl::kStage;
-      const unsigned char* vst = kst + kMqBlock * Tl::kStride;
-      // S = q K^T over the block's 32 rows: four 8-row tiles
-      float sc[4][4];
+      // this lane's ldmatrix row addresses in the stage (shared-space, bytes)
+      const uint32_t kbase = smem_u32 + s * Tl::kStage + k_lane_off;
+      const uint32_t vbase = smem_u32 + s * Tl::kStage + kMqBlock * Tl::kStride + v_lane_off;
+      // S = q K^T over the block's rows, 8-row tiles, each summed in two
+      // chains (even and odd 16-dim slices) to halve the dependent mma latency
+      float sc[kMqNT][4], s2[kMqNT][4];
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt)
+      for (int nt = 0; nt < kMqNT; ++nt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) sc[nt][e] = 0.f;
+        for (int e = 0; e < 4; ++e) sc[nt][e] = s2[nt][e] = 0.f;
 #pragma unroll
       for (int kk = 0; kk < NKD; ++kk)
 #pragma unroll
-        for (int np = 0; np < 2; ++np) {
+        for (int np = 0; np < kMqNT / 2; ++np) {
           uint32_t bf[4];
-          ldsm_x4(bf, kst + (np * 16 + ((lane >> 4) & 1) * 8 + (lane & 7)) * Tl::kStride +
-                          (16 * kk + ((lane >> 3) & 1) * 8) * 2);
-          mma_bf16(sc[2 * np], qa[kk], bf[0], bf[1]);
-          mma_bf16(sc[2 * np + 1], qa[kk], bf[2], bf[3]);
+          ldsm_x4_at(bf, kbase + np * 16 * Tl::kStride + 32 * kk);
+          if (kk & 1) {
+            mma_bf16(s2[2 * np], qa[kk], bf[0], bf[1]);
+            mma_bf16(s2[2 * np + 1], qa[kk], bf[2], bf[3]);
+          } else {
+            mma_bf16(sc[2 * np], qa[kk], bf[0], bf[1]);
+            mma_bf16(sc[2 * np + 1], qa[kk], bf[2], bf[3]);
+          }
         }
-      // scale; mask pairs the query does not keep (and positions past R)
+#pragma unroll
+      for (int nt = 0; nt < kMqNT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sc[nt][e] += s2[nt][e];
+      // scale; mask pairs the query does not keep (and positions past R).  A
+      // whole block of prompt rows at or before every query of the tile is kept
+      // by all of them.
       const int p0 = k * kMqBlock;
-      const bool plain = p0 + kMqBlock <= nA && p0 + kMqBlock - 1 <= i_first;
+      if (p0 + kMqBlock <= nA && p0 + kMqBlock - 1 <= i_first) {
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt)
+        for (int nt = 0; nt < kMqNT; ++nt)
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const int p = p0 + nt * 8 + 2 * tig + c;
-          const int j = row_of(p);
-          const bool in = p < R;
-          const bool k0 = v0 && in && (plain || kept(iq0, j));
-          const bool k1 = v1 && in && (plain || kept(iq1, j));
-          sc[nt][c] = k0 ? sc[nt][c] * a.scale_log2 : -INFINITY;
-          sc[nt][2 + c] = k1 ? sc[nt][2 + c] * a.scale_log2 : -INFINITY;
-        }
+          for (int c = 0; c < 2; ++c) {
+            sc[nt][c] = v0 ? sc[nt][c] * a.scale_log2 : -INFINITY;
+            sc[nt][2 + c] = v1 ? sc[nt][2 + c] * a.scale_log2 : -INFINITY;
+          }
+      } else {
+#pragma unroll
+        for (int nt = 0; nt < kMqNT; ++nt)
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const int p = p0 + nt * 8 + 2 * tig + c;
+            const int j = row_of(p);
+            const bool in = p < R;
+            const bool k0 = v0 && in && kept(iq0, j);
+            const bool k1 = v1 && in && kept(iq1, j);
+            sc[nt][c] = k0 ? sc[nt][c] * a.scale_log2 : -INFINITY;
+            sc[nt][2 + c] = k1 ? sc[nt][2 + c] * a.scale_log2 : -INFINITY;
+          }
+      }
       // online softmax of rows r0 (elements 0, 1) and r1 (elements 2, 3)
       float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
+      for (int nt = 0; nt < kMqNT; ++nt) {
         mx0 = fmaxf(mx0, fmaxf(sc[nt][0], sc[nt][1]));
         mx1 = fmaxf(mx1, fmaxf(sc[nt][2], sc[nt][3]));
       }
@@ -328,7 +380,7 @@ __global__ void __launch_bounds__(NW * 32) multi_kernel(const MultiLaunch a) {
       m1 = mn1;
       float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
+      for (int nt = 0; nt < kMqNT; ++nt) {
         sc[nt][0] = exp2f(sc[nt][0] - bs0);
         sc[nt][1] = exp2f(sc[nt][1] - bs0);
         sc[nt][2] = exp2f(sc[nt][2] - bs1);
@@ -338,16 +390,20 @@ __global__ void __launch_bounds__(NW * 32) multi_kernel(const MultiLaunch a) {
       }
       l0 = l0 * al0 + ps0;
       l1 = l1 * al1 + ps1;
+      // O is rescaled only when some row's running max moved (else every
+      // factor is exactly 1)
+      if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
 #pragma unroll
-      for (int nt = 0; nt < NTD; ++nt) {
-        o[nt][0] *= al0;
-        o[nt][1] *= al0;
-        o[nt][2] *= al1;
-        o[nt][3] *= al1;
+        for (int nt = 0; nt < NTD; ++nt) {
+          o[nt][0] *= al0;
+          o[nt][1] *= al0;
+          o[nt][2] *= al1;
+          o[nt][3] *= al1;
+        }
       }
       // O += P V: P (bf16) straight from the score registers as A fragments
 #pragma unroll
-      for (int j2 = 0; j2 < 2; ++j2) {
+      for (int j2 = 0; j2 < kMqBlock / 16; ++j2) {
         uint32_t pa[4];
         pa[0] = pack_bf16(sc[2 * j2][0], sc[2 * j2][1]);
         pa[1] = pack_bf16(sc[2 * j2][2], sc[2 * j2][3]);
@@ -356,15 +412,18 @@ __global__ void __launch_bounds__(NW * 32) multi_kernel(const MultiLaunch a) {
 #pragma unroll
         for (int dp = 0; dp < NTD / 2; ++dp) {
           uint32_t bf[4];
-          ldsm_x4_trans(bf, vst + (16 * j2 + ((lane >> 3) & 1) * 8 + (lane & 7)) * Tl::kStride +
-                                (16 * dp + (lane >> 4) * 8) * 2);
+          ldsm_x4_trans_at(bf, vbase + 16 * j2 * Tl::kStride + 32 * dp);
           mma_bf16(o[2 * dp], pa, bf[0], bf[1]);
           mma_bf16(o[2 * dp + 1], pa, bf[2], bf[3]);
         }
       }
     }
-    // this warp's reads of the stage are done
-    fence_proxy_async_smem();
+    // this warp's reads of the stage are done (the producer orders them before
+    // its copies: it acquires the stage through this barrier, then fences)
+#ifndef DSA_MQ_CFENCE
+#define DSA_MQ_CFENCE 1
+#endif
+    if (DSA_MQ_CFENCE) fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
   }
