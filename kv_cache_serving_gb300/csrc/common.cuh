@@ -126,6 +126,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
+// 16 bytes global -> shared through the L2 (cp.async, completion tracked below).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src)
+               : "memory");
+}
+// One arrival on `bar` once every cp.async this thread issued so far has landed
+// (the barrier's count must include it).
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar))
+               : "memory");
+}
+
 // Orders this thread's generic-proxy shared-memory accesses before later
 // async-proxy (bulk copy) writes to the same shared memory.
 __device__ __forceinline__ void fence_proxy_async_smem() {

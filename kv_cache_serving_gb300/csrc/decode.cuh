@@ -78,6 +78,11 @@ namespace dsa {
 #ifndef DSA_DECODE_WARPS
 #define DSA_DECODE_WARPS 4
 #endif
+// Rows on a stage ring are gathered with 16-byte cp.async copies: 1 for rows of
+// 128 bytes, 2 for every row size, 0 never (one bulk copy per row).
+#ifndef DSA_GATHER_CPASYNC
+#define DSA_GATHER_CPASYNC 1
+#endif
 // Cluster launches (sparse decode split over a thread-block cluster) are also
 // programmatic dependents when set.
 #ifndef DSA_PDL_CLUSTER
@@ -327,9 +332,14 @@ __global__ void __launch_bounds__(NWARPS * 32,
         smem + (Tl::kSlotInRing ? w * Tl::kWarpBytes : Tl::kSlotOff + w * Tl::kSlotBytes));
   };
 
+  // 128-byte rows on a stage ring: 16-byte cp.async copies, 8 lanes per row (a
+  // bulk copy per row of this size streams far below the HBM rate); the stage
+  // barrier then counts one arrival per lane instead of transaction bytes.
+  constexpr bool kCpa =
+      !kSplit && (DSA_GATHER_CPASYNC == 2 || (DSA_GATHER_CPASYNC == 1 && kRowBytes == 128));
   if (lane == 0) {
 #pragma unroll
-    for (int s = 0; s < Tl::kBars; ++s) mbar_init(&bars[s], 1);
+    for (int s = 0; s < Tl::kBars; ++s) mbar_init(&bars[s], kCpa ? 32 : 1);
     fence_mbar_init();
   }
   __syncwarp();
@@ -390,6 +400,34 @@ __global__ void __launch_bounds__(NWARPS * 32,
   // Enqueue the bulk copies of local tile t (rows of global tile warp + t*NW).
   auto issue = [&](int t, int stage, int j, int pg) {
     const int nrows = tile_rows(t);
+    if constexpr (kCpa) {
+      // global row of this lane's row (page * 16 + slot), -2 for the appended row
+      int rg = 0;
+      if (my_r < nrows) {
+        if (static_cast<unsigned>(pg) >= static_cast<unsigned>(a.num_pages)) {
+          set_error(a.err, DSA_DEV_BAD_PAGE);
+          pg = 0;
+        }
+        rg = (knew != nullptr && j == L - 1) ? -2 : pg * kPage + (j & (kPage - 1));
+      }
+      // kLpr lanes per row (16 bytes each), kRpg rows per 32-lane group
+      constexpr int kLpr = kRowBytes / 16, kRpg = 32 / kLpr;
+      const int rq = lane / kLpr, c16 = (lane % kLpr) * 16;
+#pragma unroll
+      for (int g = 0; g < T / kRpg; ++g) {
+        const int r = kRpg * g + rq;
+        const int src_rg = __shfl_sync(0xffffffffu, rg, r);
+        if (r < nrows) {
+          const size_t dst = (static_cast<size_t>(stage) * T + r) * kRowStride + c16;
+          const KV* ks = src_rg == -2 ? knew : kg + (static_cast<size_t>(src_rg) * a.hkv + hk) * D;
+          const KV* vs = src_rg == -2 ? vnew : vg + (static_cast<size_t>(src_rg) * a.hkv + hk) * D;
+          cp_async16(kst + dst, reinterpret_cast<const unsigned char*>(ks) + c16);
+          cp_async16(vst + dst, reinterpret_cast<const unsigned char*>(vs) + c16);
+        }
+      }
+      cp_async_arrive(&bars[stage]);
+      return;
+    }
     if (lane == 0) mbar_arrive_expect_tx(&bars[stage], static_cast<uint32_t>(nrows * 2 * kRowBytes));
     __syncwarp();
     if (my_r < nrows && (T == 32 || lane < 2 * T)) {
