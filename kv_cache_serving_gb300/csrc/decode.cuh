@@ -79,7 +79,8 @@ namespace dsa {
 #define DSA_DECODE_WARPS 4
 #endif
 // Rows on a stage ring are gathered with 16-byte cp.async copies: 1 for rows of
-// 128 bytes, 2 for every row size, 0 never (one bulk copy per row).
+// 128 bytes, dense rows and the wide build, 2 for every stage ring, 0 never (one
+// bulk copy per row).
 #ifndef DSA_GATHER_CPASYNC
 #define DSA_GATHER_CPASYNC 1
 #endif
@@ -332,11 +333,16 @@ __global__ void __launch_bounds__(NWARPS * 32,
         smem + (Tl::kSlotInRing ? w * Tl::kWarpBytes : Tl::kSlotOff + w * Tl::kSlotBytes));
   };
 
-  // 128-byte rows on a stage ring: 16-byte cp.async copies, 8 lanes per row (a
-  // bulk copy per row of this size streams far below the HBM rate); the stage
-  // barrier then counts one arrival per lane instead of transaction bytes.
+  // Stage rings gathered with 16-byte cp.async copies (kRowBytes/16 lanes per
+  // row) instead of one bulk copy per row: rows of 128 bytes (a bulk copy of that
+  // size streams far below the HBM rate), dense rows and the wide build (both
+  // measured faster); the stage barrier then counts one arrival per lane
+  // instead of transaction bytes.
+  constexpr bool kWideBuild = NWARPS == DSA_DECODE_WARPS_WIDE && STAGES == 1;
   constexpr bool kCpa =
-      !kSplit && (DSA_GATHER_CPASYNC == 2 || (DSA_GATHER_CPASYNC == 1 && kRowBytes == 128));
+      !kSplit && (DSA_GATHER_CPASYNC == 2 ||
+                  (DSA_GATHER_CPASYNC == 1 &&
+                   (kRowBytes == 128 || MODE == kRowsDense || kWideBuild)));
   if (lane == 0) {
 #pragma unroll
     for (int s = 0; s < Tl::kBars; ++s) mbar_init(&bars[s], kCpa ? 32 : 1);

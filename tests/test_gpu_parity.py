@@ -246,6 +246,60 @@ def test_small_batch_build(name, batch):
     run_both(w, mask=mask)
 
 
+def test_request_schedule_changes_no_bits():
+    """dsa_build_index leaves a longest-first request schedule in the workspace;
+    dsa_decode_sparse on it must give the bits it gives on a workspace without
+    one (a zero-filled copy: no schedule tag), and a schedule written for
+    another batch size must be ignored."""
+    w = wl.generate(wl.scaled(wl.WORKLOADS["mixed-serving"], batch=24))
+    mask = top_mass_masks_from_oracle(w)
+    bt = DecodeBatch.from_workload(w, keep_mask=mask)
+    bt.build_index()
+    with_sched = [t.clone() for t in bt.decode_sparse()]
+    fresh = torch.zeros_like(bt.ws)
+    out = torch.empty_like(bt.out)
+    lse = torch.empty_like(bt.lse)
+    dsa.dsa_decode_sparse(bt.dims, bt.q, bt.k_pages, bt.v_pages, bt.page_table, bt.seq_len,
+                          bt.kept_idx, bt.kept_cnt, bt.scale, out, lse, fresh)
+    torch.cuda.synchronize()
+    assert bt.device_error() == 0 and dsa.dsa_get_device_error(fresh) == 0
+    assert torch.equal(out, with_sched[0]) and torch.equal(lse, with_sched[1])
+    # the first 12 requests alone, decoded on the workspace that holds the
+    # 24-request schedule: the tag does not match, batch order is used
+    d12 = dsa.make_dims(12, w["hq"], w["hkv"], w["head_dim"], w["num_pages"], w["max_pages"],
+                        w["max_window"], w["mask_words"], w["max_kept"], "bf16", "bf16")
+    o12 = torch.empty_like(bt.out[:12])
+    l12 = torch.empty_like(bt.lse[:12])
+    dsa.dsa_decode_sparse(d12, bt.q[:12].contiguous(), bt.k_pages, bt.v_pages,
+                          bt.page_table[:12].contiguous(), bt.seq_len[:12].contiguous(),
+                          bt.kept_idx[:12].contiguous(), bt.kept_cnt[:12].contiguous(), bt.scale,
+                          o12, l12, bt.ws)
+    torch.cuda.synchronize()
+    assert bt.device_error() == 0
+    ref, ref_lse = oracle.decode(oracle_inputs(w, mask), sparse=True,
+                                 bh=[(b, h) for b in range(12) for h in range(w["hq"])])
+    assert_outputs(o12.cpu().numpy().reshape(-1, w["head_dim"]), ref, fp32=False)
+    assert np.abs(l12.cpu().numpy().reshape(-1) - ref_lse).max() <= LSE_MAX
+
+
+def test_wide_build_for_small_batches():
+    """At most one (request, kv head) per SM: one 8-warp CTA per unit (automatic
+    cluster setting), checked against the oracle; forcing clusters of 2 falls
+    back to the cluster split."""
+    w = wl.generate(wl.scaled(wl.WORKLOADS["emu3-8b"], batch=4))
+    bt = DecodeBatch.from_workload(w)
+    saved = dsa.dsa_get_sparse_cluster()
+    try:
+        dsa.dsa_set_sparse_cluster(0)
+        plan = dsa.dsa_decode_plan(bt.dims, dsa.PLAN_MASKED)
+        assert plan[1] == 1 and plan[2] == 1 and plan[3] == 8, plan
+        dsa.dsa_set_sparse_cluster(2)
+        assert dsa.dsa_decode_plan(bt.dims, dsa.PLAN_MASKED)[3] != 8
+    finally:
+        dsa.dsa_set_sparse_cluster(saved)
+    run_both(w)
+
+
 # ---------------------------------------------------------------------------
 # invariants and edge cases
 # ---------------------------------------------------------------------------
