@@ -61,22 +61,29 @@ FALLBACK_HBM_GBS = 6800.0
 # step's decode kernel, per workload, from one ncu capture of
 # `bench.py --workload NAME --profile masked --warmup 2 --steps 1` (the same launch
 # on the same batch; the summaries are under profiles/).  They describe the
-# kernel sources whose digest is `digest` and are reported as null otherwise.
+# decode-kernel sources whose digest is `digest` and are reported as null
+# otherwise.
 NCU_TRAFFIC = {
-    "digest": "d6e403b3d0905063",
+    "digest": "27e58a18fbf44d2b",
     "bytes": {
-        "llamagen-xl-like-24x24": 21429504,
-        "janus-pro-7b-like-32x32": 316743680,
-        "emu3-8b-like-90x90-gqa4": 3282432,
-        "mixed-serving-gqa4": 168586240,
+        "mixed-serving-gqa4": 167970816,
+        "janus-pro-7b-like-32x32": 316311040,
+        "llamagen-xl-like-24x24": 21440512,
+        "emu3-8b-like-90x90-gqa4": 3282176,
     },
 }
 
 
+# Sources the timed decode kernel (and its launch plan) is built from.
+DECODE_SOURCES = ("common.cuh", "decode.cuh", "warp_attn.cuh", "mma.cuh", "internal.h",
+                  "decode_bf16.cu", "decode_bf16_list.cu", "decode_bf16_mask.cu", "decode_f32.cu",
+                  "dsa_api.cu")
+
+
 def kernel_digest() -> str:
-    """sha256 over the kernel sources (csrc/ and the public header)."""
+    """sha256 over the sources of the timed decode kernel and the public header."""
     h = hashlib.sha256()
-    files = sorted(glob.glob(os.path.join(ROOT, "kv_cache_serving_gb300", "csrc", "*")))
+    files = [os.path.join(ROOT, "kv_cache_serving_gb300", "csrc", f) for f in DECODE_SOURCES]
     files.append(os.path.join(ROOT, "include", "dsa.h"))
     for f in files:
         h.update(os.path.basename(f).encode())
