@@ -130,6 +130,18 @@ def test_prefill_whole_sequences_and_edges():
     compare(w, q, ql, out, lse)
 
 
+def test_prefill_window_past_1024_offsets():
+    """Windows longer than the fused decode's limit (1024 offsets): 47 mask words
+    in shared memory, kept offsets spread over all of them."""
+    cfg = small_cfg(128, 2, batch=3, Lmax=2200, Pmax=60, W=1500, seed=11)
+    w = wl.generate(cfg)
+    assert w["mask_words"] == 47
+    bt = DecodeBatch.from_workload(w)
+    q, ql = chunk_inputs(w, 40, seed=12)
+    out, lse = run_prefill(bt, q, ql)
+    compare(w, q, ql, out, lse)
+
+
 def test_prefill_single_query_is_a_decode_step():
     """q_len = 1 is a decode step: within the bars of the decode oracle."""
     w = wl.generate(wl.scaled(wl.WORKLOADS["janus-pro-7b"], batch=4))
