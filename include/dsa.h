@@ -348,6 +348,10 @@ dsa_status dsa_attention_mass(const dsa_dims* dims, const void* q, const void* k
  *                     are not written
  *   lse   (out)       [batch][max_q][hq] float32 natural-log LSE, or NULL
  * Rows of the scanned range that no query of a CTA's tile keeps are not read.
+ * Units may be split over several CTAs (dsa_set_prefill_split), which use the
+ * workspace's partials region and its arrival counters: those counters are
+ * back at zero after every call that completes without a device error (after
+ * one, zero-fill the workspace again).
  * q and KV must be bf16 and max_window <= 32768, else DSA_ERR_UNSUPPORTED.  An
  * invalid per-request value (seq_len, prompt_len, window as above; q_len gives
  * DSA_DEV_BAD_QLEN) sets the error word and NaN in that request's slots.
@@ -458,6 +462,23 @@ dsa_status dsa_decode_sparse_noalloc(const dsa_dims* dims, const void* q, const 
  */
 dsa_status dsa_set_sparse_cluster(int32_t ctas);
 int32_t dsa_get_sparse_cluster(void);
+
+/*
+ * dsa_set_prefill_split -- process-wide tuning of dsa_prefill_sparse (not in
+ * the paper: a scheduling choice).  A unit of that call (a tile of query tokens
+ * of one request and kv head) normally runs in one CTA.  With parts >= 2 every
+ * unit (as many as the workspace holds: the last ones) is split into `parts`
+ * CTAs along its scanned rows; their partial softmax states go to the workspace
+ * and the unit's last CTA to finish merges them (no second kernel).  With 1 no
+ * unit is split; with 0 (the default) each call splits only what balances the
+ * GPU: the units of a last, partial wave of resident CTAs (or every unit of a
+ * batch smaller than one wave) into up to 4 parts.  Results equal the oracle's
+ * within the same bounds either way; the floating-point summation order depends
+ * on the split.  parts in 0..8, else DSA_ERR_INVALID_ARG.  Takes effect for
+ * calls issued afterwards.  dsa_get_prefill_split returns the current value.
+ */
+dsa_status dsa_set_prefill_split(int32_t parts);
+int32_t dsa_get_prefill_split(void);
 
 /*
  * Waits for `stream`, then reads the workspace error word into *code_out (one of

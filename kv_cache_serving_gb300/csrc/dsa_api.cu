@@ -44,6 +44,8 @@ constexpr int kMaxDevices = 64;
 
 // Process-wide: CTAs per cluster of sparse decode (dsa_set_sparse_cluster).
 std::atomic<int> g_sparse_cluster{DSA_SPARSE_CLUSTER};
+// Process-wide: parts of dsa_prefill_sparse's units (dsa_set_prefill_split).
+std::atomic<int> g_prefill_split{0};
 
 bool dims_valid(const dsa_dims* d) {
   if (d == nullptr) return false;
@@ -140,7 +142,13 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 size_t partials_region(const dsa_dims* d) {
   const size_t dec = partial_bytes(d, d->head_dim + 2);
   const size_t mass = partial_bytes(d, 6);
-  return round_up(dec > mass ? dec : mass, 256);
+  // dsa_prefill_sparse's split parts: at most one wave of resident CTAs, at
+  // most kMultiPartWarpsPerSm warps of 16 (query, head) rows each per SM
+  const size_t multi = static_cast<size_t>(sm_count()) * kMultiPartWarpsPerSm * 16 *
+                       (d->head_dim + 2) * sizeof(float);
+  size_t r = dec > mass ? dec : mass;
+  if (multi > r) r = multi;
+  return round_up(r, 256);
 }
 
 // [batch][hkv] kept counts of dsa_decode_sparse_masked, after the partials.
@@ -163,6 +171,14 @@ int32_t* sched_region(const dsa_dims* d, void* ws) {
 size_t sched_bytes(const dsa_dims* d) {
   return round_up(static_cast<size_t>(d->batch) * sizeof(int32_t), 256);
 }
+
+// Arrival counters of dsa_prefill_sparse's split units, after the schedule.
+int32_t* multi_count_region(const dsa_dims* d, void* ws) {
+  return reinterpret_cast<int32_t*>(reinterpret_cast<unsigned char*>(ws) + kWsHeader +
+                                    partials_region(d) + unit_ints_region(d) + sched_bytes(d));
+}
+
+constexpr size_t kMultiCountBytes = kMultiCounters * sizeof(int32_t);
 
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -386,7 +402,8 @@ const char* dsa_status_string(dsa_status status) {
 
 size_t dsa_workspace_size(const dsa_dims* dims) {
   if (check_dims(dims) != DSA_OK) return 0;
-  return kWsHeader + partials_region(dims) + unit_ints_region(dims) + sched_bytes(dims);
+  return kWsHeader + partials_region(dims) + unit_ints_region(dims) + sched_bytes(dims) +
+         kMultiCountBytes;
 }
 
 dsa_status dsa_build_index(const dsa_dims* dims, const int32_t* seq_len,
@@ -567,7 +584,6 @@ dsa_status dsa_prefill_sparse(const dsa_dims* dims, int32_t max_q, const void* q
   if (dims->q_dtype != DSA_BF16 || dims->kv_dtype != DSA_BF16 ||
       dims->max_window > kMultiMaxWindow)
     return DSA_ERR_UNSUPPORTED;
-  if (dims->hkv > 65535 || dims->batch > 65535) return DSA_ERR_UNSUPPORTED;  // grid y, z
   if (dims->batch == 0 || max_q == 0) return DSA_OK;
   MultiLaunch a{};
   a.q = q;
@@ -591,10 +607,19 @@ dsa_status dsa_prefill_sparse(const dsa_dims* dims, int32_t max_q, const void* q
   a.warps = multi_warps(max_q, dims->hq / dims->hkv);
   const int per_cta = multi_queries_per_cta(a.warps, dims->hq / dims->hkv);
   a.q_tiles = static_cast<int32_t>(ceil_div(max_q, per_cta));
+  // work items (units times parts) index a 1-D grid
+  if (static_cast<int64_t>(a.q_tiles) * dims->hkv * dims->batch * kMultiMaxParts > INT32_MAX)
+    return DSA_ERR_UNSUPPORTED;
   a.scale_log2 = scale * kLog2e;
   a.out = out;
   a.lse = lse;
   a.err = err_word(ws);
+  a.split_setting = g_prefill_split.load(std::memory_order_relaxed);
+  a.part = partials(ws);
+  a.part_rows_cap = static_cast<int64_t>(partials_region(dims) / ((dims->head_dim + 2) * sizeof(float)));
+  a.part_count = multi_count_region(dims, ws);
+  a.count_cap = kMultiCounters;
+  a.sms = sm_count();
   return from_cuda(launch_multi(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -671,6 +696,14 @@ dsa_status dsa_set_sparse_cluster(int32_t ctas) {
 }
 
 int32_t dsa_get_sparse_cluster(void) { return g_sparse_cluster.load(std::memory_order_relaxed); }
+
+dsa_status dsa_set_prefill_split(int32_t parts) {
+  if (parts < 0 || parts > kMultiMaxParts) return DSA_ERR_INVALID_ARG;
+  g_prefill_split.store(parts, std::memory_order_relaxed);
+  return DSA_OK;
+}
+
+int32_t dsa_get_prefill_split(void) { return g_prefill_split.load(std::memory_order_relaxed); }
 
 dsa_status dsa_get_device_error(const void* ws, void* stream, int32_t* code_out) {
   if (!ws || !code_out) return DSA_ERR_INVALID_ARG;

@@ -109,6 +109,18 @@ struct MultiLaunch {
   float* out;                 // [batch][max_q][hq][head_dim]
   float* lse;                 // [batch][max_q][hq] or null
   int32_t* err;
+  // Units are (query tile, kv head, request) in that order, x fastest.  The first
+  // n_whole run whole, one CTA each; every later one is split along its scanned
+  // rows into `split` parts whose partial states the unit's last-arriving part
+  // merges.  Filled by launch_multi from the fields below it.
+  int32_t n_whole, split;
+  float* part;                // [split unit][part][16 warps][head_dim + 2]
+  int32_t* part_count;        // [split unit] arrivals, 0 between launches
+  // host only: split setting (0 automatic, 1 never, n: every unit in n parts),
+  // partial rows the workspace holds, arrival counters it holds, SMs
+  int32_t split_setting;
+  int64_t part_rows_cap;
+  int32_t count_cap, sms;
 };
 
 // Row sources of a decode launch (`mode` below).
@@ -140,6 +152,13 @@ int multi_warps(int max_q, int group);
 int multi_queries_per_cta(int warps, int group);
 // Largest max_window of the multi-query call (its mask words sit in shared memory).
 constexpr int kMultiMaxWindow = 32768;
+// Arrival counters of split multi-query units in the workspace, and the most
+// parts a unit is split into.
+constexpr int kMultiCounters = 4096;
+constexpr int kMultiMaxParts = 8;
+// Resident warps per SM of the multi-query kernel the workspace's partials
+// region is sized for (6 CTAs of 2 warps, or 3 of 4).
+constexpr int kMultiPartWarpsPerSm = 12;
 cudaError_t launch_evict(const EvictLaunch& a, cudaStream_t s);
 
 // Host copies of a step (hostio.cu): a copy kernel when the host side is

@@ -12,11 +12,13 @@
 // skipped).  The abstract also reports prefill attention to be diffuse; the
 // call serves chunks whose queries share one mask, as decode steps do.
 //
-// Work decomposition: grid (query tile, kv head, request).  A CTA holds 16 NW
-// (query, head) rows (NW = 2 or 4 warps, the fewest that hold max_q x G) --
-// 16 NW/G consecutive query tokens times the G query heads of one kv head --
+// Work decomposition: a unit is (query tile, kv head, request).  A unit holds
+// 16 NW (query, head) rows (NW = 2 or 4 warps, the fewest that hold max_q x G)
+// -- 16 NW/G consecutive query tokens times the G query heads of one kv head --
 // and scans the union of their kept rows: the prompt rows
-// [0, min(P, i_last+1)) and the window range [max(., i_first-W), i_last].
+// [0, min(P, i_last+1)) and the window range [max(., i_first-W), i_last].  A
+// 1-D grid runs the first units whole, one CTA each, and the rest split along
+// the scanned blocks into parts merged by the unit's last part (plan_split).
 // This is a dense contraction (every staged K/V row meets up to 64 query rows),
 // so it runs on the tensor cores: each warp owns 16 (query, head) rows, its q
 // fragments stay in registers, S = q K^T and O += P V are mma.sync m16n8k16
@@ -84,6 +86,119 @@ __device__ __forceinline__ bool any_bit(const uint32_t* m, int lo, int hi) {
   return false;
 }
 
+// End of one part of a split unit: its partial state goes to the workspace --
+// [16 NW rows][head_dim] unnormalised O, then [16 NW rows][2] (running max in
+// the log2 domain, sum) -- and the unit's last part to arrive merges the parts
+// as a split softmax does: M = max m_p, l = sum l_p 2^(m_p - M), O = sum O_p
+// 2^(m_p - M) / l.  Parts are summed in part order, so the result does not
+// depend on which part arrives last.  The arrival counter is back at 0 after
+// the merge.
+template <int D, int G, int NW>
+__device__ __forceinline__ void multi_merge_parts(const MultiLaunch& a, unsigned char* smem,
+                                                  int item, int unit,
+                                                  int nparts, int b, int hk, int t0, int t1,
+                                                  bool warp_active, bool v0, bool v1, int pr0,
+                                                  int pr1, const float (&o)[D / 8][4], float m0,
+                                                  float m1, float l0, float l1) {
+  constexpr int kRows = 16 * NW;
+  constexpr int kPartFloats = kRows * (D + 2);
+  const int tig = threadIdx.x & 3;
+  float* mine = a.part + static_cast<size_t>(item - a.n_whole) * kPartFloats;
+  if (warp_active) {
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+#pragma unroll
+    for (int nt = 0; nt < D / 8; ++nt) {
+      const int d = 8 * nt + 2 * tig;
+      if (v0) *reinterpret_cast<float2*>(mine + pr0 * D + d) = make_float2(o[nt][0], o[nt][1]);
+      if (v1) *reinterpret_cast<float2*>(mine + pr1 * D + d) = make_float2(o[nt][2], o[nt][3]);
+    }
+    if (tig == 0) {
+      if (v0) *reinterpret_cast<float2*>(mine + kRows * D + 2 * pr0) = make_float2(m0, l0);
+      if (v1) *reinterpret_cast<float2*>(mine + kRows * D + 2 * pr1) = make_float2(m1, l1);
+    }
+  }
+  __threadfence();
+  __syncthreads();
+  __shared__ int last;
+  const int su = unit - a.n_whole;
+  if (threadIdx.x == 0) {
+    const int prev = atomicAdd(a.part_count + su, 1);
+    last = prev == nparts - 1;
+    if (last) a.part_count[su] = 0;  // every part has arrived
+  }
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  // the stages are free (every block was consumed before the barriers above):
+  // weights 2^(m_p - M) [16 NW rows][kMultiMaxParts], then 1/l per row
+  float* wsm = reinterpret_cast<float*>(smem);
+  const float* ub = a.part + static_cast<size_t>(su) * nparts * kPartFloats;
+  const int rows = (t1 - t0) * G;  // row r: query t0 + r / G, head hk G + r % G
+  auto qh_of = [&](int r) {
+    return (static_cast<size_t>(b) * a.max_q + t0 + r / G) * a.hq + hk * G + r % G;
+  };
+  if (static_cast<int>(threadIdx.x) < rows) {
+    const int r = threadIdx.x;
+    float mp[kMultiMaxParts], lp[kMultiMaxParts];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int p = 0; p < kMultiMaxParts; ++p) {
+      if (p < nparts) {
+        const float2 ml = __ldcg(reinterpret_cast<const float2*>(ub + p * kPartFloats + kRows * D) + r);
+        mp[p] = ml.x;
+        lp[p] = ml.y;
+        mx = fmaxf(mx, ml.x);
+      }
+    }
+    float lsum = 0.f;
+#pragma unroll
+    for (int p = 0; p < kMultiMaxParts; ++p) {
+      if (p < nparts) {
+        const float w = mp[p] == -INFINITY ? 0.f : exp2f(mp[p] - mx);
+        wsm[r * kMultiMaxParts + p] = w;
+        lsum += lp[p] * w;
+      }
+    }
+    wsm[kRows * kMultiMaxParts + r] = 1.f / lsum;
+    if (a.lse != nullptr) a.lse[qh_of(r)] = (mx + log2f(lsum)) * kLn2;
+  }
+  __syncthreads();
+  // O: each thread owns D/8 float4 chunks of the [16 NW][D] tile; one part's
+  // chunks are loaded together, so each part costs about one L2 round trip
+  constexpr int kPer = D / 8;
+  float4 acc[kPer];
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int p = 0; p < nparts; ++p) {
+    const float4* pp = reinterpret_cast<const float4*>(ub + p * kPartFloats);
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int c = threadIdx.x + j * NW * 32, r = c / (D / 4);
+      if (r < rows) {
+        const float4 v = __ldcg(pp + c);
+        const float w = wsm[r * kMultiMaxParts + p];
+        acc[j].x += v.x * w;
+        acc[j].y += v.y * w;
+        acc[j].z += v.z * w;
+        acc[j].w += v.w * w;
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int c = threadIdx.x + j * NW * 32, r = c / (D / 4);
+    if (r < rows) {
+      const float inv = wsm[kRows * kMultiMaxParts + r];
+      float* dst = a.out + qh_of(r) * D + 4 * (c % (D / 4));
+      *reinterpret_cast<float2*>(dst) = make_float2(acc[j].x * inv, acc[j].y * inv);
+      *reinterpret_cast<float2*>(dst + 2) = make_float2(acc[j].z * inv, acc[j].w * inv);
+    }
+  }
+}
+
 // Resident CTAs per SM the 2-warp and 4-warp builds must allow for (register
 // budget: 168 per thread either way, no spills).  With two 17 KB stages, six
 // 2-warp CTAs fit an SM: Janus-like 32-token chunk 176 -> 143 us against the
@@ -110,7 +225,17 @@ __global__ void __launch_bounds__(NW * 32, NW == 2 ? DSA_MQ_MINB2 : DSA_MQ_MINB4
   griddep_launch_dependents();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g4 = lane >> 2, tig = lane & 3;
-  const int qtile = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
+  // work item -> unit (query tile, kv head, request) and part of the unit
+  const int item = blockIdx.x;
+  int unit = item, part = 0, nparts = 1;
+  if (item >= a.n_whole) {
+    const int x = item - a.n_whole;
+    unit = a.n_whole + x / a.split;
+    part = x % a.split;
+    nparts = a.split;
+  }
+  const int qtile = unit % a.q_tiles, hk = (unit / a.q_tiles) % a.hkv;
+  const int b = unit / (a.q_tiles * a.hkv);
   const int L = a.seq_len[b], n = a.q_len[b], P = a.prompt_len[b], W = a.window[b];
   int code = 0;
   if (L < 1 || L > a.max_pages * kPage) code = DSA_DEV_BAD_SEQ_LEN;
@@ -119,7 +244,8 @@ __global__ void __launch_bounds__(NW * 32, NW == 2 ? DSA_MQ_MINB2 : DSA_MQ_MINB4
   else if (W < 0 || W > a.max_window) code = DSA_DEV_BAD_WINDOW;
   const int t0 = qtile * QT;
   if (code != 0) {
-    // q_len is not trusted: NaN into every slot this CTA covers
+    // q_len is not trusted: NaN into every slot this unit covers (by part 0)
+    if (part != 0) return;
     if (qtile == 0 && hk == 0 && threadIdx.x == 0) set_error(a.err, code);
     for (int x = threadIdx.x; x < QT * G * D; x += kMqWarps * 32) {
       const int t = t0 + x / (G * D);
@@ -137,7 +263,10 @@ __global__ void __launch_bounds__(NW * 32, NW == 2 ? DSA_MQ_MINB2 : DSA_MQ_MINB4
   const int nA = min(P, i_last + 1);
   const int bstart = max(nA, i_first - W);
   const int R = nA + (i_last >= bstart ? i_last - bstart + 1 : 0);
-  const int nblocks = (R + kMqBlock - 1) / kMqBlock;
+  // this part's blocks kb0 .. kb0 + nblocks - 1 of the unit's
+  const int nb_unit = (R + kMqBlock - 1) / kMqBlock;
+  const int kb0 = static_cast<int>(static_cast<int64_t>(nb_unit) * part / nparts);
+  const int nblocks = static_cast<int>(static_cast<int64_t>(nb_unit) * (part + 1) / nparts) - kb0;
   auto row_of = [&](int p) { return p < nA ? p : bstart + (p - nA); };
 
   uint32_t* msk = reinterpret_cast<uint32_t*>(smem + Tl::kMaskOff);
@@ -238,7 +367,7 @@ __global__ void __launch_bounds__(NW * 32, NW == 2 ? DSA_MQ_MINB2 : DSA_MQ_MINB4
 
   int produced = 0;
   if (warp == 0) {
-    for (; produced < S && produced < nblocks; ++produced) produce(produced, produced);
+    for (; produced < S && produced < nblocks; ++produced) produce(kb0 + produced, produced);
   }
 
   // This thread's two (query, head) rows of the warp's 16: r0 = g4, r1 = g4 + 8.
@@ -298,7 +427,7 @@ __global__ void __launch_bounds__(NW * 32, NW == 2 ? DSA_MQ_MINB2 : DSA_MQ_MINB4
         failed = true;
         break;
       }
-      produce(k - 1 + S, sp);
+      produce(kb0 + k - 1 + S, sp);
       ++produced;
     }
     if (!__all_sync(0xffffffffu, mbar_wait(&full[s], static_cast<uint32_t>(k / S) & 1u))) {
@@ -337,7 +466,7 @@ __global__ void __launch_bounds__(NW * 32, NW == 2 ? DSA_MQ_MINB2 : DSA_MQ_MINB4
       // scale; mask pairs the query does not keep (and positions past R).  A
       // whole block of prompt rows at or before every query of the tile is kept
       // by all of them.
-      const int p0 = k * kMqBlock;
+      const int p0 = (kb0 + k) * kMqBlock;
       if (p0 + kMqBlock <= nA && p0 + kMqBlock - 1 <= i_first) {
 #pragma unroll
         for (int nt = 0; nt < kMqNT; ++nt)
@@ -433,6 +562,18 @@ __global__ void __launch_bounds__(NW * 32, NW == 2 ? DSA_MQ_MINB2 : DSA_MQ_MINB4
     if (warp == 0)
       for (int kb = k; kb < produced; ++kb)
         mbar_wait(&full[kb % S], static_cast<uint32_t>(kb / S) & 1u);
+    if (nparts == 1) return;
+    // a part still arrives (with an empty state), so the unit's count stays whole
+    m0 = m1 = -INFINITY;
+    l0 = l1 = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < NTD; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[nt][e] = 0.f;
+  }
+  if (nparts > 1) {
+    multi_merge_parts<D, G, NW>(a, smem, item, unit, nparts, b, hk, t0, t1, warp_active, v0, v1, pr0,
+                                pr1, o, m0, m1, l0, l1);
     return;
   }
   if (!warp_active) return;
@@ -453,13 +594,51 @@ __global__ void __launch_bounds__(NW * 32, NW == 2 ? DSA_MQ_MINB2 : DSA_MQ_MINB4
   }
 }
 
+// Most parts of the automatic split.
+#ifndef DSA_MQ_MAX_SPLIT
+#define DSA_MQ_MAX_SPLIT 4
+#endif
+
+// Which units run split, and into how many parts.  Units of equal work fill the
+// resident CTA slots in waves, so a last wave of `rem` units leaves most slots
+// idle for a whole unit's time: those units are split into up to
+// slots / rem parts (and a batch of fewer units than slots into up to
+// slots / units parts): at most one wave of parts, which the workspace's
+// partials region is sized for; never past its partial rows and counters.
+// With a fixed setting n >= 2 every unit the workspace holds is split in n.
+void plan_split(MultiLaunch& a, int64_t units, int64_t slots, int rows) {
+  a.n_whole = static_cast<int32_t>(units);
+  a.split = 1;
+  int64_t n_split = 0, parts = 1;
+  if (a.split_setting >= 2) {
+    parts = a.split_setting;
+    n_split = units;
+  } else if (a.split_setting == 0 && slots > 0 && units > 0) {
+    n_split = units >= slots ? units % slots : units;
+    parts = n_split > 0 ? slots / n_split : 1;
+    if (parts > DSA_MQ_MAX_SPLIT) parts = DSA_MQ_MAX_SPLIT;
+  }
+  if (parts < 2 || n_split == 0) return;
+  if (n_split > a.count_cap) n_split = a.count_cap;
+  if (n_split * parts * rows > a.part_rows_cap) n_split = a.part_rows_cap / (parts * rows);
+  if (n_split <= 0) return;
+  a.n_whole = static_cast<int32_t>(units - n_split);
+  a.split = static_cast<int32_t>(parts);
+}
+
 template <int D, int G, int NW>
-cudaError_t launch_multi_nw(const MultiLaunch& a, cudaStream_t s) {
+cudaError_t launch_multi_nw(MultiLaunch a, cudaStream_t s) {
   const int smem = MqTiling<D>::smem(a.mask_words);
   auto kern = multi_kernel<D, G, NW>;
-  const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(a.q_tiles, a.hkv, a.batch), dim3(NW * 32),
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NW * 32, smem);
+  if (e != cudaSuccess) return e;
+  const int64_t units = static_cast<int64_t>(a.q_tiles) * a.hkv * a.batch;
+  plan_split(a, units, static_cast<int64_t>(per_sm) * a.sms, 16 * NW);
+  const int64_t items = a.n_whole + (units - a.n_whole) * a.split;
+  return launch_pdl(kern, dim3(static_cast<unsigned>(items)), dim3(NW * 32),
                     static_cast<size_t>(smem), s, a);
 }
 

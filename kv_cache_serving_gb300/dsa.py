@@ -89,6 +89,8 @@ def _load():
         "dsa_graph_destroy": ([P], I32),
         "dsa_set_sparse_cluster": ([I32], I32),
         "dsa_get_sparse_cluster": ([], I32),
+        "dsa_set_prefill_split": ([I32], I32),
+        "dsa_get_prefill_split": ([], I32),
         "dsa_get_device_error": ([P, P, ctypes.POINTER(I32)], I32),
         "dsa_clear_device_error": ([P, P], I32),
     }
@@ -400,6 +402,16 @@ def dsa_set_sparse_cluster(ctas: int) -> None:
 
 def dsa_get_sparse_cluster() -> int:
     return int(_load().dsa_get_sparse_cluster())
+
+
+def dsa_set_prefill_split(parts: int) -> None:
+    """CTAs per unit of dsa_prefill_sparse (1 = never split, 0 = the units of a
+    last partial wave, or of a batch below one wave, split per call)."""
+    _check(_load().dsa_set_prefill_split(int(parts)), "dsa_set_prefill_split")
+
+
+def dsa_get_prefill_split() -> int:
+    return int(_load().dsa_get_prefill_split())
 
 
 

@@ -42,7 +42,8 @@ def test_library_exports_every_declared_symbol():
 
 def test_tuning_setters():
     for setter, getter, good, bad in (
-            (dsa.dsa_set_sparse_cluster, dsa.dsa_get_sparse_cluster, (0, 1, 2, 8), (-1, 9)),):
+            (dsa.dsa_set_sparse_cluster, dsa.dsa_get_sparse_cluster, (0, 1, 2, 8), (-1, 9)),
+            (dsa.dsa_set_prefill_split, dsa.dsa_get_prefill_split, (0, 1, 2, 8), (-1, 9)),):
         saved = getter()
         try:
             for v in good:

@@ -186,3 +186,35 @@ def test_prefill_invalid_q_len_is_flagged():
     assert bt.device_error() == 11            # DSA_DEV_BAD_QLEN
     assert np.isnan(out[1]).all() and np.isnan(lse[1]).all()
     dsa.dsa_clear_device_error(bt.ws)
+
+
+@pytest.mark.parametrize("parts", [1, 2, 3, 8])
+@pytest.mark.parametrize("D,G", [(128, 4), (64, 1)])
+def test_prefill_split_parts(D, G, parts):
+    """Every unit split into `parts` CTAs along its scanned rows (1: none), the
+    partial states merged by the unit's last part: vs the oracle, with parts that
+    get no block at all among them; a repeat on the same workspace gives the same
+    bits (the arrival counters are back at zero after each call)."""
+    w = wl.generate(small_cfg(D, G, batch=5, Lmax=600, Pmax=100, W=200, seed=20 + D + G))
+    bt = DecodeBatch.from_workload(w)
+    q, ql = chunk_inputs(w, 40, seed=22)
+    saved = dsa.dsa_get_prefill_split()
+    try:
+        dsa.dsa_set_prefill_split(parts)
+        out, lse = run_prefill(bt, q, ql)
+        compare(w, q, ql, out, lse)
+        out2, lse2 = run_prefill(bt, q, ql)
+        assert np.array_equal(out, out2) and np.array_equal(lse, lse2)
+    finally:
+        dsa.dsa_set_prefill_split(saved)
+
+
+def test_prefill_full_size_chunk():
+    """The benchmark's chunk: the full Janus-like batch, 32 query tokens per
+    request, in the automatic split (the units of the last, partial wave of
+    resident CTAs split and merged in the kernel): every slot vs the oracle."""
+    w = wl.generate(wl.WORKLOADS["janus-pro-7b"])
+    bt = DecodeBatch.from_workload(w)
+    q, ql = chunk_inputs(w, 32, seed=31, q_len=np.full(w["batch"], 32, np.int32))
+    out, lse = run_prefill(bt, q, ql)
+    compare(w, q, ql, out, lse)
