@@ -116,12 +116,12 @@ struct DecodeTiling {
   static constexpr int kBars = kSplit ? 2 : S;  // mbarriers per warp
   static constexpr int kWarpBytes = kSplit ? kStageBytes : S * kStageBytes;
   static constexpr int kBarOff = NW * kWarpBytes;
-  static constexpr int kPsOff = kBarOff + NW * kBars * 8;  // [NW][hi, lo][8 heads][T] bf16
+  static constexpr int kBarEnd = kBarOff + NW * kBars * 8;
   // End-of-CTA state of each warp, G x [acc(D), m, l] floats: at the start of
   // the warp's own ring (idle by then) when it fits, else in a region of its own.
   static constexpr int kSlotBytes = G * (D + 2) * 4;
   static constexpr bool kSlotInRing = kSlotBytes <= kWarpBytes;
-  static constexpr int kSlotOff = kPsOff + (MMA ? NW * 2 * 8 * T * 2 : 0);
+  static constexpr int kSlotOff = kBarEnd;
   static constexpr int kSmem = kSlotOff + (kSlotInRing ? 0 : NW * kSlotBytes);
   // a warp's end-of-CTA state [G][D+2] floats reuses the start of its own ring
   // Largest cluster whose merge buffer [cluster][G][D+2] floats fits the rings.
@@ -325,7 +325,6 @@ __global__ void __launch_bounds__(NWARPS * 32,
   constexpr bool kSplit = Tl::kSplit;
   unsigned char* kst = smem + warp * Tl::kWarpBytes;  // [S][T] K rows, kRowStride apart
   unsigned char* vst = kst + (kSplit ? 1 : S) * T * kRowStride;  // [S][T] V rows
-  uint16_t* ps = reinterpret_cast<uint16_t*>(smem + Tl::kPsOff) + warp * 2 * 8 * T;  // [2][8][T]
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Tl::kBarOff) + warp * Tl::kBars;
   // end-of-CTA state of warp w: [G][D+2] floats at the start of w's ring
   auto mslot = [&](int w) {
@@ -505,7 +504,7 @@ __global__ void __launch_bounds__(NWARPS * 32,
         break;
       }
       const int nrows = min(T, row1 - (row0 + (warp + t * NW) * T));
-      wa.qk_softmax(wq_, kst, nrows, a.scale_log2, ps, lane);
+      wa.qk_softmax(wq_, kst, nrows, a.scale_log2, lane);
       __syncwarp();
       fence_proxy_async_smem();
       if (t + 1 < my_tiles) issue_half(t + 1, 0, ja, pa);
@@ -514,7 +513,7 @@ __global__ void __launch_bounds__(NWARPS * 32,
         failed_on_v = true;
         break;
       }
-      wa.pv(vst, nrows, ps, lane);
+      wa.pv(vst, nrows, lane);
       __syncwarp();
       fence_proxy_async_smem();
       if (t + 1 < my_tiles) issue_half(t + 1, 1, ja, pa);
@@ -547,7 +546,7 @@ __global__ void __launch_bounds__(NWARPS * 32,
     const unsigned char* kt = kst + static_cast<size_t>(stage) * T * kRowStride;
     unsigned char* vt = vst + static_cast<size_t>(stage) * T * kRowStride;
 
-    wa.tile(wq_, kt, vt, nrows, a.scale_log2, ps, lane);
+    wa.tile(wq_, kt, vt, nrows, a.scale_log2, lane);
     __syncwarp();
     fence_proxy_async_smem();
     if (t + S < my_tiles) issue(t + S, stage, j0, pg0);

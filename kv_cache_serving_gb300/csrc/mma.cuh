@@ -44,6 +44,20 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
+// Two floats as packed bf16 (lo in the low half: the lower column of an mma
+// fragment pair), round to nearest even.
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// Transpose of an 8x8 b16 matrix held in mma fragment layout (thread t: row
+// t/4, columns 2(t%4) and 2(t%4)+1), across the warp.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
+}
 __device__ __forceinline__ uint16_t f32_to_bf16_rn(float x) {
   uint16_t h;
   asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(h) : "f"(x));

@@ -16,7 +16,8 @@
 //    fma.rn.f32.bf16 (bf16 x bf16 is exact in fp32).
 //  * tensor cores (bf16 q and K, group >= 2): S = K q^T per 16-row block with
 //    mma.sync m16n8k16 (K via ldmatrix, q as the B operand, heads as columns),
-//    then O^T += V^T P with V via ldmatrix.trans and P split into bf16 hi + lo.
+//    then O^T += V^T P with V via ldmatrix.trans and P split into bf16 hi + lo,
+//    moved from the S accumulators into B fragments by movmatrix (no shared memory).
 #pragma once
 
 #include <math.h>
@@ -151,6 +152,9 @@ struct WarpAttn {
   // of heads 2(t%4), 2(t%4)+1 for thread t.
   float m_run[GC], l_run[GC], acc[GC][kMMA ? 1 : kEPL];
   float m2[2], l2[2], oacc[kMMA ? NK : 1][4];
+  // Tensor cores: P of the tile as mma B fragments per 16-row block (hi rows
+  // 0-7, hi rows 8-15, lo rows 0-7, lo rows 8-15), from qk_softmax to pv.
+  uint32_t pb[kMMA ? T / 16 : 1][4];
 
   __device__ __forceinline__ void reset() {
     if constexpr (kMMA) {
@@ -175,11 +179,11 @@ struct WarpAttn {
   }
 
   // Tensor cores, first half of a tile: S = K q^T, the online-softmax update,
-  // and P (bf16 hi + lo) into ps.  Reads kt only.
+  // and P (bf16 hi + lo) as the B fragments of pv.  Reads kt only.
   __device__ __forceinline__ void qk_softmax(const Q& q, const unsigned char* kt, int nrows,
-                                             float scale_log2, uint16_t* ps, int lane) {
+                                             float scale_log2, int lane) {
     static_assert(kMMA, "tensor-core engine");
-    const int g4 = lane >> 2, tig = lane & 3;
+    const int g4 = lane >> 2;
     constexpr int RB = T / 16;
     float sm[RB][4];
 #pragma unroll
@@ -239,24 +243,28 @@ struct WarpAttn {
     for (int mt = 0; mt < NK; ++mt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) oacc[mt][e] *= alpha[e & 1];
-    // P as bf16 hi + lo into the warp's [head][row] buffers (mma B operand)
+    // P as bf16 hi + lo, straight into B fragments: an 8x8 block of S (rows =
+    // K rows, columns = heads) in accumulator layout, transposed across the
+    // warp, is the B fragment (rows 2(t%4), +1 of head t/4)
 #pragma unroll
-    for (int rb = 0; rb < RB; ++rb)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int h = 2 * tig + (e & 1), r = rb * 16 + g4 + 8 * (e >> 1);
-        const float x = sm[rb][e];
-        const uint16_t xh = f32_to_bf16_rn(x);
-        ps[h * T + r] = xh;
-        ps[8 * T + h * T + r] = f32_to_bf16_rn(x - bf16_lo(xh));
-      }
+    for (int rb = 0; rb < RB; ++rb) {
+      const uint32_t h0 = bf16x2_rn(sm[rb][0], sm[rb][1]);  // rows g4
+      const uint32_t h1 = bf16x2_rn(sm[rb][2], sm[rb][3]);  // rows g4 + 8
+      const uint32_t l0 = bf16x2_rn(sm[rb][0] - __uint_as_float(h0 << 16),
+                                    sm[rb][1] - __uint_as_float(h0 & 0xffff0000u));
+      const uint32_t l1 = bf16x2_rn(sm[rb][2] - __uint_as_float(h1 << 16),
+                                    sm[rb][3] - __uint_as_float(h1 & 0xffff0000u));
+      pb[rb][0] = movmatrix_trans(h0);
+      pb[rb][1] = movmatrix_trans(h1);
+      pb[rb][2] = movmatrix_trans(l0);
+      pb[rb][3] = movmatrix_trans(l1);
+    }
   }
 
-  // Tensor cores, second half: O^T += V^T P from ps.  Zeroes V rows past nrows
-  // in place (stale shared memory times p = 0 must stay 0).
-  __device__ __forceinline__ void pv(unsigned char* vt, int nrows, const uint16_t* ps, int lane) {
+  // Tensor cores, second half: O^T += V^T P (P from qk_softmax).  Zeroes V rows
+  // past nrows in place (stale shared memory times p = 0 must stay 0).
+  __device__ __forceinline__ void pv(unsigned char* vt, int nrows, int lane) {
     static_assert(kMMA, "tensor-core engine");
-    const int g4 = lane >> 2, tig = lane & 3;
     constexpr int RB = T / 16;
     // rows past nrows may hold stale shared memory: zero them so 0 * V stays 0
     if (nrows < T) {
@@ -267,10 +275,7 @@ struct WarpAttn {
     __syncwarp();
 #pragma unroll
     for (int kb = 0; kb < RB; ++kb) {
-      const uint32_t* ph = reinterpret_cast<const uint32_t*>(ps + g4 * T + kb * 16 + 2 * tig);
-      const uint32_t* pl =
-          reinterpret_cast<const uint32_t*>(ps + 8 * T + g4 * T + kb * 16 + 2 * tig);
-      const uint32_t bh0 = ph[0], bh1 = ph[4], bl0 = pl[0], bl1 = pl[4];
+      const uint32_t bh0 = pb[kb][0], bh1 = pb[kb][1], bl0 = pb[kb][2], bl1 = pb[kb][3];
       const unsigned char* vrow =
           vt + (kb * 16 + (lane & 7) + 8 * (lane >> 4)) * kRowStride + 16 * ((lane >> 3) & 1);
 #pragma unroll
@@ -284,13 +289,12 @@ struct WarpAttn {
   }
 
   // One tile: rows 0..nrows-1 of kt / vt (kRowStride apart; rows past nrows may
-  // hold stale data).  ps: this warp's [hi, lo][8 heads][T] bf16 scratch (tensor
-  // cores only).  The tensor-core engine zeroes V rows past nrows in place.
+  // hold stale data).  The tensor-core engine zeroes V rows past nrows in place.
   __device__ __forceinline__ void tile(const Q& q, const unsigned char* kt, unsigned char* vt,
-                                       int nrows, float scale_log2, uint16_t* ps, int lane) {
+                                       int nrows, float scale_log2, int lane) {
     if constexpr (kMMA) {
-      qk_softmax(q, kt, nrows, scale_log2, ps, lane);
-      pv(vt, nrows, ps, lane);
+      qk_softmax(q, kt, nrows, scale_log2, lane);
+      pv(vt, nrows, lane);
     } else {
       const int grp = lane >> 3, jl = lane & 7;  // row group, lane in group
       // scores of this lane's rows (rows past nrows hold stale data: masked)
