@@ -413,6 +413,23 @@ __global__ void __launch_bounds__(NW * 32, NW == 2 ? DSA_MQ_MINB2 : DSA_MQ_MINB4
     if (off > W) return false;
     return (msk[(off - 1) >> 5] >> ((off - 1) & 31)) & 1u;
   };
+  // Window rows j0 .. j0+31 (consecutive, all >= P) against query i: bit x set
+  // iff i keeps row j0 + x, i.e. offset o = o0 - x (o0 = i - j0) is 0, or lies in
+  // 1..W with mask bit o-1 set.  E holds offsets lo .. lo+31 (lo = o0 - 31)
+  // ascending, so the answer is E bit-reversed.
+  auto kept_word = [&](int o0) -> uint32_t {
+    const int lo = o0 - 31, sbit = lo - 1;  // mask bit of offset lo
+    const int w = sbit >= 0 ? (sbit >> 5) : -((31 - sbit) >> 5);
+    const int sh = sbit - 32 * w;
+    const uint32_t x0 = (w >= 0 && w < a.mask_words) ? msk[w] : 0u;
+    const uint32_t x1 = (w + 1 >= 0 && w + 1 < a.mask_words) ? msk[w + 1] : 0u;
+    uint32_t e = __funnelshift_r(x0, x1, sh);
+    const int kmin = max(0, 1 - lo), kmax = min(31, W - lo);
+    e = kmin > kmax ? 0u
+                    : e & (kmax == 31 ? 0xffffffffu : (2u << kmax) - 1u) & (0xffffffffu << kmin);
+    if (lo <= 0 && lo >= -31) e |= 1u << (-lo);  // offset 0: the query's own row
+    return __brev(e);
+  };
 
   bool failed = false;
   int k = 0;
@@ -474,6 +491,20 @@ __global__ void __launch_bounds__(NW * 32, NW == 2 ? DSA_MQ_MINB2 : DSA_MQ_MINB4
           for (int c = 0; c < 2; ++c) {
             sc[nt][c] = v0 ? sc[nt][c] * a.scale_log2 : -INFINITY;
             sc[nt][2 + c] = v1 ? sc[nt][2 + c] * a.scale_log2 : -INFINITY;
+          }
+      } else if (p0 >= nA) {
+        // a block of window rows: the kept bits of this thread's two queries as
+        // words (columns past R are rows after i_last: offsets below 0, unset)
+        const int j0 = bstart + (p0 - nA);
+        const uint32_t kw0 = v0 ? kept_word(iq0 - j0) : 0u;
+        const uint32_t kw1 = v1 ? kept_word(iq1 - j0) : 0u;
+#pragma unroll
+        for (int nt = 0; nt < kMqNT; ++nt)
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const int col = nt * 8 + 2 * tig + c;
+            sc[nt][c] = (kw0 >> col) & 1u ? sc[nt][c] * a.scale_log2 : -INFINITY;
+            sc[nt][2 + c] = (kw1 >> col) & 1u ? sc[nt][2 + c] * a.scale_log2 : -INFINITY;
           }
       } else {
 #pragma unroll
