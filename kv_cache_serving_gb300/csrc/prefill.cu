@@ -26,11 +26,13 @@
 // (query, row) pair the query does not keep is masked to -inf before it.
 //
 // Staging: blocks of 32 consecutive row positions, K then V, in a ring of
-// DSA_MQ_STAGES stages shared by the CTA's warps.  Warp 0 fills a stage with one
+// DSA_MQ_STAGES stages shared by the CTA's warps.  The producer of a block (the
+// role rotates: block b is staged by warp b mod NW) fills a stage with one
 // bulk async copy per K row and per V row (completing on the stage's "full"
 // mbarrier with the expected byte count), the rows' page ids held in its
 // registers; every warp arrives on the stage's "empty" mbarrier once its reads
-// are done, and warp 0 refills that stage before it computes the next block.
+// are done, and the next block's producer refills that stage before it computes
+// its own next block.
 // A row in the scanned range that no query of the tile keeps is never read:
 // its slot is zero-filled instead, so skipped rows have no effect even when
 // they hold NaN (0 x NaN would be NaN inside the mma).  Every wait is bounded
@@ -54,7 +56,7 @@ namespace {
 constexpr int kMqBlock = DSA_MQ_BLOCK;    // K/V rows per staged block (16 or 32)
 static_assert(kMqBlock == 16 || kMqBlock == 32, "block rows");
 constexpr int kMqNT = kMqBlock / 8;       // 8-row tiles of S per block
-constexpr int kMqHeld = 3;                // page ids the producer warp holds per lane
+constexpr int kMqHeld = 3;                // page ids every warp holds per lane
 
 template <int D>
 struct MqTiling {
@@ -290,7 +292,7 @@ __global__ void __launch_bounds__(NW * 32, NW == 2 ? DSA_MQ_MINB2 : DSA_MQ_MINB4
   const bf16_t* vg = reinterpret_cast<const bf16_t*>(a.v);
   const int32_t* pt = a.page_table + static_cast<size_t>(b) * a.max_pages;
   // Page slots of the scanned rows: those of the prompt range, then those of
-  // the window range.  The producer warp holds up to 32 * kMqHeld of them (lane
+  // the window range.  Every warp holds up to 32 * kMqHeld of them (lane
   // l: slots l, l + 32, ...), loaded once, so a block's copies wait on no
   // page-table load; longer ranges load their page ids per block.
   const int slotsA = nA > 0 ? ((nA - 1) >> 4) + 1 : 0;
@@ -298,7 +300,7 @@ __global__ void __launch_bounds__(NW * 32, NW == 2 ? DSA_MQ_MINB2 : DSA_MQ_MINB4
   const int nslots = slotsA + (R > nA ? (i_last >> 4) - sB0 + 1 : 0);
   const bool held = nslots <= 32 * kMqHeld;
   int hpg[kMqHeld] = {0, 0, 0};
-  if (warp == 0 && held) {
+  if (held) {
 #pragma unroll
     for (int h = 0; h < kMqHeld; ++h) {
       const int x = lane + 32 * h;
@@ -306,7 +308,7 @@ __global__ void __launch_bounds__(NW * 32, NW == 2 ? DSA_MQ_MINB2 : DSA_MQ_MINB4
     }
   }
 
-  // Warp 0: stage block `blk` into stage s.  32-row blocks: lane l copies the K
+  // The calling warp stages block `blk` into stage s.  32-row blocks: lane l copies the K
   // and V rows of position 32 blk + l; 16-row blocks: lanes 0-15 the K rows and
   // lanes 16-31 the V rows of positions 16 blk + (l % 16).
   auto produce = [&](int blk, int s) {
@@ -365,10 +367,14 @@ __global__ void __launch_bounds__(NW * 32, NW == 2 ? DSA_MQ_MINB2 : DSA_MQ_MINB4
     }
   };
 
-  int produced = 0;
-  if (warp == 0) {
-    for (; produced < S && produced < nblocks; ++produced) produce(kb0 + produced, produced);
-  }
+  // local block kb is staged by warp producer_of(kb); my_last: the last one this warp staged
+  auto producer_of = [&](int kb) { return kb % kMqWarps; };
+  int my_last = -1;
+  for (int kb = 0; kb < S && kb < nblocks; ++kb)
+    if (producer_of(kb) == warp) {
+      produce(kb0 + kb, kb);
+      my_last = kb;
+    }
 
   // This thread's two (query, head) rows of the warp's 16: r0 = g4, r1 = g4 + 8.
   const int pr0 = warp * 16 + g4, pr1 = pr0 + 8;
@@ -435,9 +441,10 @@ __global__ void __launch_bounds__(NW * 32, NW == 2 ? DSA_MQ_MINB2 : DSA_MQ_MINB4
   int k = 0;
   for (; k < nblocks; ++k) {
     const int s = k % S;
-    // warp 0 refills the stage of block k-1 (once every warp is done with it)
-    // before computing block k, so that its copies fly during that work
-    if (warp == 0 && k >= 1 && k - 1 + S < nblocks) {
+    // the producer of block k-1+S refills the stage of block k-1 (once every
+    // warp is done with it) before computing block k, so that its copies fly
+    // during that work
+    if (k >= 1 && k - 1 + S < nblocks && producer_of(k - 1 + S) == warp) {
       const int sp = (k - 1) % S;
       if (!__all_sync(0xffffffffu,
                       mbar_wait(&empty[sp], static_cast<uint32_t>((k - 1) / S) & 1u))) {
@@ -445,7 +452,7 @@ __global__ void __launch_bounds__(NW * 32, NW == 2 ? DSA_MQ_MINB2 : DSA_MQ_MINB4
         break;
       }
       produce(kb0 + k - 1 + S, sp);
-      ++produced;
+      my_last = k - 1 + S;
     }
     if (!__all_sync(0xffffffffu, mbar_wait(&full[s], static_cast<uint32_t>(k / S) & 1u))) {
       failed = true;
@@ -589,10 +596,9 @@ __global__ void __launch_bounds__(NW * 32, NW == 2 ? DSA_MQ_MINB2 : DSA_MQ_MINB4
   }
   if (failed) {
     if (lane == 0) set_error(a.err, DSA_DEV_TIMEOUT);
-    // copies warp 0 issued and nobody waited for: give them a bounded chance to land
-    if (warp == 0)
-      for (int kb = k; kb < produced; ++kb)
-        mbar_wait(&full[kb % S], static_cast<uint32_t>(kb / S) & 1u);
+    // copies this warp issued and nobody waited for: give them a bounded chance to land
+    for (int kb = k; kb <= my_last; ++kb)
+      if (producer_of(kb) == warp) mbar_wait(&full[kb % S], static_cast<uint32_t>(kb / S) & 1u);
     if (nparts == 1) return;
     // a part still arrives (with an empty state), so the unit's count stays whole
     m0 = m1 = -INFINITY;

@@ -218,3 +218,41 @@ def test_prefill_full_size_chunk():
     q, ql = chunk_inputs(w, 32, seed=31, q_len=np.full(w["batch"], 32, np.int32))
     out, lse = run_prefill(bt, q, ql)
     compare(w, q, ql, out, lse)
+
+
+def test_prefill_split_without_lse_and_in_a_graph():
+    """Split units with lse = NULL (the merge writes out only), and the chunk
+    captured in a CUDA graph and replayed: every replay gives the eager call's
+    bits (the arrival counters return to zero inside each replay)."""
+    w = wl.generate(small_cfg(128, 2, batch=4, Lmax=500, Pmax=80, W=120, seed=41))
+    bt = DecodeBatch.from_workload(w)
+    q, ql = chunk_inputs(w, 24, seed=42)
+    dev = bt.device
+    qd, qld = q.to(dev), torch.as_tensor(ql).to(dev)
+    saved = dsa.dsa_get_prefill_split()
+    try:
+        dsa.dsa_set_prefill_split(3)
+        ref, _ = run_prefill(bt, q, ql)
+        out = torch.full(tuple(q.shape), SENTINEL, dtype=torch.float32, device=dev)
+        dsa.dsa_prefill_sparse(bt.dims, qd, bt.k_pages, bt.v_pages, bt.page_table, bt.seq_len,
+                               qld, bt.prompt_len, bt.window, bt.keep_mask, bt.scale, out, None,
+                               bt.ws)
+        torch.cuda.synchronize()
+        assert bt.device_error() == 0
+        assert np.array_equal(out.cpu().numpy().astype(np.float64), ref)
+        stream = torch.cuda.Stream(dev)
+        gout = torch.full(tuple(q.shape), SENTINEL, dtype=torch.float32, device=dev)
+        glse = torch.full(tuple(q.shape[:3]), SENTINEL, dtype=torch.float32, device=dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            dsa.dsa_prefill_sparse(bt.dims, qd, bt.k_pages, bt.v_pages, bt.page_table,
+                                   bt.seq_len, qld, bt.prompt_len, bt.window, bt.keep_mask,
+                                   bt.scale, gout, glse, bt.ws, stream)
+        for _ in range(3):
+            gout.fill_(SENTINEL)
+            g.replay()
+            torch.cuda.synchronize()
+            assert np.array_equal(gout.cpu().numpy().astype(np.float64), ref)
+        assert bt.device_error() == 0
+    finally:
+        dsa.dsa_set_prefill_split(saved)
