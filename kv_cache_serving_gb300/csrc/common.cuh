@@ -114,6 +114,15 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 
+// 2^x by the hardware approximation (ex2.approx.ftz: relative error about
+// 2^-22, subnormal results flushed to zero, 2^-inf = +0), for the online
+// softmax weights and rescale factors.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Bounded wait for phase `parity` of `bar` to complete: false after kWaitLimitNs.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;

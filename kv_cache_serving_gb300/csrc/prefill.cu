@@ -540,18 +540,18 @@ __global__ void __launch_bounds__(NW * 32, NW == 2 ? DSA_MQ_MINB2 : DSA_MQ_MINB4
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
       const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
       // a row with no kept entry yet keeps m = -inf, o = l = 0
-      const float al0 = mn0 == -INFINITY ? 1.f : exp2f(m0 - mn0);
-      const float al1 = mn1 == -INFINITY ? 1.f : exp2f(m1 - mn1);
+      const float al0 = mn0 == -INFINITY ? 1.f : ex2_approx(m0 - mn0);
+      const float al1 = mn1 == -INFINITY ? 1.f : ex2_approx(m1 - mn1);
       const float bs0 = mn0 == -INFINITY ? 0.f : mn0, bs1 = mn1 == -INFINITY ? 0.f : mn1;
       m0 = mn0;
       m1 = mn1;
       float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
       for (int nt = 0; nt < kMqNT; ++nt) {
-        sc[nt][0] = exp2f(sc[nt][0] - bs0);
-        sc[nt][1] = exp2f(sc[nt][1] - bs0);
-        sc[nt][2] = exp2f(sc[nt][2] - bs1);
-        sc[nt][3] = exp2f(sc[nt][3] - bs1);
+        sc[nt][0] = ex2_approx(sc[nt][0] - bs0);
+        sc[nt][1] = ex2_approx(sc[nt][1] - bs0);
+        sc[nt][2] = ex2_approx(sc[nt][2] - bs1);
+        sc[nt][3] = ex2_approx(sc[nt][3] - bs1);
         ps0 += sc[nt][0] + sc[nt][1];
         ps1 += sc[nt][2] + sc[nt][3];
       }
