@@ -64,11 +64,11 @@ FALLBACK_HBM_GBS = 6800.0
 # decode-kernel sources whose digest is `digest` and are reported as null
 # otherwise.
 NCU_TRAFFIC = {
-    "digest": "b8de7c8cbc921ce9",
+    "digest": "9a2a3e14a7f0ac77",
     "bytes": {
-        "mixed-serving-gqa4": 167993600,
-        "janus-pro-7b-like-32x32": 316262912,
-        "llamagen-xl-like-24x24": 21441024,
+        "mixed-serving-gqa4": 168025344,
+        "janus-pro-7b-like-32x32": 316282880,
+        "llamagen-xl-like-24x24": 21440768,
         "emu3-8b-like-90x90-gqa4": 3280896,
     },
 }
