@@ -410,6 +410,15 @@ def prefill_inputs(w, q_len, device):
     return q, ql
 
 
+def prefill_order(w, q_len):
+    """Requests by decreasing rows their chunk scans (prompt rows, then the
+    window range of the chunk's queries), ties by index."""
+    L, P, W = (np.asarray(w[k], np.int64) for k in ("seq_len", "prompt_len", "window"))
+    n = np.minimum(q_len, L)
+    nA = np.minimum(P, L)
+    return np.argsort(-(nA + np.minimum(W + n, L - nA)), kind="stable")
+
+
 def prefill_bytes(w, q_len, dense=False):
     """Algorithmic bytes of one chunk: the union over the chunk's queries of their
     kept rows (each read once per (request, kv head)), q, out and lse; and the
@@ -453,6 +462,9 @@ def measure_prefill(name, q_len, K, W, device, stream, peak):
                                                frac=cfg.top_mass_frac)
         bt.set_keep_mask(w["keep_mask"])
     q, ql = prefill_inputs(w, q_len, device)
+    order = torch.as_tensor(prefill_order(w, q_len), dtype=torch.int32, device=device)
+    order_d = torch.as_tensor(np.argsort(-w["seq_len"], kind="stable"), dtype=torch.int32,
+                              device=device)
     out = torch.empty(tuple(q.shape), dtype=torch.float32, device=device)
     lse = torch.empty(tuple(q.shape[:3]), dtype=torch.float32, device=device)
     by, flops = prefill_bytes(w, q_len)
@@ -471,12 +483,14 @@ def measure_prefill(name, q_len, K, W, device, stream, peak):
     def sparse(k):
         kp, vp = pools[k % R]
         dsa.dsa_prefill_sparse(bt.dims, q, kp, vp, bt.page_table, bt.seq_len, ql, bt.prompt_len,
-                               bt.window, bt.keep_mask, bt.scale, out, lse, bt.ws, stream)
+                               bt.window, bt.keep_mask, bt.scale, out, lse, bt.ws, stream,
+                               request_order=order)
 
     def dense(k):
         kp, vp = pools[k % R]
         dsa.dsa_prefill_sparse(dd, q, kp, vp, bt.page_table, bt.seq_len, ql, bt.prompt_len,
-                               win_d, mask_d, bt.scale, out, lse, ws_d, stream)
+                               win_d, mask_d, bt.scale, out, lse, ws_d, stream,
+                               request_order=order_d)
 
     for k in range(W):
         sparse(k)
@@ -492,7 +506,8 @@ def measure_prefill(name, q_len, K, W, device, stream, peak):
     bt.check("prefill timed")
     res = {
         "call": "dsa_prefill_sparse: the last q_len rows of every request as query tokens, "
-                "each over its own kept set",
+                "each over its own kept set; requests handed to the GPU by decreasing scanned "
+                "rows (dense: by length)",
         "workload": cfg.name, "batch": w["batch"], "q_len": q_len,
         "us": 1e6 * ts, "query_tokens_per_s": w["batch"] * q_len / ts,
         "bytes": by, "gbs": by / ts / 1e9, "frac_hbm": by / ts / 1e9 / peak,
@@ -1000,10 +1015,12 @@ def run_profile(args):
     q4, ql = prefill_inputs(w, 32, device)
     o4 = torch.empty(tuple(q4.shape), dtype=torch.float32, device=device)
     l4 = torch.empty(tuple(q4.shape[:3]), dtype=torch.float32, device=device)
+    porder = torch.as_tensor(prefill_order(w, 32), dtype=torch.int32, device=device)
 
     def prefill_call():
         dsa.dsa_prefill_sparse(bt.dims, q4, bt.k_pages, bt.v_pages, bt.page_table, bt.seq_len, ql,
-                               bt.prompt_len, bt.window, bt.keep_mask, bt.scale, o4, l4, bt.ws)
+                               bt.prompt_len, bt.window, bt.keep_mask, bt.scale, o4, l4, bt.ws,
+                               request_order=porder)
     call = {"prefill": prefill_call, "index": bt.build_index, "sparse": bt.decode_sparse,
             "masked": lambda: bt.decode_sparse_masked(request_order=order),
             "dense": bt.decode_dense,

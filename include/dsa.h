@@ -343,6 +343,12 @@ dsa_status dsa_attention_mass(const dsa_dims* dims, const void* q, const void* k
  *   k_pages, v_pages, page_table, seq_len, prompt_len, window, keep_mask
  *                     as in dsa_decode_sparse_masked (K/V bf16)
  *   q_len             [batch] int32 (device), 0 <= q_len[b] <= min(L_b, max_q)
+ *   request_order     [batch] int32 (device), or NULL: the order in which
+ *                     requests are handed to the GPU, as in
+ *                     dsa_decode_sparse_masked; the requests that scan the most
+ *                     rows first (about min(P,L) + min(W + q_len, L - min(P,L)))
+ *                     shortens the tail of a batch with mixed lengths.  An entry
+ *                     outside 0..batch-1 sets DSA_DEV_BAD_ORDER and is skipped.
  *   scale             softmax scale, normally 1/sqrt(head_dim)
  *   out   (out)       [batch][max_q][hq][head_dim] float32; slots t >= q_len[b]
  *                     are not written
@@ -360,8 +366,9 @@ dsa_status dsa_prefill_sparse(const dsa_dims* dims, int32_t max_q, const void* q
                               const void* k_pages, const void* v_pages,
                               const int32_t* page_table, const int32_t* seq_len,
                               const int32_t* q_len, const int32_t* prompt_len,
-                              const int32_t* window, const uint32_t* keep_mask, float scale,
-                              float* out, float* lse, void* ws, void* stream);
+                              const int32_t* window, const uint32_t* keep_mask,
+                              const int32_t* request_order, float scale, float* out, float* lse,
+                              void* ws, void* stream);
 
 /*
  * dsa_evict_pages -- unmap the pages no later decode step can read, and hand

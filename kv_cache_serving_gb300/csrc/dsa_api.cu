@@ -571,8 +571,9 @@ dsa_status dsa_prefill_sparse(const dsa_dims* dims, int32_t max_q, const void* q
                               const void* k_pages, const void* v_pages,
                               const int32_t* page_table, const int32_t* seq_len,
                               const int32_t* q_len, const int32_t* prompt_len,
-                              const int32_t* window, const uint32_t* keep_mask, float scale,
-                              float* out, float* lse, void* ws, void* stream) {
+                              const int32_t* window, const uint32_t* keep_mask,
+                              const int32_t* request_order, float scale, float* out, float* lse,
+                              void* ws, void* stream) {
   const dsa_status st = check_dims(dims);
   if (st != DSA_OK) return st;
   if (max_q < 0 || !q || !k_pages || !v_pages || !page_table || !seq_len || !q_len ||
@@ -595,6 +596,7 @@ dsa_status dsa_prefill_sparse(const dsa_dims* dims, int32_t max_q, const void* q
   a.prompt_len = prompt_len;
   a.window = window;
   a.keep_mask = keep_mask;
+  a.order = request_order;
   a.batch = dims->batch;
   a.hq = dims->hq;
   a.hkv = dims->hkv;

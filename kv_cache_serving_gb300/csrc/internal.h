@@ -102,6 +102,7 @@ struct MultiLaunch {
   const int32_t* prompt_len;
   const int32_t* window;
   const uint32_t* keep_mask;  // [batch][hkv][mask_words]
+  const int32_t* order;       // [batch] request handed to the GPU at each position, or null
   int32_t batch, hq, hkv, head_dim, max_pages, num_pages, max_window, mask_words, max_q;
   int32_t q_tiles;            // CTAs along the query axis of one (request, kv head)
   int32_t warps;              // warps per CTA (multi_warps)

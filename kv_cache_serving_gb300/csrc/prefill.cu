@@ -43,8 +43,13 @@
 #include "internal.h"
 #include "mma.cuh"
 
+// Stages of the 2-warp and the 4-warp builds (the 4-warp CTAs are fewer per
+// SM, limited by registers, and have shared memory for more stages).
 #ifndef DSA_MQ_STAGES
 #define DSA_MQ_STAGES 2
+#endif
+#ifndef DSA_MQ_STAGES4
+#define DSA_MQ_STAGES4 4
 #endif
 
 namespace dsa {
@@ -58,12 +63,12 @@ static_assert(kMqBlock == 16 || kMqBlock == 32, "block rows");
 constexpr int kMqNT = kMqBlock / 8;       // 8-row tiles of S per block
 constexpr int kMqHeld = 3;                // page ids every warp holds per lane
 
-template <int D>
+template <int D, int NW>
 struct MqTiling {
   static constexpr int kRowBytes = D * 2;              // bf16
   static constexpr int kStride = kRowBytes + 16;       // padded: conflict-free ldmatrix
   static constexpr int kStage = 2 * kMqBlock * kStride;  // K rows, then V rows
-  static constexpr int kS = DSA_MQ_STAGES;
+  static constexpr int kS = NW == 4 ? DSA_MQ_STAGES4 : DSA_MQ_STAGES;
   static constexpr int kBarOff = kS * kStage;          // full[kS], empty[kS]
   static constexpr int kMaskOff = kBarOff + 2 * kS * 8;
   static int smem(int mask_words) { return kMaskOff + mask_words * 4; }
@@ -215,7 +220,7 @@ __device__ __forceinline__ void multi_merge_parts(const MultiLaunch& a, unsigned
 template <int D, int G, int NW>
 __global__ void __launch_bounds__(NW * 32, NW == 2 ? DSA_MQ_MINB2 : DSA_MQ_MINB4)
     multi_kernel(const MultiLaunch a) {
-  using Tl = MqTiling<D>;
+  using Tl = MqTiling<D, NW>;
   constexpr int kMqWarps = NW;      // warps per CTA, 16 (query, head) rows each
   constexpr int QT = 16 * NW / G;   // query tokens per CTA
   constexpr int NKD = D / 16;       // k-steps of S = q K^T
@@ -237,7 +242,12 @@ __global__ void __launch_bounds__(NW * 32, NW == 2 ? DSA_MQ_MINB2 : DSA_MQ_MINB4
     nparts = a.split;
   }
   const int qtile = unit % a.q_tiles, hk = (unit / a.q_tiles) % a.hkv;
-  const int b = unit / (a.q_tiles * a.hkv);
+  const int bpos = unit / (a.q_tiles * a.hkv);  // position in the request order
+  const int b = a.order != nullptr ? __ldg(a.order + bpos) : bpos;
+  if (static_cast<unsigned>(b) >= static_cast<unsigned>(a.batch)) {
+    if (qtile == 0 && hk == 0 && part == 0 && threadIdx.x == 0) set_error(a.err, DSA_DEV_BAD_ORDER);
+    return;
+  }
   const int L = a.seq_len[b], n = a.q_len[b], P = a.prompt_len[b], W = a.window[b];
   int code = 0;
   if (L < 1 || L > a.max_pages * kPage) code = DSA_DEV_BAD_SEQ_LEN;
@@ -665,7 +675,7 @@ void plan_split(MultiLaunch& a, int64_t units, int64_t slots, int rows) {
 
 template <int D, int G, int NW>
 cudaError_t launch_multi_nw(MultiLaunch a, cudaStream_t s) {
-  const int smem = MqTiling<D>::smem(a.mask_words);
+  const int smem = MqTiling<D, NW>::smem(a.mask_words);
   auto kern = multi_kernel<D, G, NW>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;

@@ -77,7 +77,7 @@ def _load():
         "dsa_decode_sparse_masked_io": ([ctypes.POINTER(dsa_host_io), D, P, P, P, P, P, P, P, P,
                                          P, P, P, F32, P, P, P, P], I32),
         "dsa_decode_dense": ([D, P, P, P, P, P, F32, P, P, P, P], I32),
-        "dsa_prefill_sparse": ([D, I32, P, P, P, P, P, P, P, P, P, F32, P, P, P, P], I32),
+        "dsa_prefill_sparse": ([D, I32, P, P, P, P, P, P, P, P, P, P, F32, P, P, P, P], I32),
         "dsa_attention_mass": ([D, P, P, P, P, P, P, P, I32, I32, F32, P, P, P, P], I32),
         "dsa_decode_plan": ([D, I32, ctypes.POINTER(I32), ctypes.POINTER(I32),
                              ctypes.POINTER(I32), ctypes.POINTER(I32), ctypes.POINTER(I32)],
@@ -353,10 +353,12 @@ def dsa_decode_dense(dims, q, k_pages, v_pages, page_table, seq_len, scale, out,
 
 
 def dsa_prefill_sparse(dims, q, k_pages, v_pages, page_table, seq_len, q_len, prompt_len,
-                       window, keep_mask, scale, out, lse, ws, stream=None):
+                       window, keep_mask, scale, out, lse, ws, stream=None, request_order=None):
     """Several query tokens per request under the mask: q is [batch, max_q, hq,
     head_dim] bf16; the q_len[b] query tokens of request b are its last cache
-    rows.  out [batch, max_q, hq, head_dim] f32, lse [batch, max_q, hq] f32 or None."""
+    rows.  out [batch, max_q, hq, head_dim] f32, lse [batch, max_q, hq] f32 or None;
+    request_order [batch] int32 (device) or None: the order requests are handed
+    to the GPU."""
     if q.dim() != 4:
         raise ValueError("q must be [batch, max_q, hq, head_dim]")
     _check(_load().dsa_prefill_sparse(
@@ -364,7 +366,8 @@ def dsa_prefill_sparse(dims, q, k_pages, v_pages, page_table, seq_len, q_len, pr
         _ptr(k_pages, torch.bfloat16, "k_pages"), _ptr(v_pages, torch.bfloat16, "v_pages"),
         _ptr(page_table, _I32, "page_table"), _ptr(seq_len, _I32, "seq_len"),
         _ptr(q_len, _I32, "q_len"), _ptr(prompt_len, _I32, "prompt_len"),
-        _ptr(window, _I32, "window"), _ptr(keep_mask, _MASK, "keep_mask"), float(scale),
+        _ptr(window, _I32, "window"), _ptr(keep_mask, _MASK, "keep_mask"),
+        _ptr(request_order, _I32, "request_order"), float(scale),
         _ptr(out, torch.float32, "out"), _ptr(lse, torch.float32, "lse"), _ptr(ws),
         _stream(stream)), "dsa_prefill_sparse")
 

@@ -136,7 +136,7 @@ def test_prefill_call_checks_before_launch():
 
     def call(dims=D, max_q=4, q_len=fake):
         return lib.dsa_prefill_sparse(dims, max_q, fake, fake, fake, fake, fake, q_len, fake,
-                                      fake, fake, 0.1, fake, None, fake, None)
+                                      fake, fake, None, 0.1, fake, None, fake, None)
     assert call(q_len=None) == dsa.DSA_ERR_INVALID_ARG
     assert call(max_q=-1) == dsa.DSA_ERR_INVALID_ARG
     assert call(max_q=0) == dsa.DSA_OK

@@ -256,3 +256,37 @@ def test_prefill_split_without_lse_and_in_a_graph():
         assert bt.device_error() == 0
     finally:
         dsa.dsa_set_prefill_split(saved)
+
+
+def test_prefill_request_order():
+    """A request order (a permutation) only changes which CTA runs which unit:
+    results within the oracle's bars; an entry outside 0..batch-1 is flagged
+    (DSA_DEV_BAD_ORDER) and the other requests are still computed."""
+    w = wl.generate(small_cfg(64, 4, batch=6, Lmax=500, Pmax=90, W=96, seed=51))
+    bt = DecodeBatch.from_workload(w)
+    q, ql = chunk_inputs(w, 20, seed=52)
+    dev = bt.device
+    perm = np.random.default_rng(53).permutation(w["batch"]).astype(np.int32)
+
+    def run(order):
+        out = torch.full(tuple(q.shape), SENTINEL, dtype=torch.float32, device=dev)
+        lse = torch.full(tuple(q.shape[:3]), SENTINEL, dtype=torch.float32, device=dev)
+        dsa.dsa_prefill_sparse(bt.dims, q.to(dev), bt.k_pages, bt.v_pages, bt.page_table,
+                               bt.seq_len, torch.as_tensor(ql).to(dev), bt.prompt_len, bt.window,
+                               bt.keep_mask, bt.scale, out, lse, bt.ws,
+                               request_order=torch.as_tensor(order).to(dev))
+        torch.cuda.synchronize()
+        return out.cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
+
+    out, lse = run(perm)
+    assert bt.device_error() == 0
+    compare(w, q, ql, out, lse)
+    bad = perm.copy()
+    skipped = int(bad[2])
+    bad[2] = w["batch"] + 3
+    out2, lse2 = run(bad)
+    assert bt.device_error() == 9               # DSA_DEV_BAD_ORDER
+    dsa.dsa_clear_device_error(bt.ws)
+    keep = [b for b in range(w["batch"]) if b != skipped]
+    assert np.array_equal(out2[keep], out[keep])  # the same units in the same CTAs
+    assert (out2[skipped] == SENTINEL).all()
