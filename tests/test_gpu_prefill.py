@@ -209,15 +209,34 @@ def test_prefill_split_parts(D, G, parts):
         dsa.dsa_set_prefill_split(saved)
 
 
-def test_prefill_full_size_chunk():
-    """The benchmark's chunk: the full Janus-like batch, 32 query tokens per
-    request, in the automatic split (the units of the last, partial wave of
-    resident CTAs split and merged in the kernel): every slot vs the oracle."""
-    w = wl.generate(wl.WORKLOADS["janus-pro-7b"])
+@pytest.mark.parametrize("name,qmax", [("janus-pro-7b", 32), ("mixed-serving", 16)])
+def test_prefill_full_size_chunk(name, qmax):
+    """The benchmark's launch at full size: every request's last qmax rows as
+    its chunk, requests in the benchmark's order (decreasing scanned rows), the
+    automatic split (the units of a last, partial wave of resident CTAs split and
+    merged in the kernel): every slot vs the oracle."""
+    import bench
+    w = wl.generate(wl.WORKLOADS[name])
+    mask = None
+    if w["keep_mask"] is None:
+        _, om = oracle.mass(w, r_local=2, r_diag=2)
+        mask = wl.top_mass_keep_mask(om.reshape(w["batch"], w["hq"], -1), w["window"], w["hkv"],
+                                     w["mask_words"], band=w["config"].band,
+                                     frac=w["config"].top_mass_frac)
+        w["keep_mask"] = mask
     bt = DecodeBatch.from_workload(w)
-    q, ql = chunk_inputs(w, 32, seed=31, q_len=np.full(w["batch"], 32, np.int32))
-    out, lse = run_prefill(bt, q, ql)
-    compare(w, q, ql, out, lse)
+    q, ql = chunk_inputs(w, qmax, seed=31,
+                         q_len=np.minimum(qmax, w["seq_len"]).astype(np.int32))
+    order = torch.as_tensor(bench.prefill_order(w, qmax), dtype=torch.int32, device=bt.device)
+    dev = bt.device
+    out = torch.full(tuple(q.shape), SENTINEL, dtype=torch.float32, device=dev)
+    lse = torch.full(tuple(q.shape[:3]), SENTINEL, dtype=torch.float32, device=dev)
+    dsa.dsa_prefill_sparse(bt.dims, q.to(dev), bt.k_pages, bt.v_pages, bt.page_table, bt.seq_len,
+                           torch.as_tensor(ql).to(dev), bt.prompt_len, bt.window, bt.keep_mask,
+                           bt.scale, out, lse, bt.ws, request_order=order)
+    torch.cuda.synchronize()
+    assert bt.device_error() == 0
+    compare(w, q, ql, out.cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64))
 
 
 def test_prefill_split_without_lse_and_in_a_graph():
