@@ -471,6 +471,18 @@ dsa_status dsa_set_sparse_cluster(int32_t ctas);
 int32_t dsa_get_sparse_cluster(void);
 
 /*
+ * dsa_prefill_plan -- the launch dsa_prefill_sparse makes for dims and max_q on
+ * the current device under the current dsa_set_prefill_split setting: warps per
+ * CTA (2 or 4), units (query tiles x kv heads x requests), the units run whole
+ * (one CTA each; the later ones are split), the parts of each split unit, the
+ * resident CTAs per SM of the kernel and the CTAs launched.  Host-only (no
+ * kernel is enqueued); any output pointer may be NULL.  The same argument
+ * checks as dsa_prefill_sparse; DSA_ERR_CUDA if the device cannot be queried.
+ */
+dsa_status dsa_prefill_plan(const dsa_dims* dims, int32_t max_q, int32_t* warps, int32_t* units,
+                            int32_t* whole, int32_t* parts, int32_t* ctas_per_sm, int32_t* ctas);
+
+/*
  * dsa_set_prefill_split -- process-wide tuning of dsa_prefill_sparse (not in
  * the paper: a scheduling choice).  A unit of that call (a tile of query tokens
  * of one request and kv head) normally runs in one CTA.  With parts >= 2 every

@@ -378,6 +378,43 @@ dsa_status decode_launch(const dsa_dims* d, int mode, const Plan& plan, const vo
   return from_cuda(launch_merge(a, mode, s));
 }
 
+// The shape of a multi-query launch on dims (every field but the pointers),
+// or DSA_ERR_UNSUPPORTED when its work items do not fit a 1-D grid.
+dsa_status multi_shape(const dsa_dims* dims, int32_t max_q, MultiLaunch* out) {
+  MultiLaunch a{};
+  a.batch = dims->batch;
+  a.hq = dims->hq;
+  a.hkv = dims->hkv;
+  a.head_dim = dims->head_dim;
+  a.max_pages = dims->max_pages_per_req;
+  a.num_pages = dims->num_pages;
+  a.max_window = dims->max_window;
+  a.mask_words = dims->mask_words;
+  a.max_q = max_q;
+  a.warps = multi_warps(max_q, dims->hq / dims->hkv);
+  const int per_cta = multi_queries_per_cta(a.warps, dims->hq / dims->hkv);
+  a.q_tiles = static_cast<int32_t>(ceil_div(max_q, per_cta));
+  // work items (units times parts) index a 1-D grid
+  if (static_cast<int64_t>(a.q_tiles) * dims->hkv * dims->batch * kMultiMaxParts > INT32_MAX)
+    return DSA_ERR_UNSUPPORTED;
+  a.split_setting = g_prefill_split.load(std::memory_order_relaxed);
+  a.part_rows_cap = static_cast<int64_t>(partials_region(dims) / ((dims->head_dim + 2) * sizeof(float)));
+  a.count_cap = kMultiCounters;
+  a.sms = sm_count();
+  *out = a;
+  return DSA_OK;
+}
+
+dsa_status multi_dims_ok(const dsa_dims* dims, int32_t max_q) {
+  const dsa_status st = check_dims(dims);
+  if (st != DSA_OK) return st;
+  if (max_q < 0) return DSA_ERR_INVALID_ARG;
+  if (dims->q_dtype != DSA_BF16 || dims->kv_dtype != DSA_BF16 ||
+      dims->max_window > kMultiMaxWindow)
+    return DSA_ERR_UNSUPPORTED;
+  return DSA_OK;
+}
+
 }  // namespace
 }  // namespace dsa
 
@@ -582,11 +619,12 @@ dsa_status dsa_prefill_sparse(const dsa_dims* dims, int32_t max_q, const void* q
   if (!(scale == scale) || !aligned(ws, 256) || !aligned(q, 16) || !aligned(k_pages, 16) ||
       !aligned(v_pages, 16) || !aligned(out, 8) || !aligned(lse, 4))
     return DSA_ERR_INVALID_ARG;
-  if (dims->q_dtype != DSA_BF16 || dims->kv_dtype != DSA_BF16 ||
-      dims->max_window > kMultiMaxWindow)
-    return DSA_ERR_UNSUPPORTED;
+  const dsa_status sm = multi_dims_ok(dims, max_q);
+  if (sm != DSA_OK) return sm;
   if (dims->batch == 0 || max_q == 0) return DSA_OK;
   MultiLaunch a{};
+  const dsa_status ss = multi_shape(dims, max_q, &a);
+  if (ss != DSA_OK) return ss;
   a.q = q;
   a.k = k_pages;
   a.v = v_pages;
@@ -597,32 +635,34 @@ dsa_status dsa_prefill_sparse(const dsa_dims* dims, int32_t max_q, const void* q
   a.window = window;
   a.keep_mask = keep_mask;
   a.order = request_order;
-  a.batch = dims->batch;
-  a.hq = dims->hq;
-  a.hkv = dims->hkv;
-  a.head_dim = dims->head_dim;
-  a.max_pages = dims->max_pages_per_req;
-  a.num_pages = dims->num_pages;
-  a.max_window = dims->max_window;
-  a.mask_words = dims->mask_words;
-  a.max_q = max_q;
-  a.warps = multi_warps(max_q, dims->hq / dims->hkv);
-  const int per_cta = multi_queries_per_cta(a.warps, dims->hq / dims->hkv);
-  a.q_tiles = static_cast<int32_t>(ceil_div(max_q, per_cta));
-  // work items (units times parts) index a 1-D grid
-  if (static_cast<int64_t>(a.q_tiles) * dims->hkv * dims->batch * kMultiMaxParts > INT32_MAX)
-    return DSA_ERR_UNSUPPORTED;
   a.scale_log2 = scale * kLog2e;
   a.out = out;
   a.lse = lse;
   a.err = err_word(ws);
-  a.split_setting = g_prefill_split.load(std::memory_order_relaxed);
   a.part = partials(ws);
-  a.part_rows_cap = static_cast<int64_t>(partials_region(dims) / ((dims->head_dim + 2) * sizeof(float)));
   a.part_count = multi_count_region(dims, ws);
-  a.count_cap = kMultiCounters;
-  a.sms = sm_count();
   return from_cuda(launch_multi(a, static_cast<cudaStream_t>(stream)));
+}
+
+dsa_status dsa_prefill_plan(const dsa_dims* dims, int32_t max_q, int32_t* warps, int32_t* units,
+                            int32_t* whole, int32_t* parts, int32_t* ctas_per_sm, int32_t* ctas) {
+  const dsa_status st = multi_dims_ok(dims, max_q);
+  if (st != DSA_OK) return st;
+  MultiPlan p{multi_warps(max_q, dims->hq / dims->hkv), 0, 0, 1, 0, 0};
+  if (dims->batch > 0 && max_q > 0) {
+    MultiLaunch a{};
+    const dsa_status ss = multi_shape(dims, max_q, &a);
+    if (ss != DSA_OK) return ss;
+    const cudaError_t e = launch_multi(a, nullptr, &p, false);
+    if (e != cudaSuccess) return from_cuda(e);
+  }
+  if (warps) *warps = p.warps;
+  if (units) *units = p.units;
+  if (whole) *whole = p.n_whole;
+  if (parts) *parts = p.parts;
+  if (ctas_per_sm) *ctas_per_sm = p.ctas_per_sm;
+  if (ctas) *ctas = p.ctas;
+  return DSA_OK;
 }
 
 dsa_status dsa_decode_plan(const dsa_dims* dims, int32_t mode, int32_t* chunk,

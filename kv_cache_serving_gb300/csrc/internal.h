@@ -148,7 +148,15 @@ cudaError_t launch_compact(const CompactLaunch& a, cudaStream_t s);
 // Several query tokens per request: bf16 q and KV only.  Warps per CTA for a
 // call (2 when max_q x group fits 32 (query, head) rows, else 4) and the query
 // tokens a CTA of that many warps holds.
-cudaError_t launch_multi(const MultiLaunch& a, cudaStream_t s);
+// The launch of a multi-query call: warps per CTA, units, units run whole,
+// parts of each later unit, resident CTAs per SM, CTAs launched.
+struct MultiPlan {
+  int32_t warps, units, n_whole, parts, ctas_per_sm, ctas;
+};
+// Plans the launch (into *plan when not null) and launches it unless `launch`
+// is false (then nothing is enqueued).
+cudaError_t launch_multi(const MultiLaunch& a, cudaStream_t s, MultiPlan* plan = nullptr,
+                         bool launch = true);
 int multi_warps(int max_q, int group);
 int multi_queries_per_cta(int warps, int group);
 // Largest max_window of the multi-query call (its mask words sit in shared memory).

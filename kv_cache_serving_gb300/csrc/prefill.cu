@@ -674,7 +674,7 @@ void plan_split(MultiLaunch& a, int64_t units, int64_t slots, int rows) {
 }
 
 template <int D, int G, int NW>
-cudaError_t launch_multi_nw(MultiLaunch a, cudaStream_t s) {
+cudaError_t launch_multi_nw(MultiLaunch a, cudaStream_t s, MultiPlan* plan, bool launch) {
   const int smem = MqTiling<D, NW>::smem(a.mask_words);
   auto kern = multi_kernel<D, G, NW>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -685,13 +685,18 @@ cudaError_t launch_multi_nw(MultiLaunch a, cudaStream_t s) {
   const int64_t units = static_cast<int64_t>(a.q_tiles) * a.hkv * a.batch;
   plan_split(a, units, static_cast<int64_t>(per_sm) * a.sms, 16 * NW);
   const int64_t items = a.n_whole + (units - a.n_whole) * a.split;
+  if (plan != nullptr)
+    *plan = MultiPlan{NW, static_cast<int32_t>(units), a.n_whole, a.split, per_sm,
+                      static_cast<int32_t>(items)};
+  if (!launch) return cudaSuccess;
   return launch_pdl(kern, dim3(static_cast<unsigned>(items)), dim3(NW * 32),
                     static_cast<size_t>(smem), s, a);
 }
 
 template <int D, int G>
-cudaError_t launch_multi_one(const MultiLaunch& a, cudaStream_t s) {
-  return a.warps == 2 ? launch_multi_nw<D, G, 2>(a, s) : launch_multi_nw<D, G, 4>(a, s);
+cudaError_t launch_multi_one(const MultiLaunch& a, cudaStream_t s, MultiPlan* plan, bool launch) {
+  return a.warps == 2 ? launch_multi_nw<D, G, 2>(a, s, plan, launch)
+                      : launch_multi_nw<D, G, 4>(a, s, plan, launch);
 }
 
 }  // namespace
@@ -700,10 +705,10 @@ int multi_warps(int max_q, int group) { return static_cast<int64_t>(max_q) * gro
 
 int multi_queries_per_cta(int warps, int group) { return 16 * warps / group; }
 
-cudaError_t launch_multi(const MultiLaunch& a, cudaStream_t s) {
+cudaError_t launch_multi(const MultiLaunch& a, cudaStream_t s, MultiPlan* plan, bool launch) {
   const int g = a.hq / a.hkv;
 #define DSA_MQ_CASE(DD, GG) \
-  if (a.head_dim == DD && g == GG) return launch_multi_one<DD, GG>(a, s);
+  if (a.head_dim == DD && g == GG) return launch_multi_one<DD, GG>(a, s, plan, launch);
   DSA_MQ_CASE(64, 1)
   DSA_MQ_CASE(64, 2)
   DSA_MQ_CASE(64, 4)

@@ -89,6 +89,7 @@ def _load():
         "dsa_graph_destroy": ([P], I32),
         "dsa_set_sparse_cluster": ([I32], I32),
         "dsa_get_sparse_cluster": ([], I32),
+        "dsa_prefill_plan": ([D, I32] + [ctypes.POINTER(I32)] * 6, I32),
         "dsa_set_prefill_split": ([I32], I32),
         "dsa_get_prefill_split": ([], I32),
         "dsa_get_device_error": ([P, P, ctypes.POINTER(I32)], I32),
@@ -405,6 +406,15 @@ def dsa_set_sparse_cluster(ctas: int) -> None:
 
 def dsa_get_sparse_cluster() -> int:
     return int(_load().dsa_get_sparse_cluster())
+
+
+def dsa_prefill_plan(dims, max_q: int):
+    """(warps per CTA, units, units run whole, parts per split unit, resident CTAs
+    per SM, CTAs launched) of dsa_prefill_sparse on the current device."""
+    v = [ctypes.c_int32() for _ in range(6)]
+    _check(_load().dsa_prefill_plan(ctypes.byref(dims), int(max_q),
+                                    *[ctypes.byref(x) for x in v]), "dsa_prefill_plan")
+    return tuple(x.value for x in v)
 
 
 def dsa_set_prefill_split(parts: int) -> None:

@@ -146,6 +146,13 @@ def test_prefill_call_checks_before_launch():
     assert call(dims=ctypes.byref(wide)) == dsa.DSA_ERR_UNSUPPORTED
     empty = dsa.make_dims(0, 8, 2, 128, 10, 4, 96, 3, 50, "bf16", "bf16")
     assert call(dims=ctypes.byref(empty)) == dsa.DSA_OK
+    # the plan query makes the same argument checks before it asks the device
+    assert lib.dsa_prefill_plan(D, -1, None, None, None, None, None, None) == dsa.DSA_ERR_INVALID_ARG
+    assert (lib.dsa_prefill_plan(ctypes.byref(f32), 4, None, None, None, None, None, None)
+            == dsa.DSA_ERR_UNSUPPORTED)
+    w = ctypes.c_int32(-1)
+    assert lib.dsa_prefill_plan(D, 0, ctypes.byref(w), None, None, None, None, None) == dsa.DSA_OK
+    assert w.value == 2
 
 
 def test_host_io_call_checks_before_copying():

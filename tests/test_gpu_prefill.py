@@ -228,6 +228,18 @@ def test_prefill_full_size_chunk(name, qmax):
     q, ql = chunk_inputs(w, qmax, seed=31,
                          q_len=np.minimum(qmax, w["seq_len"]).astype(np.int32))
     order = torch.as_tensor(bench.prefill_order(w, qmax), dtype=torch.int32, device=bt.device)
+    warps, units, whole, parts, per_sm, ctas = dsa.dsa_prefill_plan(bt.dims, qmax)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    slots = per_sm * sms
+    assert units == w["batch"] * w["hkv"] * -(-qmax * (w["hq"] // w["hkv"]) // (16 * warps))
+    assert ctas == whole + (units - whole) * parts
+    # the units of a last partial wave run split into up to 4 parts (one wave of parts)
+    rem = units % slots if units >= slots else units
+    want = min(4, slots // rem) if rem else 1
+    if want >= 2:
+        assert (whole, parts) == (units - rem, want), (units, slots, whole, parts)
+    else:
+        assert (whole, parts) == (units, 1), (units, slots, whole, parts)
     dev = bt.device
     out = torch.full(tuple(q.shape), SENTINEL, dtype=torch.float32, device=dev)
     lse = torch.full(tuple(q.shape[:3]), SENTINEL, dtype=torch.float32, device=dev)
