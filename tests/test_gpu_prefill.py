@@ -321,3 +321,15 @@ def test_prefill_request_order():
     keep = [b for b in range(w["batch"]) if b != skipped]
     assert np.array_equal(out2[keep], out[keep])  # the same units in the same CTAs
     assert (out2[skipped] == SENTINEL).all()
+
+
+@pytest.mark.parametrize("qmax,warps", [(16, 2), (30, 4), (70, 4)])
+def test_prefill_each_warp_count(qmax, warps):
+    """The 2- and 4-warp builds (chunks of up to 32 and of more (query, head)
+    rows per kv head) against the oracle, the last over three query tiles."""
+    w = wl.generate(small_cfg(128, 2, batch=5, Lmax=700, Pmax=120, W=150, seed=60 + qmax))
+    bt = DecodeBatch.from_workload(w)
+    assert dsa.dsa_prefill_plan(bt.dims, qmax)[0] == warps
+    q, ql = chunk_inputs(w, qmax, seed=61)
+    out, lse = run_prefill(bt, q, ql)
+    compare(w, q, ql, out, lse)
