@@ -66,3 +66,22 @@ def test_top_mass_rule_hand_example():
     # group mean: 5 -> .3, 9 -> .2, 12 -> .2, 13 -> .2, 14 -> .2  => 5, then 9, 12, 13
     m = wl.top_mass_keep_mask(om, np.array([16]), hkv=1, words=1, band=2, frac=0.375)
     assert wl.bits_to_offsets(m[0, 0]) == [1, 2, 5, 9, 12, 13]
+
+
+def test_prefill_request_order_by_scanned_rows():
+    """The benchmark's multi-query order: a permutation of the batch by
+    decreasing rows a chunk scans -- the prompt rows min(P, L), then the window
+    range of its queries min(W + q_len, L - min(P, L)) -- ties by index."""
+    import bench
+    w = {"seq_len": np.array([10, 300, 300, 50, 5000, 40]),
+         "prompt_len": np.array([20, 100, 100, 0, 10, 40]),
+         "window": np.array([8, 64, 64, 16, 96, 8])}
+    # scanned rows with q_len 16: 10, 100+80, 100+80, 0+32, 10+112, 40+0
+    assert bench.prefill_order(w, 16).tolist() == [1, 2, 4, 5, 3, 0]
+    big = wl.generate(wl.scaled(wl.WORKLOADS["mixed-serving"], batch=40), with_kv=False)
+    order = bench.prefill_order(big, 16)
+    assert sorted(order.tolist()) == list(range(40))
+    L, P, W = big["seq_len"], big["prompt_len"], big["window"]
+    nA = np.minimum(P, L)
+    rows = (nA + np.minimum(W + np.minimum(16, L), L - nA))[order]
+    assert (np.diff(rows) <= 0).all()
