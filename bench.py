@@ -64,12 +64,12 @@ FALLBACK_HBM_GBS = 6800.0
 # decode-kernel sources whose digest is `digest` and are reported as null
 # otherwise.
 NCU_TRAFFIC = {
-    "digest": "3d3d6ed5565f29b0",
+    "digest": "364987f01e71c6af",
     "bytes": {
-        "mixed-serving-gqa4": 167961088,
-        "janus-pro-7b-like-32x32": 316392448,
-        "llamagen-xl-like-24x24": 21440256,
-        "emu3-8b-like-90x90-gqa4": 3281920,
+        "mixed-serving-gqa4": 167968768,
+        "janus-pro-7b-like-32x32": 316389376,
+        "llamagen-xl-like-24x24": 21441024,
+        "emu3-8b-like-90x90-gqa4": 3281408,
     },
 }
 
