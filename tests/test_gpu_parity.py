@@ -246,6 +246,15 @@ def test_small_batch_build(name, batch):
     run_both(w, mask=mask)
 
 
+def test_batch_past_the_schedule_limit():
+    """1100 requests: more than dsa_build_index schedules (1024), so no schedule
+    is written and dsa_decode_sparse runs in batch order; every path still
+    matches the oracle on every pair (many short units, several waves)."""
+    w = wl.generate(small_cfg(128, 4, "bf16", batch=1100, hkv=1, Lmax=120, Pmax=30, W=48,
+                              seed=77))
+    run_both(w)
+
+
 def test_request_schedule_changes_no_bits():
     """dsa_build_index leaves a longest-first request schedule in the workspace;
     dsa_decode_sparse on it must give the bits it gives on a workspace without
