@@ -333,3 +333,23 @@ def test_prefill_each_warp_count(qmax, warps):
     q, ql = chunk_inputs(w, qmax, seed=61)
     out, lse = run_prefill(bt, q, ql)
     compare(w, q, ql, out, lse)
+
+
+def test_prefill_forced_split_clipped_by_the_workspace():
+    """Every unit asked to split in 8 on the full Janus-like chunk: the
+    workspace's partial rows hold only some of them, so the last units run
+    split and the rest whole (the plan says which); every slot vs the oracle."""
+    w = wl.generate(wl.WORKLOADS["janus-pro-7b"])
+    bt = DecodeBatch.from_workload(w)
+    q, ql = chunk_inputs(w, 32, seed=71, q_len=np.full(w["batch"], 32, np.int32))
+    saved = dsa.dsa_get_prefill_split()
+    try:
+        dsa.dsa_set_prefill_split(8)
+        warps, units, whole, parts, per_sm, ctas = dsa.dsa_prefill_plan(bt.dims, 32)
+        assert parts == 8 and 0 < whole < units, (units, whole, parts)
+        rows_cap = (dsa.dsa_workspace_size(bt.dims) - 256) // ((w["head_dim"] + 2) * 4)
+        assert (units - whole) * parts * 16 * warps <= rows_cap
+        out, lse = run_prefill(bt, q, ql)
+        compare(w, q, ql, out, lse)
+    finally:
+        dsa.dsa_set_prefill_split(saved)
