@@ -219,9 +219,11 @@ __global__ void __launch_bounds__(NWARPS * 32,
   // Page ids of this lane's rows in the warp's first S+1 tiles, loaded
   // speculatively with the request's sizes (they need only b and the CTA's
   // first row): a row that is its own kept index -- every dense row, and the
-  // prompt rows of a kept set -- then needs no dependent page-table load
-  // before its first copy.
-  constexpr bool kSpec = MODE != kRowsList;
+  // prompt rows of a kept set, and of a kept list outside the split-staged
+  // builds (the ids are used only where the loaded kept index equals the row;
+  // on the split-staged build the kept-list step measured slower with them) --
+  // then needs no dependent page-table load before its first copy.
+  constexpr bool kSpec = MODE != kRowsList || !Tl::kSplit;
   const int spec_row0 = a.cluster > 1 ? (c == 0 ? 0 : -1) : c * a.chunk;
   int spec_pg[Tl::S + 1];
 #pragma unroll
