@@ -64,11 +64,11 @@ FALLBACK_HBM_GBS = 6800.0
 # decode-kernel sources whose digest is `digest` and are reported as null
 # otherwise.
 NCU_TRAFFIC = {
-    "digest": "364987f01e71c6af",
+    "digest": "9f7d16093e2dc428",
     "bytes": {
-        "mixed-serving-gqa4": 167968768,
-        "janus-pro-7b-like-32x32": 316389376,
-        "llamagen-xl-like-24x24": 21441024,
+        "mixed-serving-gqa4": 167971840,
+        "janus-pro-7b-like-32x32": 316328960,
+        "llamagen-xl-like-24x24": 21440768,
         "emu3-8b-like-90x90-gqa4": 3281408,
     },
 }
